@@ -1,0 +1,161 @@
+"""The C ABI on the host, no GPU: the library loads, exports every function the
+header declares, and rejects bad arguments with the documented status codes
+before making any CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_router.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from top_gating_expert_row_gb300 import build
+
+    build.build()
+    import top_gating_expert_row_gb300 as m
+
+    return m
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(moe_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for want in ("moe_router_fwd", "moe_router_bwd", "moe_aux_scores_fwd", "moe_aux_scores_bwd", "moe_sort",
+                 "moe_sort_capacity", "moe_sort_workspace_bytes", "moe_router_fused_fwd_sort",
+                 "moe_router_fused_workspace_bytes", "moe_router_strerror"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r" T (\w+)$", out, re.M))
+    missing = [n for n in _declared() if n not in exported]
+    assert not missing, missing
+    cdll = ctypes.CDLL(lib.LIB_PATH)
+    for n in _declared():
+        assert getattr(cdll, n) is not None
+
+
+def test_binding_wraps_every_symbol(lib):
+    for n in _declared():
+        assert callable(getattr(lib, n)), n
+
+
+def test_strerror(lib):
+    for code in range(5):
+        assert lib.strerror(code).startswith("MR_")
+    assert "unknown" in lib.strerror(99)
+
+
+def _p(lib, **kw):
+    base = dict(T=4, E=64, topk=4)
+    base.update(kw)
+    return lib.RouterParams(**base)
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def _fwd(lib, p, logits=FAKE, probs=FAKE):
+    cp = p.c()
+    return lib._lib.moe_router_fwd(ctypes.byref(cp), logits, probs, None, None, None, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(E=0), 1), (dict(T=-1), 1), (dict(topk=0), 1), (dict(topk=65), 1),
+    (dict(score_fn=2), 1), (dict(in_dtype=5), 1), (dict(n_shared=4), 1), (dict(n_shared=-1), 1),
+    (dict(n_group=3, topk_group=1, score_fn=1), 1),           # E % n_group != 0
+    (dict(n_group=4, topk_group=5, score_fn=1), 1),           # topk_group > n_group
+    (dict(n_group=4, topk_group=3, score_fn=1), 1),           # k_r % topk_group != 0
+    (dict(n_group=32, topk_group=1, topk=4, score_fn=1), 1),  # k_r/topk_group > E/n_group
+    (dict(T=1 << 20, E=2048), 1),                             # T*E > INT_MAX
+    (dict(E=4096, topk=8), 2),                                # beyond the register-resident width
+    (dict(E=512, topk=300), 2),                               # k_r beyond MR_MAX_TOPK
+    (dict(n_group=64, topk_group=2, E=128, score_fn=1), 2),   # more groups than lanes
+    (dict(E=256, topk=32, n_group=2, topk_group=2, score_fn=1), 2),  # 16 keys per group score
+    (dict(n_group=4, topk_group=2), 2),                       # softmax with groups
+])
+def test_fwd_rejects(lib, kw, code):
+    assert _fwd(lib, _p(lib, **kw)) == code
+
+
+def test_fwd_rejects_bias_with_softmax_and_missing_pointers(lib):
+    p = _p(lib)
+    cp = p.c()
+    cp.bias = FAKE
+    assert lib._lib.moe_router_fwd(ctypes.byref(cp), FAKE, FAKE, None, None, None, None, None) == 2
+    assert _fwd(lib, _p(lib), logits=None) == 1
+    assert _fwd(lib, _p(lib), probs=None) == 1  # no output at all
+    assert lib._lib.moe_router_fwd(None, FAKE, FAKE, None, None, None, None, None) == 1
+
+
+def test_zero_tokens_is_a_no_op(lib):
+    assert _fwd(lib, _p(lib, T=0)) == 0
+    cp = _p(lib, T=0).c()
+    assert lib._lib.moe_router_bwd(ctypes.byref(cp), FAKE, FAKE, FAKE, FAKE, None) == 0
+    assert lib._lib.moe_aux_scores_fwd(0, 64, 4, 0, 0, FAKE, FAKE, None, None) == 0
+    assert lib._lib.moe_aux_scores_bwd(0, 64, 0, FAKE, FAKE, FAKE, None) == 0
+
+
+def test_bwd_and_aux_reject(lib):
+    cp = _p(lib).c()
+    assert lib._lib.moe_router_bwd(ctypes.byref(cp), None, FAKE, FAKE, FAKE, None) == 1
+    assert lib._lib.moe_router_bwd(ctypes.byref(cp), FAKE, FAKE, None, FAKE, None) == 1
+    cp = _p(lib, E=3000).c()
+    assert lib._lib.moe_router_bwd(ctypes.byref(cp), FAKE, FAKE, FAKE, FAKE, None) == 2
+    assert lib._lib.moe_aux_scores_fwd(4, 64, 65, 0, 0, FAKE, FAKE, None, None) == 1
+    assert lib._lib.moe_aux_scores_fwd(4, 64, 4, 0, 0, FAKE, None, None, None) == 1
+    assert lib._lib.moe_aux_scores_bwd(4, 64, 3, FAKE, FAKE, FAKE, None) == 1
+
+
+def test_sort_sizes_and_rejects(lib):
+    assert lib.moe_sort_capacity(16, 2, 8, 4) == 32 + 8 * 3
+    assert lib.moe_sort_capacity(16384, 9, 385, 64) == 147456 + 385 * 63
+    assert lib.moe_sort_capacity(1, 8, 256, 32) == 8 + 8 * 31
+    assert lib.moe_sort_workspace_bytes(16384, 9, 385, 64) >= 385 * 4
+    assert lib.moe_sort_workspace_bytes(4, 2, 8, 0) == 0
+    s = lib._lib.moe_sort
+    args = [FAKE, FAKE, 4, 2, 8, 4, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None, None]
+
+    def call(**over):
+        a = list(args)
+        pos = dict(idx=0, T=2, topk=3, E_tot=4, bm=5, ids=6, eids=8, npp=9, ws=10, wsb=11)
+        for k, v in over.items():
+            a[pos[k]] = v
+        return s(*a)
+
+    assert call(T=-1) == 1 and call(topk=0) == 1 and call(E_tot=0) == 1 and call(bm=0) == 1
+    assert call(ids=None) == 1 and call(eids=None) == 1 and call(npp=None) == 1 and call(ws=None) == 1
+    assert call(idx=None) == 1
+    assert call(wsb=0) == 1                       # workspace too small
+    assert call(E_tot=5000) == 2                  # beyond MR_MAX_SORT_EXPERTS
+    assert call(T=1 << 28, topk=16) == 1          # T*topk >= INT_MAX
+
+
+def test_fused_rejects(lib):
+    cp = _p(lib, T=64).c()
+    f = lib._lib.moe_router_fused_fwd_sort
+    assert f(ctypes.byref(cp), FAKE, 0, None, None, FAKE, FAKE, FAKE, FAKE, None, 0, None) == 1
+    assert f(ctypes.byref(cp), FAKE, 8, None, None, None, FAKE, FAKE, FAKE, None, 0, None) == 1
+    # above the one-launch size a workspace is needed
+    assert lib.moe_router_fused_workspace_bytes(_p(lib, T=64), 8) > 0
+    assert f(ctypes.byref(cp), FAKE, 8, None, None, FAKE, FAKE, FAKE, FAKE, None, 0, None) == 1
+    assert lib.moe_router_fused_workspace_bytes(_p(lib, T=16), 8) == 0
+
+
+def test_set_topk_path(lib):
+    assert lib._lib.moe_router_set_topk_path(-1, 0) == 1
+    assert lib._lib.moe_router_set_topk_path(8, 3) == 1
+    assert lib._lib.moe_router_set_topk_path(8, 0) == 0
+    assert lib._lib.moe_router_expf(None, None, -1, None) == 1
+    assert lib._lib.moe_router_expf(None, None, 0, None) == 0

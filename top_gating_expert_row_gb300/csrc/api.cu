@@ -1,0 +1,410 @@
+// C ABI of the MoE routing library: argument validation (before anything is
+// enqueued), path and grid selection, and the launches. Host checks follow
+// TransformerEngine PR 3012 "Hardening" (T*E <= INT_MAX, topk in [1, E],
+// topk % group_topk == 0) plus this library's own limits.
+#include <climits>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe_router.h"
+#include "internal.h"
+
+namespace mr {
+
+// ---- launch configuration helpers -------------------------------------------------------------
+
+namespace {
+struct OccEntry {
+    const void* func;
+    size_t smem;
+    int device;
+    int blocks;
+};
+std::mutex g_occ_mu;
+OccEntry g_occ[128];
+int g_occ_n = 0;
+
+struct SmemEntry {
+    const void* func;
+    int device;
+    size_t bytes;
+};
+SmemEntry g_smem[128];
+int g_smem_n = 0;
+
+int g_sm_count[64] = {0};
+}  // namespace
+
+int persistent_grid(const void* func, int threads, size_t smem, long long units)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    if (dev < 0 || dev >= 64) return -1;
+    if (g_sm_count[dev] == 0) {
+        if (cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return -1;
+    }
+    int blocks = -1;
+    for (int i = 0; i < g_occ_n; ++i)
+        if (g_occ[i].func == func && g_occ[i].smem == smem && g_occ[i].device == dev) blocks = g_occ[i].blocks;
+    if (blocks < 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, func, threads, smem) != cudaSuccess) return -1;
+        if (g_occ_n < 128) g_occ[g_occ_n++] = OccEntry{func, smem, dev, blocks};
+    }
+    if (blocks < 1) return -1;
+    const long long cap = static_cast<long long>(blocks) * g_sm_count[dev];
+    const long long g = units < cap ? units : cap;
+    return static_cast<int>(g < 1 ? 1 : g);
+}
+
+int ensure_smem(const void* func, size_t bytes)
+{
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    for (int i = 0; i < g_smem_n; ++i)
+        if (g_smem[i].func == func && g_smem[i].device == dev && g_smem[i].bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e != cudaSuccess) return e;
+    if (g_smem_n < 128) g_smem[g_smem_n++] = SmemEntry{func, dev, bytes};
+    return cudaSuccess;
+}
+
+// ---- per-(score, dtype) launchers defined in fwd.cu compilations --------------------------------
+
+int launch_fwd_s0_d0(const RouteArgs&, int, bool, cudaStream_t);
+int launch_fwd_s0_d1(const RouteArgs&, int, bool, cudaStream_t);
+int launch_fwd_s1_d0(const RouteArgs&, int, bool, cudaStream_t);
+int launch_fwd_s1_d1(const RouteArgs&, int, bool, cudaStream_t);
+int launch_fused_s0_d0(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
+int launch_fused_s0_d1(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
+int launch_fused_s1_d0(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
+int launch_fused_s1_d1(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
+
+int launch_fwd(int score_fn, int in_dtype, const RouteArgs& a, int nv_idx, bool select, cudaStream_t st)
+{
+    if (score_fn == kSoftmax)
+        return in_dtype ? launch_fwd_s0_d1(a, nv_idx, select, st) : launch_fwd_s0_d0(a, nv_idx, select, st);
+    return in_dtype ? launch_fwd_s1_d1(a, nv_idx, select, st) : launch_fwd_s1_d0(a, nv_idx, select, st);
+}
+
+int launch_fused_decode(int score_fn, int in_dtype, const RouteArgs& a, const SortArgs& s, int nv_idx,
+                        bool select, cudaStream_t st)
+{
+    if (score_fn == kSoftmax)
+        return in_dtype ? launch_fused_s0_d1(a, s, nv_idx, select, st) : launch_fused_s0_d0(a, s, nv_idx, select, st);
+    return in_dtype ? launch_fused_s1_d1(a, s, nv_idx, select, st) : launch_fused_s1_d0(a, s, nv_idx, select, st);
+}
+
+// ---- diagnostics ------------------------------------------------------------------------------
+
+__global__ void k_expf(const float* __restrict__ x, float* __restrict__ y, int n)
+{
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) y[i] = exp_f32(x[i]);
+}
+
+__global__ void k_noop() {}
+
+int launch_expf(const float* x, float* y, int n, cudaStream_t st)
+{
+    const long long blocks = (static_cast<long long>(n) + 255) / 256;
+    const int grid = static_cast<int>(blocks < 4096 ? blocks : 4096);
+    k_expf<<<grid, 256, 0, st>>>(x, y, n);
+    return cudaGetLastError();
+}
+
+int launch_noop(cudaStream_t st)
+{
+    k_noop<<<1, 32, 0, st>>>();
+    return cudaGetLastError();
+}
+
+// ---- top-k path configuration -----------------------------------------------------------------
+
+namespace {
+struct PathConfig {
+    int threshold = 8;
+    int force = 0;  // 0 by threshold, 1 arg-max, 2 threshold-select
+    PathConfig()
+    {
+        if (const char* t = std::getenv("MR_TOPK_SELECT_THRESHOLD")) {
+            const int v = std::atoi(t);
+            if (v >= 0) threshold = v;
+        }
+        if (const char* f = std::getenv("MR_FORCE_PATH")) {
+            if (!std::strcmp(f, "argmax")) force = 1;
+            else if (!std::strcmp(f, "select")) force = 2;
+        }
+    }
+};
+PathConfig g_path;
+
+bool use_select(int k_r) { return g_path.force == 2 || (g_path.force == 0 && k_r >= g_path.threshold); }
+
+int select_stop(int k_r)
+{
+    int s = 2 * k_r > 64 ? 2 * k_r : 64;
+    return (s + 31) & ~31;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int from_cuda(int e) { return e == cudaSuccess ? MR_OK : MR_ECUDA; }
+
+// Validation shared by the forward calls. Returns MR_OK or an error code.
+int check_router(const mr_router_params* p)
+{
+    if (!p) return MR_EINVAL;
+    if (p->T < 0 || p->E < 1 || p->topk < 1 || p->n_shared < 0) return MR_EINVAL;
+    if (p->score_fn != MR_SOFTMAX && p->score_fn != MR_SIGMOID) return MR_EINVAL;
+    if (p->in_dtype != MR_F32 && p->in_dtype != MR_BF16) return MR_EINVAL;
+    const int k_r = p->topk - p->n_shared;
+    if (k_r < 1 || k_r > p->E) return MR_EINVAL;
+    if (static_cast<long long>(p->T) * p->E > INT_MAX) return MR_EINVAL;
+    if (static_cast<long long>(p->T) * p->topk >= INT_MAX) return MR_EINVAL;
+    if (p->n_group < 0) return MR_EINVAL;
+    if (p->n_group > 0) {
+        if (p->E % p->n_group != 0) return MR_EINVAL;
+        if (p->topk_group < 1 || p->topk_group > p->n_group) return MR_EINVAL;
+        if (k_r % p->topk_group != 0) return MR_EINVAL;
+        if (k_r / p->topk_group > p->E / p->n_group) return MR_EINVAL;
+    }
+    if (p->E > MR_MAX_EXPERTS || k_r > MR_MAX_TOPK) return MR_EUNSUPPORTED;
+    if (p->n_group > MR_MAX_GROUPS) return MR_EUNSUPPORTED;
+    if (p->n_group > 0 && k_r / p->topk_group > MR_MAX_GROUP_TOPK) return MR_EUNSUPPORTED;
+    if (p->score_fn == MR_SOFTMAX && (p->bias || p->n_group > 0)) return MR_EUNSUPPORTED;
+    return MR_OK;
+}
+
+RouteArgs route_args(const mr_router_params* p, const void* logits, void* probs, uint8_t* map, float* inter,
+                     int32_t* idx, float* w)
+{
+    RouteArgs a;
+    a.logits = logits;
+    a.bias = p->bias;
+    a.probs = probs;
+    a.map = map;
+    a.inter = inter;
+    a.topk_idx = idx;
+    a.topk_w = w;
+    a.T = p->T;
+    a.E = p->E;
+    a.topk = p->topk;
+    a.n_shared = p->n_shared;
+    a.k_r = p->topk - p->n_shared;
+    a.renorm = p->renorm ? 1 : 0;
+    a.n_group = p->n_group;
+    a.topk_group = p->n_group > 0 ? p->topk_group : 0;
+    a.scaling = p->scaling;
+    a.shared_weight = p->shared_weight;
+    a.stop = select_stop(a.k_r);
+    const uintptr_t in_al = p->in_dtype == MR_BF16 ? 8 : 16;
+    a.vec = (p->E % 4 == 0) && aligned(logits, in_al) && aligned(probs, in_al) && aligned(inter, 16) &&
+            aligned(map, 4) && aligned(p->bias, 16);
+    return a;
+}
+
+size_t sort_ws_bytes(long long N, int E_tot) { return static_cast<size_t>(sort_chunks(N)) * E_tot * 4; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int check_sort(int T, int topk, int E_tot, int block_m)
+{
+    if (T < 0 || topk < 1 || E_tot < 1 || block_m < 1) return MR_EINVAL;
+    const long long N = static_cast<long long>(T) * topk;
+    if (N >= INT_MAX) return MR_EINVAL;
+    const long long nonempty = N < E_tot ? N : E_tot;
+    if (N + nonempty * (block_m - 1) >= INT_MAX) return MR_EINVAL;
+    if (E_tot > MR_MAX_SORT_EXPERTS) return MR_EUNSUPPORTED;
+    return MR_OK;
+}
+}  // namespace
+
+}  // namespace mr
+
+using namespace mr;
+
+extern "C" {
+
+const char* moe_router_strerror(int code)
+{
+    switch (code) {
+        case MR_OK: return "MR_OK: success";
+        case MR_EINVAL: return "MR_EINVAL: invalid argument";
+        case MR_EUNSUPPORTED: return "MR_EUNSUPPORTED: outside the library's supported limits";
+        case MR_ECUDA: return "MR_ECUDA: CUDA launch or query failed";
+        case MR_ERANGE: return "MR_ERANGE: expert id out of range (dropped)";
+    }
+    return "unknown moe_router status";
+}
+
+int moe_router_set_topk_path(int select_threshold, int force_path)
+{
+    if (select_threshold < 0 || force_path < 0 || force_path > 2) return MR_EINVAL;
+    g_path.threshold = select_threshold;
+    g_path.force = force_path;
+    return MR_OK;
+}
+
+int moe_router_fwd(const mr_router_params* p, const void* logits, void* probs, uint8_t* routing_map,
+                   float* intermediate, int32_t* topk_idx, float* topk_w, mr_stream_t stream)
+{
+    int rc = check_router(p);
+    if (rc != MR_OK) return rc;
+    if (!logits) return MR_EINVAL;
+    if (!probs && !routing_map && !intermediate && !topk_idx && !topk_w) return MR_EINVAL;
+    if (p->T == 0) return MR_OK;
+    const RouteArgs a = route_args(p, logits, probs, routing_map, intermediate, topk_idx, topk_w);
+    const int nv = nv_index(p->E);
+    if (nv < 0) return MR_EUNSUPPORTED;
+    return from_cuda(launch_fwd(p->score_fn, p->in_dtype, a, nv, use_select(a.k_r),
+                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_aux_scores_fwd(int T, int E, int topk, int score_fn, int in_dtype, const void* logits, float* scores,
+                       uint8_t* routing_map, mr_stream_t stream)
+{
+    mr_router_params p;
+    std::memset(&p, 0, sizeof p);
+    p.T = T;
+    p.E = E;
+    p.topk = topk;
+    p.score_fn = score_fn;
+    p.in_dtype = in_dtype;
+    p.scaling = 1.0f;
+    int rc = check_router(&p);
+    if (rc != MR_OK) return rc;
+    if (!logits || (!scores && !routing_map)) return MR_EINVAL;
+    if (T == 0) return MR_OK;
+    const RouteArgs a = route_args(&p, logits, nullptr, routing_map, scores, nullptr, nullptr);
+    const int nv = nv_index(E);
+    if (nv < 0) return MR_EUNSUPPORTED;
+    return from_cuda(launch_fwd(score_fn, in_dtype, a, nv, use_select(a.k_r), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_router_bwd(const mr_router_params* p, const float* grad_probs, const float* intermediate,
+                   const uint8_t* routing_map, float* grad_logits, mr_stream_t stream)
+{
+    if (!p || !grad_probs || !intermediate || !routing_map || !grad_logits) return MR_EINVAL;
+    if (p->T < 0 || p->E < 1) return MR_EINVAL;
+    if (p->score_fn != MR_SOFTMAX && p->score_fn != MR_SIGMOID) return MR_EINVAL;
+    if (static_cast<long long>(p->T) * p->E > INT_MAX) return MR_EINVAL;
+    if (p->E > MR_MAX_EXPERTS) return MR_EUNSUPPORTED;
+    if (p->T == 0) return MR_OK;
+    const int nv = nv_index(p->E);
+    const bool vec = p->E % 4 == 0 && aligned(grad_probs, 16) && aligned(intermediate, 16) &&
+                     aligned(grad_logits, 16) && aligned(routing_map, 4);
+    return from_cuda(launch_bwd(p->score_fn, nv, grad_probs, intermediate, routing_map, grad_logits, p->T, p->E,
+                                p->renorm ? 1 : 0, p->scaling, vec, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_aux_scores_bwd(int T, int E, int score_fn, const float* grad_scores, const float* scores,
+                       float* grad_logits, mr_stream_t stream)
+{
+    if (!grad_scores || !scores || !grad_logits) return MR_EINVAL;
+    if (T < 0 || E < 1) return MR_EINVAL;
+    if (score_fn != MR_SOFTMAX && score_fn != MR_SIGMOID) return MR_EINVAL;
+    if (static_cast<long long>(T) * E > INT_MAX) return MR_EINVAL;
+    if (E > MR_MAX_EXPERTS) return MR_EUNSUPPORTED;
+    if (T == 0) return MR_OK;
+    const int nv = nv_index(E);
+    const bool vec = E % 4 == 0 && aligned(grad_scores, 16) && aligned(scores, 16) && aligned(grad_logits, 16);
+    return from_cuda(launch_bwd(score_fn, nv, grad_scores, scores, nullptr, grad_logits, T, E, 0, 1.0f, vec,
+                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_sort_capacity(int T, int topk, int E_tot, int block_m)
+{
+    if (T < 0 || topk < 1 || E_tot < 1 || block_m < 1) return 0;
+    const size_t N = static_cast<size_t>(T) * static_cast<size_t>(topk);
+    const size_t nonempty = N < static_cast<size_t>(E_tot) ? N : static_cast<size_t>(E_tot);
+    return N + nonempty * static_cast<size_t>(block_m - 1);
+}
+
+size_t moe_sort_workspace_bytes(int T, int topk, int E_tot, int block_m)
+{
+    if (check_sort(T, topk, E_tot, block_m) != MR_OK) return 0;
+    return sort_ws_bytes(static_cast<long long>(T) * topk, E_tot);
+}
+
+int moe_sort(const int32_t* topk_idx, const float* topk_w, int T, int topk, int E_tot, int block_m,
+             int32_t* sorted_token_ids, float* sorted_weights, int32_t* expert_ids, int32_t* num_tokens_post_pad,
+             void* workspace, size_t ws_bytes, int32_t* status, mr_stream_t stream)
+{
+    int rc = check_sort(T, topk, E_tot, block_m);
+    if (rc != MR_OK) return rc;
+    if (!sorted_token_ids || !expert_ids || !num_tokens_post_pad || !workspace) return MR_EINVAL;
+    if (T > 0 && !topk_idx) return MR_EINVAL;
+    const long long N = static_cast<long long>(T) * topk;
+    if (ws_bytes < sort_ws_bytes(N, E_tot) || !aligned(workspace, 4)) return MR_EINVAL;
+    return from_cuda(launch_sort(topk_idx, topk_w, static_cast<int>(N), E_tot, block_m, sorted_token_ids,
+                                 sorted_weights, expert_ids, num_tokens_post_pad, static_cast<uint32_t*>(workspace),
+                                 status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_router_fused_workspace_bytes(const mr_router_params* p, int block_m)
+{
+    if (check_router(p) != MR_OK || block_m < 1) return 0;
+    const int nv = nv_index(p->E);
+    if (nv < 0) return 0;
+    if (p->T <= MR_MAX_FUSED_TOKENS && kNvBuckets[nv] <= kFusedMaxNv) return 0;
+    const size_t N = static_cast<size_t>(p->T) * p->topk;
+    return align_up(N * 4, 256) * 2 + sort_ws_bytes(static_cast<long long>(N), p->E + p->n_shared);
+}
+
+int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int block_m, int32_t* topk_idx,
+                              float* topk_w, int32_t* sorted_token_ids, float* sorted_weights, int32_t* expert_ids,
+                              int32_t* num_tokens_post_pad, void* workspace, size_t ws_bytes, mr_stream_t stream)
+{
+    int rc = check_router(p);
+    if (rc != MR_OK) return rc;
+    const int E_tot = p->E + p->n_shared;
+    rc = check_sort(p->T, p->topk, E_tot, block_m);
+    if (rc != MR_OK) return rc;
+    if (!logits || !sorted_token_ids || !expert_ids || !num_tokens_post_pad) return MR_EINVAL;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int nv = nv_index(p->E);
+    if (nv < 0) return MR_EUNSUPPORTED;
+    const int k_r = p->topk - p->n_shared;
+    if (p->T <= MR_MAX_FUSED_TOKENS && kNvBuckets[nv] <= kFusedMaxNv) {
+        RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, topk_idx, topk_w);
+        SortArgs s{sorted_token_ids, sorted_weights, expert_ids, num_tokens_post_pad, E_tot, block_m};
+        const bool sel = use_select(k_r);
+        const int nw = kFusedThreads / 32;
+        const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, sel, a.n_group > 0);
+        const size_t smem = static_cast<size_t>(L.bytes) * nw + fused_sort_smem(p->T * p->topk, E_tot, nw);
+        int dev = 0, maxsm = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return MR_ECUDA;
+        if (smem > static_cast<size_t>(maxsm)) return MR_EUNSUPPORTED;
+        return from_cuda(launch_fused_decode(p->score_fn, p->in_dtype, a, s, nv, sel, st));
+    }
+    const size_t N = static_cast<size_t>(p->T) * p->topk;
+    if (!workspace || ws_bytes < moe_router_fused_workspace_bytes(p, block_m)) return MR_EINVAL;
+    unsigned char* w = static_cast<unsigned char*>(workspace);
+    if (!aligned(w, 4)) return MR_EINVAL;
+    int32_t* idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(w);
+    float* wt = topk_w ? topk_w : reinterpret_cast<float*>(w + align_up(N * 4, 256));
+    uint32_t* sws = reinterpret_cast<uint32_t*>(w + align_up(N * 4, 256) * 2);
+    const RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, idx, wt);
+    int e = launch_fwd(p->score_fn, p->in_dtype, a, nv, use_select(k_r), st);
+    if (e != cudaSuccess) return MR_ECUDA;
+    return from_cuda(launch_sort(idx, wt, static_cast<int>(N), E_tot, block_m, sorted_token_ids, sorted_weights,
+                                 expert_ids, num_tokens_post_pad, sws, nullptr, st));
+}
+
+int moe_router_expf(const float* x, float* y, int n, mr_stream_t stream)
+{
+    if (n < 0 || (n > 0 && (!x || !y))) return MR_EINVAL;
+    if (n == 0) return MR_OK;
+    return from_cuda(launch_expf(x, y, n, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_router_noop(mr_stream_t stream) { return from_cuda(launch_noop(reinterpret_cast<cudaStream_t>(stream))); }
+
+}  // extern "C"

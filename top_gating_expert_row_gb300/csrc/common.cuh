@@ -1,0 +1,183 @@
+// Device helpers shared by the routing kernels: the written fp32 exponential,
+// order-preserving selection keys, warp reductions and row loads/stores.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace mr {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kSoftmax = 0;
+constexpr int kSigmoid = 1;
+
+// ---------------------------------------------------------------------------
+// fp32 exponential, reproducible bit for bit on any IEEE-754 machine.
+//
+// Cody & Waite argument reduction ("Software Manual for the Elementary
+// Functions", 1980) and the degree-7 Taylor polynomial of exp about 0:
+//   n = rint(x * log2 e);  r = (x - n*ln2_hi) - n*ln2_lo;  p = sum_{i<=7} r^i/i!
+//   exp(x) = (p * 2^(n/2)) * 2^(n - n/2)      (n/2 truncates toward zero)
+// ln2_hi is ln 2 cut to 16 fraction bits, so n*ln2_hi is exact; every step is a
+// single correctly rounded fp32 operation written with an explicit _rn
+// intrinsic, so the compiler cannot contract or reorder it. Error: < 1 ulp
+// (the Taylor remainder r^8/8! is under 0.1 ulp for |r| <= ln2/2).
+// x >= 89 -> +inf, x <= -104 -> +0, NaN -> NaN.
+// ---------------------------------------------------------------------------
+constexpr double kLn2 = 0.693147180559945309417232121458176568;
+constexpr float kLog2e = static_cast<float>(1.0 / kLn2);
+constexpr float kLn2Hi = static_cast<float>(static_cast<double>(static_cast<long long>(kLn2 * 65536.0)) / 65536.0);
+constexpr float kLn2Lo = static_cast<float>(kLn2 - static_cast<double>(kLn2Hi));
+
+__device__ __forceinline__ float pow2_normal(int k)  // 2^k, -126 <= k <= 127
+{
+    return __int_as_float((k + 127) << 23);
+}
+
+__device__ __forceinline__ float exp_f32(float x)
+{
+    if (x != x) return x;
+    if (x >= 89.0f) return __int_as_float(0x7f800000);
+    if (x <= -104.0f) return 0.0f;
+    const float nf = rintf(__fmul_rn(x, kLog2e));
+    const int n = __float2int_rn(nf);
+    float r = __fmaf_rn(-nf, kLn2Hi, x);
+    r = __fmaf_rn(-nf, kLn2Lo, r);
+    float p = static_cast<float>(1.0 / 5040.0);
+    p = __fmaf_rn(p, r, static_cast<float>(1.0 / 720.0));
+    p = __fmaf_rn(p, r, static_cast<float>(1.0 / 120.0));
+    p = __fmaf_rn(p, r, static_cast<float>(1.0 / 24.0));
+    p = __fmaf_rn(p, r, static_cast<float>(1.0 / 6.0));
+    p = __fmaf_rn(p, r, 0.5f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    const int n1 = n / 2;
+    const int n2 = n - n1;
+    return __fmul_rn(__fmul_rn(p, pow2_normal(n1)), pow2_normal(n2));
+}
+
+// Logistic function 1 / (1 + exp(-x)) with IEEE add and divide.
+__device__ __forceinline__ float sigmoid_f32(float x)
+{
+    return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_f32(-x)));
+}
+
+// ---------------------------------------------------------------------------
+// Selection keys: a strictly increasing map from fp32 to uint32, so that
+// "larger key" is an unsigned compare. -0 is folded onto +0 (they compare
+// equal as floats) and NaN onto 0, the value reserved for "not a candidate"
+// (padding lanes, experts of dropped groups). Every finite or infinite float
+// maps to a key >= 0x007fffff.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t key_of(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    if (f == 0.0f) u = 0u;
+    const uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (f != f) ? 0u : k;
+}
+
+__device__ __forceinline__ float float_of(uint32_t k)
+{
+    const uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+    return __uint_as_float(u);
+}
+
+// ---------------------------------------------------------------------------
+// Warp reductions (all 32 lanes participate).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+
+// Exclusive prefix sum over lanes.
+__device__ __forceinline__ uint32_t warp_exclusive_scan(uint32_t v, int lane)
+{
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    return incl - v;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt()
+{
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// ---------------------------------------------------------------------------
+// Element access for logits (fp32 or bf16 storage, fp32 compute).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+template <typename InT>
+__device__ __forceinline__ float load_scalar(const InT* p);
+template <>
+__device__ __forceinline__ float load_scalar<float>(const float* p) { return __ldcs(p); }
+template <>
+__device__ __forceinline__ float load_scalar<__nv_bfloat16>(const __nv_bfloat16* p)
+{
+    return bf16_bits_to_f32(__ldcs(reinterpret_cast<const unsigned short*>(p)));
+}
+
+// Four consecutive elements starting at a 4-element-aligned position.
+template <typename InT>
+__device__ __forceinline__ void load4(const InT* p, float (&x)[4]);
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, float (&x)[4])
+{
+    const float4 q = __ldcs(reinterpret_cast<const float4*>(p));
+    x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
+}
+template <>
+__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, float (&x)[4])
+{
+    const uint2 q = __ldcs(reinterpret_cast<const uint2*>(p));
+    x[0] = bf16_bits_to_f32(q.x & 0xffffu); x[1] = bf16_bits_to_f32(q.x >> 16);
+    x[2] = bf16_bits_to_f32(q.y & 0xffffu); x[3] = bf16_bits_to_f32(q.y >> 16);
+}
+
+template <typename OutT>
+__device__ __forceinline__ void store_scalar(OutT* p, float v);
+template <>
+__device__ __forceinline__ void store_scalar<float>(float* p, float v) { *p = v; }
+template <>
+__device__ __forceinline__ void store_scalar<__nv_bfloat16>(__nv_bfloat16* p, float v)
+{
+    *p = __float2bfloat16_rn(v);
+}
+
+template <typename OutT>
+__device__ __forceinline__ void store4(OutT* p, const float (&v)[4]);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, const float (&v)[4])
+{
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const float (&v)[4])
+{
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
+    uint2 q;
+    q.x = *reinterpret_cast<const uint32_t*>(&a);
+    q.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = q;
+}
+
+}  // namespace mr

@@ -1,0 +1,76 @@
+// Host-side interface between the C ABI (api.cu) and the kernel translation
+// units. Not installed; not part of the public header.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "route.cuh"
+
+namespace mr {
+
+constexpr int kFwdThreads = 256;     // 8 warps, one token row per warp at a time
+constexpr int kFusedThreads = 512;   // 16 warps: one per decode token, then the whole CTA sorts
+constexpr int kSortThreads = 512;
+constexpr int kSortChunk = 4096;     // flat (token, slot) pairs per sort CTA
+constexpr int kBwdThreads = 256;
+
+// Register-resident row widths: NV chunks of 128 elements per row (E <= 2304).
+constexpr int kNvBuckets[] = {1, 2, 3, 4, 6, 8, 12, 18};
+constexpr int kNumNv = sizeof(kNvBuckets) / sizeof(kNvBuckets[0]);
+
+// Index into kNvBuckets of the smallest width that holds E experts, or -1.
+inline int nv_index(int E)
+{
+    const int need = (E + 127) / 128;
+    for (int i = 0; i < kNumNv; ++i)
+        if (kNvBuckets[i] >= need) return i;
+    return -1;
+}
+
+// The one-CTA fused decode kernel keeps rows up to this many chunks (E <= 1024).
+constexpr int kFusedMaxNv = 8;
+
+struct SortArgs {
+    int32_t* ids;
+    float* w;
+    int32_t* expert_ids;
+    int32_t* num_post_pad;
+    int E_tot;
+    int block_m;
+};
+
+// Shared-memory bytes of the fused decode kernel after the warp regions.
+inline size_t fused_sort_smem(int N, int E_tot, int nwarps)
+{
+    size_t b = 0;
+    b += static_cast<size_t>(align16(N * 4)) * 2;           // pair ids and weights
+    b += static_cast<size_t>(align16(E_tot * 4));            // counts
+    b += static_cast<size_t>(align16((E_tot + 1) * 4));      // offsets
+    b += static_cast<size_t>(align16(33 * 4));               // scan scratch
+    b += static_cast<size_t>(align16(nwarps * E_tot * 2));   // per-warp counters
+    return b;
+}
+
+// Launch helpers; each returns a cudaError_t value (cudaSuccess on success).
+int launch_fwd(int score_fn, int in_dtype, const RouteArgs& a, int nv_idx, bool select,
+               cudaStream_t st);
+int launch_fused_decode(int score_fn, int in_dtype, const RouteArgs& a, const SortArgs& s,
+                        int nv_idx, bool select, cudaStream_t st);
+int launch_bwd(int score_fn, int nv_idx, const float* g, const float* s, const uint8_t* m,
+               float* dx, int T, int E, int renorm, float scaling, bool vec, cudaStream_t st);
+int launch_sort(const int32_t* idx, const float* w, int N, int E_tot, int block_m, int32_t* ids,
+                float* sw, int32_t* eids, int32_t* npp, uint32_t* ws, int32_t* status,
+                cudaStream_t st);
+int launch_expf(const float* x, float* y, int n, cudaStream_t st);
+int launch_noop(cudaStream_t st);
+
+inline int sort_chunks(long long N) { return N <= 0 ? 1 : static_cast<int>((N + kSortChunk - 1) / kSortChunk); }
+
+// Persistent-grid size: min(units, SMs x resident CTAs) for a kernel.
+int persistent_grid(const void* func, int threads, size_t smem, long long units);
+// Raise a kernel's dynamic shared-memory limit when needed.
+int ensure_smem(const void* func, size_t smem);
+
+}  // namespace mr
