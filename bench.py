@@ -1,0 +1,579 @@
+"""Benchmark of the MoE routing path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one pass of the routing hot path over one batch of synthetic
+router logits, T=8192 tokens x E=2304 experts, topk=36, fp32, softmax:
+router forward (probs, routing_map, intermediate, topk_idx, topk_w), router
+backward, aux-loss scores forward and aux-loss scores backward -- the four
+kernels TransformerEngine PR 3012 reports effective bandwidth for. The metric
+is effective GB/s: the minimum bytes each kernel must move (the page's rule:
+fwd reads logits and writes probs, routing_map and intermediate) over device
+time. Prints ONE JSON line (rank 0).
+
+Also reported in the same line: per-kernel GB/s on the other large-T
+workloads, fused decode route+sort in us/call (eager and CUDA-graph replayed,
+against the launch floor), the prefill route+sort, the end-to-end rate through
+host buffers, the roofline of the dominant kernel and the CPU oracle baseline.
+
+--impl reference times the CPU oracle (the reference for this build) on a
+bounded sample of the same workload and prints the same line shape.
+
+Multi-GPU: one process per GPU (torchrun); every rank routes its own T=8192
+batch (tokens are independent, so there is no collective on the data path);
+value = bytes of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "effective GB/s vs 8 TB/s HBM (T=8192); µs/call fused route+sort at T≤16"
+WORKLOAD = "router fwd+bwd+aux fwd+aux bwd, T=8192 E=2304 topk=36 fp32 softmax"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "router_fwd_T8192_E2304_k36.md")
+PAGE_B300 = {  # TransformerEngine PR 3012 "Performance" (B300 SXM6, fp32, T=8192), context only
+    ("fwd", "softmax", 2304, 36): 964, ("bwd", "softmax", 2304, 36): 2766,
+    ("aux_fwd", "softmax", 2304, 36): 891, ("aux_bwd", "softmax", 2304, 36): 4201,
+    ("fwd", "softmax", 512, 4): 1784, ("fwd", "softmax", 512, 8): 904, ("fwd", "softmax", 512, 22): 924,
+    ("fwd", "softmax", 512, 36): 908, ("bwd", "softmax", 512, 22): 5362, ("aux_fwd", "softmax", 512, 22): 896,
+    ("aux_bwd", "softmax", 512, 22): 6155, ("fwd", "sigmoid", 2304, 36): 798, ("bwd", "sigmoid", 2304, 36): 2274,
+    ("aux_fwd", "sigmoid", 2304, 36): 867, ("aux_bwd", "sigmoid", 2304, 36): 2757,
+}
+
+
+def kernel_bytes(kind: str, T: int, E: int, topk: int, in_bytes: int = 4, compact: bool = True) -> int:
+    """Algorithmic bytes of one launch (page-3 rule; compact outputs added when written)."""
+    n = T * E
+    if kind == "fwd":
+        b = n * (in_bytes + in_bytes + 1 + 4)
+        return b + (T * topk * 8 if compact else 0)
+    if kind == "bwd":
+        return n * (4 + 4 + 1 + 4)
+    if kind == "aux_fwd":
+        return n * (in_bytes + 4 + 1)
+    if kind == "aux_bwd":
+        return n * (4 + 4 + 4)
+    raise ValueError(kind)
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "top_gating_expert_row_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+    if it was taken on the current kernel sources (else None)."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    text = open(PROFILE_TRAFFIC).read()
+    src = traf = None
+    for line in text.splitlines():
+        if line.startswith("kernel_source_hash:"):
+            src = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_launch:"):
+            traf = int(line.split(":", 1)[1].strip())
+    if src != kernel_source_hash():
+        return None
+    return traf
+
+
+# ---------------------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l for (ts, l) in self.lines if t0 - 0.05 <= ts <= t1 + 0.05] or [l for _, l in self.lines[-3:]]
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------------------- ours
+
+
+class Timer:
+    """Per-kernel CUDA events on the launching stream."""
+
+    def __init__(self, stream):
+        self.stream = stream
+        self.pairs = {}
+
+    def around(self, name, fn):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(self.stream)
+        fn()
+        b.record(self.stream)
+        self.pairs.setdefault(name, []).append((a, b))
+
+    def mean_ms(self, name):
+        ps = self.pairs.get(name, [])
+        return sum(a.elapsed_time(b) for a, b in ps) / max(1, len(ps))
+
+
+def make_step(mr, w, dev, stream):
+    """Allocates the step's tensors and returns the list of (name, launch) pairs."""
+    T, E, k = w.T, w.E, w.topk
+    x = w.make_logits().to(dev)
+    g = synth.grad(T, E).to(dev)
+    b = w.make_bias()
+    b = b.to(dev) if b is not None else None
+    f32 = dict(dtype=torch.float32, device=dev)
+    t = dict(x=x, g=g, bias=b, probs=torch.empty(T, E, dtype=x.dtype, device=dev),
+             map=torch.empty(T, E, dtype=torch.uint8, device=dev), inter=torch.empty(T, E, **f32),
+             idx=torch.empty(T, k, dtype=torch.int32, device=dev), w=torch.empty(T, k, **f32),
+             dx=torch.empty(T, E, **f32), scores=torch.empty(T, E, **f32),
+             amap=torch.empty(T, E, dtype=torch.uint8, device=dev), adx=torch.empty(T, E, **f32))
+    p = mr.RouterParams(T=T, E=E, topk=k, score_fn=w.score_fn, in_dtype=w.in_dtype, renorm=w.renorm,
+                        scaling=w.scaling, bias=b)
+    cp = p.c()
+    L = mr._lib
+    s = stream.cuda_stream
+    P = ctypes.byref(cp)
+    ptr = {n: (v.data_ptr() if v is not None else None) for n, v in t.items()}
+
+    def chk(rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what}: {mr.strerror(rc)}")
+
+    launches = [
+        ("fwd", lambda: chk(L.moe_router_fwd(P, ptr["x"], ptr["probs"], ptr["map"], ptr["inter"], ptr["idx"],
+                                             ptr["w"], s), "fwd")),
+        ("bwd", lambda: chk(L.moe_router_bwd(P, ptr["g"], ptr["inter"], ptr["map"], ptr["dx"], s), "bwd")),
+        ("aux_fwd", lambda: chk(L.moe_aux_scores_fwd(T, E, k, w.score_fn, w.in_dtype, ptr["x"], ptr["scores"],
+                                                     ptr["amap"], s), "aux_fwd")),
+        ("aux_bwd", lambda: chk(L.moe_aux_scores_bwd(T, E, w.score_fn, ptr["g"], ptr["scores"], ptr["adx"], s),
+                                "aux_bwd")),
+    ]
+    return launches, t, p
+
+
+def step_bytes(w, kinds=("fwd", "bwd", "aux_fwd", "aux_bwd")) -> dict:
+    ib = 2 if w.in_dtype == synth.BF16 else 4
+    return {kd: kernel_bytes(kd, w.T, w.E, w.topk, ib) for kd in kinds}
+
+
+def time_kernels(mr, w, dev, stream, reps=20, warmup=3) -> dict:
+    launches, _, _ = make_step(mr, w, dev, stream)
+    tm = Timer(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            for _, fn in launches:
+                fn()
+        for _ in range(reps):
+            for name, fn in launches:
+                tm.around(name, fn)
+    torch.cuda.synchronize()
+    out = {}
+    fn_name = "softmax" if w.score_fn == synth.SOFTMAX else "sigmoid"
+    for name, nb in step_bytes(w).items():
+        ms = tm.mean_ms(name)
+        gbs = nb / (ms * 1e-3) / 1e9
+        d = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1)}
+        page = PAGE_B300.get((name, fn_name, w.E, w.topk))
+        if page:
+            d["page_B300_GB/s"] = page
+        out[name] = d
+    return out
+
+
+def decode_latency(mr, dev, stream, n_calls=200) -> dict:
+    """Fused vs unfused decode route+sort (E=256, topk=8, bf16), eager and graph."""
+    L = mr._lib
+    res = {}
+    s = stream.cuda_stream
+
+    def eager(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(20):
+                fn(s)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(n_calls):
+                fn(s)
+            torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / n_calls * 1e6
+
+    def graph(fn):
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(cs):
+            for _ in range(5):
+                fn(cs.cuda_stream)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=cs):
+            for _ in range(n_calls):
+                fn(cs.cuda_stream)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        reps = 10
+        a.record(cs)
+        for _ in range(reps):
+            g.replay()
+        b.record(cs)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / (reps * n_calls)
+
+    noop = lambda st: L.moe_router_noop(st)  # noqa: E731
+    floor = {"eager_us": round(eager(noop), 2), "graph_us": round(graph(noop), 2)}
+    res["launch_floor"] = floor
+    for T in synth.DECODE_TS:
+        w = synth.decode(T)
+        x = w.make_logits().to(dev)
+        p = mr.RouterParams(T=T, E=w.E, topk=w.topk, in_dtype=w.in_dtype, renorm=w.renorm)
+        cp = p.c()
+        P = ctypes.byref(cp)
+        bufs = mr.sort_buffers(T, w.topk, w.E, w.block_m, dev)
+        idx = torch.empty(T, w.topk, dtype=torch.int32, device=dev)
+        wt = torch.empty(T, w.topk, dtype=torch.float32, device=dev)
+        ws = torch.empty(mr.moe_sort_workspace_bytes(T, w.topk, w.E, w.block_m), dtype=torch.uint8, device=dev)
+        a = [bufs[n].data_ptr() for n in ("sorted_token_ids", "sorted_weights", "expert_ids", "num_tokens_post_pad")]
+        xp, ip, wp, wsp, wsn = x.data_ptr(), idx.data_ptr(), wt.data_ptr(), ws.data_ptr(), ws.numel()
+
+        def fused(st):
+            return L.moe_router_fused_fwd_sort(P, xp, w.block_m, ip, wp, a[0], a[1], a[2], a[3], None, 0, st)
+
+        def unfused(st):
+            L.moe_router_fwd(P, xp, None, None, None, ip, wp, st)
+            return L.moe_sort(ip, wp, T, w.topk, w.E, w.block_m, a[0], a[1], a[2], a[3], wsp, wsn, None, st)
+
+        fe, fg = eager(fused), graph(fused)
+        ue, ug = eager(unfused), graph(unfused)
+        res[f"T={T}"] = {"fused_eager_us": round(fe, 2), "fused_graph_us": round(fg, 2),
+                         "unfused_eager_us": round(ue, 2), "unfused_graph_us": round(ug, 2),
+                         "fused_graph_minus_floor_us": round(fg - floor["graph_us"], 2),
+                         "fused_eager_minus_floor_us": round(fe - floor["eager_us"], 2)}
+    return res
+
+
+def prefill_route_sort(mr, dev, stream, reps=20) -> dict:
+    """T=16384, E=384+1 shared, topk=9, bf16 sigmoid + bias, 8 groups keep 4, block_m=64."""
+    w = synth.prefill_grouped()
+    x = w.make_logits().to(dev)
+    b = w.make_bias().to(dev)
+    p = mr.RouterParams(T=w.T, E=w.E, topk=w.topk, score_fn=w.score_fn, in_dtype=w.in_dtype, renorm=w.renorm,
+                        n_group=w.n_group, topk_group=w.topk_group, n_shared=w.n_shared, scaling=w.scaling,
+                        shared_weight=w.shared_weight, bias=b)
+    cp = p.c()
+    P = ctypes.byref(cp)
+    L = mr._lib
+    idx = torch.empty(w.T, w.topk, dtype=torch.int32, device=dev)
+    wt = torch.empty(w.T, w.topk, dtype=torch.float32, device=dev)
+    bufs = mr.sort_buffers(w.T, w.topk, w.E_tot, w.block_m, dev)
+    ws = torch.empty(mr.moe_sort_workspace_bytes(w.T, w.topk, w.E_tot, w.block_m), dtype=torch.uint8, device=dev)
+    a = [bufs[n].data_ptr() for n in ("sorted_token_ids", "sorted_weights", "expert_ids", "num_tokens_post_pad")]
+    s = stream.cuda_stream
+    tm = Timer(stream)
+    route = lambda: L.moe_router_fwd(P, x.data_ptr(), None, None, None, idx.data_ptr(), wt.data_ptr(), s)  # noqa
+    srt = lambda: L.moe_sort(idx.data_ptr(), wt.data_ptr(), w.T, w.topk, w.E_tot, w.block_m, a[0], a[1], a[2],  # noqa
+                             a[3], ws.data_ptr(), ws.numel(), None, s)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            route()
+            srt()
+        for _ in range(reps):
+            tm.around("route", route)
+            tm.around("sort", srt)
+    torch.cuda.synchronize()
+    r_us = tm.mean_ms("route") * 1e3
+    s_us = tm.mean_ms("sort") * 1e3
+    rb = w.T * w.E * 2 + w.T * w.topk * 8 + w.E * 4
+    npp = int(bufs["num_tokens_post_pad"].item())
+    sb = w.T * w.topk * 8 + npp * 8 + (npp // w.block_m) * 4 + 4
+    return {"workload": w.name, "route_us": round(r_us, 2), "sort_us": round(s_us, 2),
+            "route_GB/s": round(rb / (r_us * 1e-6) / 1e9, 1), "sort_GB/s": round(sb / (s_us * 1e-6) / 1e9, 1),
+            "route_plus_sort_us": round(r_us + s_us, 2), "num_tokens_post_pad": npp}
+
+
+def e2e_rate(mr, w, dev, stream, steps=5) -> dict:
+    """The same step through the C ABI with host buffers: every step copies the
+    inputs from pinned host memory and reads every output back."""
+    launches, t, _ = make_step(mr, w, dev, stream)
+    host_in = {n: t[n].cpu().pin_memory() for n in ("x", "g")}
+    outs = ("probs", "map", "inter", "idx", "w", "dx", "scores", "amap", "adx")
+    host_out = {n: torch.empty(t[n].shape, dtype=t[n].dtype).pin_memory() for n in outs}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def one():
+        for n, h in host_in.items():
+            t[n].copy_(h, non_blocking=True)
+        for _, fn in launches:
+            fn()
+        for n in outs:
+            host_out[n].copy_(t[n], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        one()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            one()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    nb = sum(step_bytes(w).values())
+    return {"value": round(nb / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------------------------------- CPU oracle
+
+
+def oracle_step_sample(w, rows: int) -> tuple[float, int, str]:
+    """Times the oracle over `rows` token rows of the step's workload; returns
+    (seconds, algorithmic bytes of the sample, description)."""
+    import oracle
+
+    oracle.build()
+    x = w.make_logits()[:rows].float().numpy()
+    g = synth.grad(w.T, w.E)[:rows].double().numpy()
+    t0 = time.perf_counter()
+    o = oracle.router_fwd(x, w.topk, w.score_fn, w.renorm, 0, 0, 0, w.scaling, 1.0, None)
+    oracle.router_bwd(g, o["intermediate"], o["routing_map"], w.score_fn, w.renorm, w.scaling)
+    a = oracle.aux_scores_fwd(x, w.topk, w.score_fn)
+    oracle.aux_scores_bwd(g, a["scores"], w.score_fn)
+    dt = time.perf_counter() - t0
+    sub = synth.Workload(w.name, rows, w.E, w.topk, w.score_fn, w.in_dtype)
+    nb = sum(step_bytes(sub).values())
+    return dt, nb, f"{rows} of {w.T} token rows of the step (fwd+bwd+aux fwd+aux bwd), single-threaded C oracle"
+
+
+def cpu_baseline(w, rows: int, reps: int = 3) -> dict:
+    runs = [oracle_step_sample(w, rows) for _ in range(reps)]
+    dt = statistics.median(r[0] for r in runs)
+    nb, desc = runs[0][1], runs[0][2]
+    return {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{desc}; median of {reps} runs", "seconds": round(dt, 3)}
+
+
+# ---------------------------------------------------------------------------------------- main
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = synth.large_e_softmax()
+    # rows per step sized so that warmup + steps take about args.ref_seconds
+    t64, _, _ = oracle_step_sample(w, 64)
+    per_step = args.ref_seconds / max(1, args.warmup + args.steps)
+    rows = int(max(8, min(w.T, 64 * per_step / max(t64, 1e-6))))
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt, nb, desc = oracle_step_sample(w, rows)
+        if i >= args.warmup:
+            times.append(dt)
+    dt = sum(times) / len(times)
+    value = nb / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "T": w.T, "E": w.E, "topk": w.topk, "score_fn": "softmax",
+                       "sample_rows_per_step": rows},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--only", choices=["all", "step"], default="all",
+                    help="step: the timed step only (used for profiling captures)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=8192, help="oracle sample size (token rows)")
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="reference arm: CPU time budget for warmup + steps")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    ws, rank, local = dist_env()
+    import top_gating_expert_row_gb300 as mr
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the routing path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.Stream(device=dev)
+    w = synth.large_e_softmax()
+    launches, _, _ = make_step(mr, w, dev, stream)
+    nbytes = step_bytes(w)
+    tm = Timer(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for _, fn in launches:
+                fn()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(args.steps):
+            for name, fn in launches:
+                tm.around(name, fn)
+        end.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    t_wall1 = time.time()
+    clocks = sampler.stop(t_wall0, t_wall1)
+    elapsed_ms = start.elapsed_time(end)
+    if ws > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    ms_per_step = elapsed_ms / args.steps
+    total_bytes = sum(nbytes.values()) * args.steps * ws
+    value = total_bytes / (elapsed_ms * 1e-3) / 1e9
+
+    pk = peaks()
+    per_kernel = {}
+    for name, nb in nbytes.items():
+        ms = tm.mean_ms(name)
+        per_kernel[name] = {"us": round(ms * 1e3, 2), "GB/s": round(nb / (ms * 1e-3) / 1e9, 1),
+                            "frac_of_peak": round(nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
+                            "page_B300_GB/s": PAGE_B300.get((name, "softmax", w.E, w.topk))}
+    dom = max(per_kernel, key=lambda n: per_kernel[n]["us"])
+    dom_ms = tm.mean_ms(dom)
+    achieved = nbytes[dom] / (dom_ms * 1e-3) / 1e9
+    traffic = profiled_traffic() if dom == "fwd" else None
+    roofline = {"kernel": {"fwd": "k_router_fwd", "bwd": "k_router_bwd", "aux_fwd": "k_router_fwd (aux scores)",
+                           "aux_bwd": "k_router_bwd (aux scores)"}[dom],
+                "bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 3), "peak_source": pk["source"] + " (hbm_gbs)",
+                "traffic": traffic, "algorithmic_bytes": nbytes[dom]}
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "T": w.T, "E": w.E, "topk": w.topk, "score_fn": "softmax",
+                       "kernels_per_step": [n for n, _ in launches], "bytes_per_step": sum(nbytes.values()),
+                       "l2": "no flush; inputs larger than L2 (each step touches ~565 MB against 129 MB of L2)",
+                       "parallelism": f"replicas x{ws} (tokens are independent; no collective)"},
+            "roofline": roofline, "per_kernel": per_kernel,
+            "gpu_launches": len(launches) * args.steps, "clocks": clocks}
+    if args.only == "all":
+        line["e2e"] = e2e_rate(mr, w, dev, stream)
+        if rank == 0:
+            line["decode"] = decode_latency(mr, dev, stream)
+            line["prefill_route_sort"] = prefill_route_sort(mr, dev, stream)
+            breakdown = {}
+            for wl in [synth.large_softmax(k) for k in synth.LARGE_TOPKS] + [synth.large_e_sigmoid()]:
+                breakdown[wl.name] = time_kernels(mr, wl, dev, stream)
+            line["breakdown"] = breakdown
+            if not args.no_cpu_baseline:
+                line["cpu_baseline"] = cpu_baseline(w, args.cpu_rows)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

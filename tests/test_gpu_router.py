@@ -228,8 +228,9 @@ def test_device_exp_matches_its_specification_bit_for_bit(mr, orc):
     rnd = (bits.to(torch.int32)).view(torch.float32)
     grid = torch.linspace(-110.0, 95.0, 1 << 22)
     special = torch.tensor([0.0, -0.0, 1.0, -1.0, 88.72, 88.73, 89.0, -87.3, -103.9, -104.0, -104.1,
-                            float("inf"), float("-inf"), 1e-30, -1e-30, 0.5 * np.log(2.0)])
+                            float("inf"), float("-inf"), 1e-30, -1e-30, 0.34657359], dtype=torch.float32)
     x = torch.cat([rnd, -rnd, grid, special]).contiguous()
+    assert x.dtype == torch.float32
     x = x[~torch.isnan(x)]
     y = torch.empty_like(x, device="cuda")
     xg = x.cuda()

@@ -77,10 +77,12 @@ __global__ void __launch_bounds__(kFusedThreads) k_fused_decode(RouteArgs a, Sor
                          a.topk_w ? a.topk_w + o : nullptr);
     }
     __syncthreads();
-    // histogram of the T*topk pairs (ids are in range by construction)
+    // histogram of the T*topk pairs (ids are in range for finite logits; the
+    // check keeps a NaN row from indexing outside the counters)
     for (int i0 = warp * 32; i0 < N; i0 += blockDim.x) {
         const int i = i0 + lane;
-        warp_hist_add(cnt, i < N ? s_idx[i] : kInvalidExpert, lane);
+        const int e = i < N ? s_idx[i] : kInvalidExpert;
+        warp_hist_add(cnt, (e >= 0 && e < s.E_tot) ? e : kInvalidExpert, lane);
     }
     __syncthreads();
     for (int e = tid; e < s.E_tot; e += blockDim.x) {
