@@ -252,13 +252,21 @@ def time_kernels(mr, w, dev, stream, reps=20, warmup=3) -> dict:
     return out
 
 
-def decode_latency(mr, dev, stream, n_calls=200) -> dict:
+def decode_latency(mr, dev, stream, n_calls=200, Ts=synth.DECODE_TS) -> dict:
     """Fused vs unfused decode route+sort (E=256, topk=8, bf16), eager and graph."""
     L = mr._lib
     res = {}
     s = stream.cuda_stream
 
+    def checked(fn):
+        def run(st):
+            rc = fn(st)
+            if rc != 0:
+                raise RuntimeError(f"decode call failed: {mr.strerror(rc)}")
+        return run
+
     def eager(fn):
+        fn = checked(fn)
         with torch.cuda.stream(stream):
             for _ in range(20):
                 fn(s)
@@ -270,6 +278,7 @@ def decode_latency(mr, dev, stream, n_calls=200) -> dict:
         return (time.perf_counter() - t0) / n_calls * 1e6
 
     def graph(fn):
+        fn = checked(fn)
         g = torch.cuda.CUDAGraph()
         cs = torch.cuda.Stream(device=dev)
         with torch.cuda.stream(cs):
@@ -279,23 +288,24 @@ def decode_latency(mr, dev, stream, n_calls=200) -> dict:
         with torch.cuda.graph(g, stream=cs):
             for _ in range(n_calls):
                 fn(cs.cuda_stream)
-        for _ in range(3):
-            g.replay()
-        torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         reps = 10
-        a.record(cs)
-        for _ in range(reps):
-            g.replay()
-        b.record(cs)
+        with torch.cuda.stream(cs):  # replay() launches on the current stream
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            a.record(cs)
+            for _ in range(reps):
+                g.replay()
+            b.record(cs)
         torch.cuda.synchronize()
         return a.elapsed_time(b) * 1e3 / (reps * n_calls)
 
     noop = lambda st: L.moe_router_noop(st)  # noqa: E731
     floor = {"eager_us": round(eager(noop), 2), "graph_us": round(graph(noop), 2)}
     res["launch_floor"] = floor
-    for T in synth.DECODE_TS:
+    for T in Ts:
         w = synth.decode(T)
         x = w.make_logits().to(dev)
         p = mr.RouterParams(T=T, E=w.E, topk=w.topk, in_dtype=w.in_dtype, renorm=w.renorm)
@@ -470,8 +480,12 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["all", "step"], default="all",
-                    help="step: the timed step only (used for profiling captures)")
+    ap.add_argument("--only", choices=["all", "step", "decode"], default="all",
+                    help="step: the timed step only; decode: the decode latency table only "
+                         "(both used for profiling captures)")
+    ap.add_argument("--decode-calls", type=int, default=200, help="calls per decode timing loop")
+    ap.add_argument("--decode-ts", default=",".join(str(t) for t in synth.DECODE_TS),
+                    help="decode token counts, comma separated")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=8192, help="oracle sample size (token rows)")
     ap.add_argument("--ref-seconds", type=float, default=90.0,
@@ -487,6 +501,12 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU (the routing path has no CPU fallback)")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.only == "decode":
+        if rank == 0:
+            ts = tuple(int(t) for t in args.decode_ts.split(","))
+            print(json.dumps({"decode": decode_latency(mr, dev, torch.cuda.Stream(device=dev),
+                                                       args.decode_calls, ts)}), flush=True)
+        return 0
     if ws > 1:
         import torch.distributed as dist
 
@@ -560,7 +580,7 @@ def main():
     if args.only == "all":
         line["e2e"] = e2e_rate(mr, w, dev, stream)
         if rank == 0:
-            line["decode"] = decode_latency(mr, dev, stream)
+            line["decode"] = decode_latency(mr, dev, stream, args.decode_calls)
             line["prefill_route_sort"] = prefill_route_sort(mr, dev, stream)
             breakdown = {}
             for wl in [synth.large_softmax(k) for k in synth.LARGE_TOPKS] + [synth.large_e_sigmoid()]:

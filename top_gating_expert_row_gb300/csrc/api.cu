@@ -7,7 +7,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/moe_router.h"
+#include "moe_router.h"
 #include "internal.h"
 
 namespace mr {
@@ -205,6 +205,8 @@ RouteArgs route_args(const mr_router_params* p, const void* logits, void* probs,
     const uintptr_t in_al = p->in_dtype == MR_BF16 ? 8 : 16;
     a.vec = (p->E % 4 == 0) && aligned(logits, in_al) && aligned(probs, in_al) && aligned(inter, 16) &&
             aligned(map, 4) && aligned(p->bias, 16);
+    const size_t row_bytes = static_cast<size_t>(p->E) * (p->in_dtype == MR_BF16 ? 2 : 4);
+    a.prefetch = a.vec && row_bytes % 16 == 0 && aligned(logits, 16);
     return a;
 }
 
@@ -373,10 +375,12 @@ int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int
     if (p->T <= MR_MAX_FUSED_TOKENS && kNvBuckets[nv] <= kFusedMaxNv) {
         RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, topk_idx, topk_w);
         SortArgs s{sorted_token_ids, sorted_weights, expert_ids, num_tokens_post_pad, E_tot, block_m};
-        const bool sel = use_select(k_r);
+        // a one-CTA decode launch is bound by instruction fetch on a cold SM: the
+        // arg-max path has the shorter code, so it is the default up to k_r = 32
+        const bool sel = g_path.force == 2 || (g_path.force == 0 && k_r > 32);
         const int nw = kFusedThreads / 32;
         const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, sel, a.n_group > 0);
-        const size_t smem = static_cast<size_t>(L.bytes) * nw + fused_sort_smem(p->T * p->topk, E_tot, nw);
+        const size_t smem = static_cast<size_t>(L.bytes) * nw + fused_sort_layout(p->T * p->topk, E_tot, block_m).bytes;
         int dev = 0, maxsm = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)

@@ -23,7 +23,10 @@ constexpr int kSigmoid = 1;
 // single correctly rounded fp32 operation written with an explicit _rn
 // intrinsic, so the compiler cannot contract or reorder it. Error: < 1 ulp
 // (the Taylor remainder r^8/8! is under 0.1 ulp for |r| <= ln2/2).
-// x >= 89 -> +inf, x <= -104 -> +0, NaN -> NaN.
+// Specification at the ends: x >= 89 -> +inf, x <= -104 -> +0, NaN -> NaN.
+// Clamping x to [-104, 89] first reproduces those ends exactly (the formula
+// overflows to +inf from 88.73 up and rounds to +0 at -104), so exp_spec is
+// the specification for every non-NaN x without a branch.
 // ---------------------------------------------------------------------------
 constexpr double kLn2 = 0.693147180559945309417232121458176568;
 constexpr float kLog2e = static_cast<float>(1.0 / kLn2);
@@ -35,15 +38,9 @@ __device__ __forceinline__ float pow2_normal(int k)  // 2^k, -126 <= k <= 127
     return __int_as_float((k + 127) << 23);
 }
 
-__device__ __forceinline__ float exp_f32(float x)
+// p(r) ~ exp(r) for |r| <= ln2/2, Horner form of the degree-7 Taylor polynomial.
+__device__ __forceinline__ float exp_poly(float r)
 {
-    if (x != x) return x;
-    if (x >= 89.0f) return __int_as_float(0x7f800000);
-    if (x <= -104.0f) return 0.0f;
-    const float nf = rintf(__fmul_rn(x, kLog2e));
-    const int n = __float2int_rn(nf);
-    float r = __fmaf_rn(-nf, kLn2Hi, x);
-    r = __fmaf_rn(-nf, kLn2Lo, r);
     float p = static_cast<float>(1.0 / 5040.0);
     p = __fmaf_rn(p, r, static_cast<float>(1.0 / 720.0));
     p = __fmaf_rn(p, r, static_cast<float>(1.0 / 120.0));
@@ -51,37 +48,63 @@ __device__ __forceinline__ float exp_f32(float x)
     p = __fmaf_rn(p, r, static_cast<float>(1.0 / 6.0));
     p = __fmaf_rn(p, r, 0.5f);
     p = __fmaf_rn(p, r, 1.0f);
-    p = __fmaf_rn(p, r, 1.0f);
+    return __fmaf_rn(p, r, 1.0f);
+}
+
+__device__ __forceinline__ float exp_spec(float x)
+{
+    x = fminf(fmaxf(x, -104.0f), 89.0f);
+    const float nf = rintf(__fmul_rn(x, kLog2e));
+    const int n = __float2int_rn(nf);
+    float r = __fmaf_rn(-nf, kLn2Hi, x);
+    r = __fmaf_rn(-nf, kLn2Lo, r);
+    const float p = exp_poly(r);
     const int n1 = n / 2;
     const int n2 = n - n1;
     return __fmul_rn(__fmul_rn(p, pow2_normal(n1)), pow2_normal(n2));
 }
 
-// Logistic function 1 / (1 + exp(-x)) with IEEE add and divide.
+// The specification including NaN (used by the diagnostic entry point).
+__device__ __forceinline__ float exp_f32(float x) { return (x != x) ? x : exp_spec(x); }
+
+// exp for x <= 0 where only the value matters (softmax numerators): the same
+// reduction and polynomial, with x clamped at -87 so that 2^n stays a normal
+// scale applied by one exponent add. Below -87 it returns exp(-87) ~ 1.6e-38
+// instead of a smaller number, an absolute error under 2e-38.
+__device__ __forceinline__ float exp_nonpos(float x)
+{
+    x = fmaxf(x, -87.0f);
+    const float nf = rintf(__fmul_rn(x, kLog2e));
+    float r = __fmaf_rn(-nf, kLn2Hi, x);
+    r = __fmaf_rn(-nf, kLn2Lo, r);
+    const float p = exp_poly(r);
+    return __int_as_float(__float_as_int(p) + (__float2int_rn(nf) << 23));
+}
+
+// Logistic function 1 / (1 + exp(-x)), IEEE add and correctly rounded
+// reciprocal (the same number as an IEEE divide of 1 by the sum).
 __device__ __forceinline__ float sigmoid_f32(float x)
 {
-    return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_f32(-x)));
+    return __frcp_rn(__fadd_rn(1.0f, exp_spec(-x)));
 }
 
 // ---------------------------------------------------------------------------
 // Selection keys: a strictly increasing map from fp32 to uint32, so that
-// "larger key" is an unsigned compare. -0 is folded onto +0 (they compare
-// equal as floats) and NaN onto 0, the value reserved for "not a candidate"
-// (padding lanes, experts of dropped groups). Every finite or infinite float
-// maps to a key >= 0x007fffff.
+// "larger key" is an unsigned compare. Adding +0 folds -0 onto +0 (they compare
+// equal as floats). Every non-NaN float maps to a key >= 0x007fffff; key 0 is
+// reserved for "not a candidate" (padding, experts of dropped groups). NaN
+// inputs give unspecified keys.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t key_of(float f)
 {
-    uint32_t u = __float_as_uint(f);
-    if (f == 0.0f) u = 0u;
-    const uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    return (f != f) ? 0u : k;
+    const uint32_t u = __float_as_uint(__fadd_rn(f, 0.0f));
+    return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
 }
 
 __device__ __forceinline__ float float_of(uint32_t k)
 {
-    const uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
-    return __uint_as_float(u);
+    const uint32_t m = (k & 0x80000000u) ? 0x80000000u : 0xffffffffu;
+    return __uint_as_float(k ^ m);
 }
 
 // ---------------------------------------------------------------------------
@@ -118,6 +141,13 @@ __device__ __forceinline__ uint32_t lanemask_lt()
     uint32_t m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
     return m;
+}
+
+// Bulk prefetch of [p, p + bytes) into L2 (one instruction; p 16-byte aligned,
+// bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -32,15 +32,24 @@ using InT = float;
 #endif
 constexpr int kScore = MR_SCORE_FN;
 
+// Resident CTAs per SM the register budget is sized for: the row's keys take
+// 4*NV registers per lane.
+constexpr int fwd_min_blocks(int nv) { return nv >= 12 ? 2 : (nv >= 6 ? 3 : 4); }
+
 template <int NV, bool SELECT>
-__global__ void __launch_bounds__(kFwdThreads) k_router_fwd(RouteArgs a)
+__global__ void __launch_bounds__(kFwdThreads, fwd_min_blocks(NV)) k_router_fwd(RouteArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nw = blockDim.x >> 5;
     const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, SELECT, a.n_group > 0);
     unsigned char* wsm = smem + static_cast<size_t>(warp) * L.bytes;
-    for (int t = blockIdx.x * nw + warp; t < a.T; t += gridDim.x * nw) {
+    const int stride = gridDim.x * nw;
+    const uint32_t row_bytes = static_cast<uint32_t>(a.E) * sizeof(InT);
+    for (int t = blockIdx.x * nw + warp; t < a.T; t += stride) {
+        // the warp's next row streams into L2 while this one is computed
+        if (a.prefetch && lane == 0 && t + stride < a.T)
+            prefetch_l2(static_cast<const InT*>(a.logits) + static_cast<size_t>(t + stride) * a.E, row_bytes);
         const float scale = route_row<kScore, InT, NV, SELECT>(a, t, wsm, L, lane);
         if (a.topk_idx || a.topk_w) {
             const size_t o = static_cast<size_t>(t) * a.topk;
@@ -54,19 +63,26 @@ __global__ void __launch_bounds__(kFwdThreads) k_router_fwd(RouteArgs a)
 template <int NV, bool SELECT>
 __global__ void __launch_bounds__(kFusedThreads) k_fused_decode(RouteArgs a, SortArgs s)
 {
+    // A decode call is one short launch on one SM whose instruction cache is
+    // usually cold, so this kernel keeps its executed code short: per-expert
+    // token bitmasks give every pair its stable rank directly (a token's topk
+    // experts are distinct, so the rank of (t, j) inside expert e is the number
+    // of earlier tokens that chose e), one warp scans the padded counts, and
+    // three block barriers separate the phases.
     extern __shared__ __align__(16) unsigned char smem[];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5, nt = blockDim.x;
     const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, SELECT, a.n_group > 0);
     const int N = a.T * a.topk;
-    unsigned char* p = smem + static_cast<size_t>(nw) * L.bytes;
-    int32_t* s_idx = reinterpret_cast<int32_t*>(p); p += align16(N * 4);
-    float* s_w = reinterpret_cast<float*>(p); p += align16(N * 4);
-    uint32_t* cnt = reinterpret_cast<uint32_t*>(p); p += align16(s.E_tot * 4);
-    uint32_t* off = reinterpret_cast<uint32_t*>(p); p += align16((s.E_tot + 1) * 4);
-    uint32_t* tmp = reinterpret_cast<uint32_t*>(p); p += align16(33 * 4);
-    uint16_t* wh = reinterpret_cast<uint16_t*>(p);
+    const int E_tot = s.E_tot, bm = s.block_m;
+    const FusedSortLayout F = fused_sort_layout(N, E_tot, bm);
+    unsigned char* base = smem + static_cast<size_t>(nw) * L.bytes;
+    int32_t* s_idx = reinterpret_cast<int32_t*>(base + F.idx);
+    float* s_w = reinterpret_cast<float*>(base + F.w);
+    uint32_t* mask = reinterpret_cast<uint32_t*>(base + F.mask);
+    uint32_t* off = reinterpret_cast<uint32_t*>(base + F.off);
+    int32_t* blk = reinterpret_cast<int32_t*>(base + F.blk);
 
-    for (int e = tid; e < s.E_tot; e += blockDim.x) cnt[e] = 0u;
+    for (int e = tid; e < E_tot; e += nt) mask[e] = 0u;
     if (warp < a.T) {
         unsigned char* wsm = smem + static_cast<size_t>(warp) * L.bytes;
         const float scale = route_row<kScore, InT, NV, SELECT>(a, warp, wsm, L, lane);
@@ -77,28 +93,63 @@ __global__ void __launch_bounds__(kFusedThreads) k_fused_decode(RouteArgs a, Sor
                          a.topk_w ? a.topk_w + o : nullptr);
     }
     __syncthreads();
-    // histogram of the T*topk pairs (ids are in range for finite logits; the
-    // check keeps a NaN row from indexing outside the counters)
-    for (int i0 = warp * 32; i0 < N; i0 += blockDim.x) {
-        const int i = i0 + lane;
-        const int e = i < N ? s_idx[i] : kInvalidExpert;
-        warp_hist_add(cnt, (e >= 0 && e < s.E_tot) ? e : kInvalidExpert, lane);
+    if (warp < a.T) {
+        __syncwarp();
+        for (int j = lane; j < a.topk; j += 32) {
+            const int e = s_idx[warp * a.topk + j];
+            if (e >= 0 && e < E_tot) atomicOr(mask + e, 1u << warp);  // range check: NaN rows only
+        }
     }
     __syncthreads();
-    for (int e = tid; e < s.E_tot; e += blockDim.x) {
-        const uint32_t c = cnt[e];
-        off[e] = (c + s.block_m - 1) / s.block_m * s.block_m;
+    // one warp: padded counts -> exclusive offsets, block -> expert map
+    if (warp == 0) {
+        const int per = (E_tot + 31) / 32;
+        const int e0 = lane * per;
+        uint32_t local = 0u;
+        for (int i = 0; i < per; ++i)
+            if (e0 + i < E_tot) local += (__popc(mask[e0 + i]) + bm - 1) / bm * bm;
+        uint32_t run = warp_exclusive_scan(local, lane);
+        for (int i = 0; i < per; ++i) {
+            const int e = e0 + i;
+            if (e >= E_tot) break;
+            const uint32_t c = __popc(mask[e]);
+            off[e] = run;
+            const int nb = static_cast<int>((c + bm - 1) / bm);
+            for (int b = 0; b < nb; ++b) blk[run / bm + b] = e;
+            run += nb * bm;
+        }
+        if (lane == 31) {
+            off[E_tot] = run;
+            *s.num_post_pad = static_cast<int32_t>(run);
+        }
     }
     __syncthreads();
-    const uint32_t total = cta_exclusive_scan(off, s.E_tot, tmp);
-    if (tid == 0) {
-        off[s.E_tot] = total;
-        *s.num_post_pad = static_cast<int32_t>(total);
+    // real pairs: warp t writes its token's slots
+    if (warp < a.T) {
+        const uint32_t before = (1u << warp) - 1u;
+        for (int j = lane; j < a.topk; j += 32) {
+            const int f = warp * a.topk + j;
+            const int e = s_idx[f];
+            if (e < 0 || e >= E_tot) continue;
+            const uint32_t pos = off[e] + __popc(mask[e] & before);
+            s.ids[pos] = f;
+            if (s.w) s.w[pos] = s_w[f];
+        }
     }
-    __syncthreads();
-    cta_scatter(s_idx, s_w, 0, N, s.E_tot, off, wh, s.ids, s.w);
-    cta_fill_pads(off, cnt, s.E_tot, s.block_m, 0, static_cast<int>(total), N, s.ids, s.w,
-                  s.expert_ids);
+    // sentinels and expert ids, one block of block_m positions per warp step
+    const int nblk = static_cast<int>(off[E_tot]) / bm;
+    for (int b = warp; b < nblk; b += nw) {
+        const int e = blk[b];
+        const uint32_t c = __popc(mask[e]);
+        const uint32_t r_first = static_cast<uint32_t>(b * bm) - off[e];
+        for (int r = lane; r < bm; r += 32) {
+            if (r_first + r >= c) {
+                s.ids[b * bm + r] = N;
+                if (s.w) s.w[b * bm + r] = 0.0f;
+            }
+        }
+        if (lane == 0) s.expert_ids[b] = e;
+    }
 }
 
 namespace {
@@ -160,7 +211,7 @@ int MR_CAT(launch_fused, MR_SUFFIX)(const RouteArgs& a, const SortArgs& s, int n
     if (!f) return cudaErrorInvalidValue;
     const int nw = kFusedThreads / 32;
     const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, select, a.n_group > 0);
-    const size_t smem = static_cast<size_t>(L.bytes) * nw + fused_sort_smem(a.T * a.topk, s.E_tot, nw);
+    const size_t smem = static_cast<size_t>(L.bytes) * nw + fused_sort_layout(a.T * a.topk, s.E_tot, s.block_m).bytes;
     int err = ensure_smem(reinterpret_cast<const void*>(f), smem);
     if (err != cudaSuccess) return err;
     f<<<1, kFusedThreads, smem, st>>>(a, s);

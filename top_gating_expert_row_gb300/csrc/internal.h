@@ -41,16 +41,26 @@ struct SortArgs {
     int block_m;
 };
 
-// Shared-memory bytes of the fused decode kernel after the warp regions.
-inline size_t fused_sort_smem(int N, int E_tot, int nwarps)
+// Shared memory of the fused decode kernel after the warp regions: the T*topk
+// pairs, one token bitmask per expert, the padded offsets and the
+// block -> expert map.
+struct FusedSortLayout {
+    int idx, w, mask, off, blk, bytes;
+};
+
+__host__ __device__ inline FusedSortLayout fused_sort_layout(int N, int E_tot, int bm)
 {
-    size_t b = 0;
-    b += static_cast<size_t>(align16(N * 4)) * 2;           // pair ids and weights
-    b += static_cast<size_t>(align16(E_tot * 4));            // counts
-    b += static_cast<size_t>(align16((E_tot + 1) * 4));      // offsets
-    b += static_cast<size_t>(align16(33 * 4));               // scan scratch
-    b += static_cast<size_t>(align16(nwarps * E_tot * 2));   // per-warp counters
-    return b;
+    FusedSortLayout F;
+    const int nonempty = N < E_tot ? N : E_tot;
+    const int nblk = (N + nonempty * (bm - 1) + bm - 1) / bm;
+    int o = 0;
+    F.idx = o; o += align16(N * 4);
+    F.w = o; o += align16(N * 4);
+    F.mask = o; o += align16(E_tot * 4);
+    F.off = o; o += align16((E_tot + 1) * 4);
+    F.blk = o; o += align16((nblk > 0 ? nblk : 1) * 4);
+    F.bytes = o;
+    return F;
 }
 
 // Launch helpers; each returns a cudaError_t value (cudaSuccess on success).

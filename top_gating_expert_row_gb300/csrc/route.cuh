@@ -4,20 +4,21 @@
 // it (flowchart: convert to the compute type, apply the score function,
 // top-k-and-mask, write probs + routing_map), rebuilt for one warp per row:
 //
-//   1. load     the row into registers: lane l holds elements (v*32+l)*4 .. +3
-//               for v < NV, so every v is one coalesced 512 B (fp32) access
-//   2. score    softmax (warp max, written exp, warp sum) or sigmoid; the
-//               selection key (logit, or sigmoid + bias) as an order-preserving u32
-//   3. groups   (optional) group scores = sum of each group's top-m keys; the
+//   1. load     the row: lane l holds elements v*128 + 4l .. +3 for v < NV, so
+//               every v is one coalesced 512 B (fp32) access; only the u32
+//               selection keys stay in registers, the scores go to a per-warp
+//               shared-memory row buffer
+//   2. groups   (optional) group scores = sum of each group's top-m keys; the
 //               topk_group best groups are kept, the others' keys set to 0
-//   4. select   k_r winners by (key desc, index asc):
+//   3. select   k_r winners by (key desc, index asc):
 //               ARGMAX  - k_r rounds of warp arg-max (REDUX max/min), for small k
 //               SELECT  - bisection on the key for a threshold that leaves at most
 //                         `stop` candidates, compaction to shared memory, then an
 //                         exact all-pairs rank of the candidates; ties at the
 //                         threshold are taken in index order
-//   5. weights  renormalise over the winners and scale
-//   6. emit     dense probs / routing_map / intermediate and compact topk_idx/w
+//   4. weights  renormalise over the winners and scale
+//   5. emit     dense probs / routing_map / intermediate (compact topk_idx/w:
+//               emit_compact)
 //
 // Both selection paths produce the identical winner list.
 #pragma once
@@ -37,13 +38,19 @@ struct RouteArgs {
     int T, E, k_r, topk, n_shared;
     int renorm, n_group, topk_group;
     float scaling, shared_weight;
-    int vec;   // rows and all arrays allow 16-byte (fp32) / 8-byte (bf16) vector access
-    int stop;  // SELECT: candidate capacity (>= k_r); bisection stops at or below it
+    int vec;       // rows and all arrays allow 16-byte (fp32) / 8-byte (bf16) vector access
+    int prefetch;  // rows are 16-byte aligned and a multiple of 16 bytes: L2 bulk prefetch allowed
+    int stop;      // SELECT: candidate capacity (>= k_r); bisection stops at or below it
 };
 
 // Byte offsets of one warp's shared-memory region (same formula on host and device).
+//   vbuf     E fp32: the row's scores (softmax: exp(x - max), unnormalised; sigmoid: s)
+//   win_*    k_r winners in selection order
+//   cand     SELECT candidates, (key << 32 | ~index)
+//   keys     E u32, group-limited selection only
+//   scal     last winner's key and index, partial-tie flag
 struct WarpLayout {
-    int win_idx, win_val, cand_comp, cand_val, keys, scal, bytes;
+    int vbuf, win_idx, win_val, cand, keys, scal, bytes;
 };
 
 __host__ __device__ inline int align16(int x) { return (x + 15) & ~15; }
@@ -52,10 +59,10 @@ __host__ __device__ inline WarpLayout warp_layout(int k_r, int stop, int E, bool
 {
     WarpLayout L;
     int o = 0;
+    L.vbuf = o; o += align16(E * 4);
     L.win_idx = o; o += align16(k_r * 4);
     L.win_val = o; o += align16(k_r * 4);
-    L.cand_comp = o; o += select ? align16(stop * 8) : 0;
-    L.cand_val = o; o += select ? align16(stop * 4) : 0;
+    L.cand = o; o += select ? align16(stop * 8) : 0;
     L.keys = o; o += groups ? align16(E * 4) : 0;
     L.scal = o; o += 16;
     L.bytes = o;
@@ -123,105 +130,137 @@ __device__ void group_limit(uint32_t* skeys, int E, int G, int gk, int m, int la
 
 // ---------------------------------------------------------------------------
 // route_row: the whole forward for token t. Winners are left in the warp's
-// shared region (win_idx / win_val, k_r entries in selection order); returns
-// the factor that turns a winner's score into its weight.
+// shared region (win_idx / win_val = their score s, k_r entries in selection
+// order); returns the factor that turns a score into its weight (dense probs
+// and compact weights are both s * factor, so they agree bit for bit).
 // ---------------------------------------------------------------------------
 template <int SCORE, typename InT, int NV, bool SELECT>
 __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned char* wsm,
                                            const WarpLayout& L, int lane)
 {
+    float* vbuf = reinterpret_cast<float*>(wsm + L.vbuf);
     uint32_t* win_idx = reinterpret_cast<uint32_t*>(wsm + L.win_idx);
     float* win_val = reinterpret_cast<float*>(wsm + L.win_val);
     uint32_t* scal = reinterpret_cast<uint32_t*>(wsm + L.scal);
     const int E = a.E;
     const int k_r = a.k_r;
     const InT* row = static_cast<const InT*>(a.logits) + static_cast<size_t>(t) * E;
+    const int lane4 = lane * 4;
+    // a chunk (4 consecutive elements) is either whole or partly past E
+    auto whole = [&](int v) { return v * 128 + lane4 + 4 <= E; };
+    auto inside = [&](int v, int c) { return v * 128 + lane4 + c < E; };
 
-    float val[NV][4];
     uint32_t key[NV][4];
+    float vmul = 1.0f;  // vbuf * vmul = s
+    uint32_t kmax;
 
-    // 1. load
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        const int e0 = (v * 32 + lane) * 4;
-        if (a.vec && e0 + 4 <= E) {
-            load4<InT>(row + e0, val[v]);
-        } else {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) val[v][c] = (e0 + c < E) ? load_scalar<InT>(row + e0 + c) : 0.0f;
-        }
-    }
-
-    // 2. scores and selection keys; padding lanes get key 0 and score 0
-    if (SCORE == kSoftmax) {
-        float m = -__int_as_float(0x7f800000);
-#pragma unroll
-        for (int v = 0; v < NV; ++v)
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                if ((v * 32 + lane) * 4 + c < E) m = fmaxf(m, val[v][c]);
-        m = warp_max(m);
-        float sum = 0.0f;
-#pragma unroll
-        for (int v = 0; v < NV; ++v)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if ((v * 32 + lane) * 4 + c < E) {
-                    key[v][c] = key_of(val[v][c]);
-                    const float e = exp_f32(__fsub_rn(val[v][c], m));
-                    val[v][c] = e;
-                    sum = __fadd_rn(sum, e);
-                } else {
-                    key[v][c] = 0u;
-                    val[v][c] = 0.0f;
-                }
-            }
-        sum = warp_sum(sum);
-        const float inv = __fdiv_rn(1.0f, sum);
-#pragma unroll
-        for (int v = 0; v < NV; ++v)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) val[v][c] = __fmul_rn(val[v][c], inv);
-    } else {
+    // 1. load, selection keys, scores into vbuf; padding keys are 0
+    {
+        float x[NV][4];
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            const int e0 = (v * 32 + lane) * 4;
-            float b[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (a.bias) {
-                if (a.vec && e0 + 4 <= E) {
-                    const float4 q = __ldg(reinterpret_cast<const float4*>(a.bias + e0));
-                    b[0] = q.x; b[1] = q.y; b[2] = q.z; b[3] = q.w;
+            const int e0 = v * 128 + lane4;
+            if (a.vec && whole(v)) {
+                load4<InT>(row + e0, x[v]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) x[v][c] = inside(v, c) ? load_scalar<InT>(row + e0 + c) : 0.0f;
+            }
+        }
+        if (SCORE == kSoftmax) {
+            // keys (4 independent max chains), raw logits to vbuf
+            uint32_t lm[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    key[v][c] = inside(v, c) ? key_of(x[v][c]) : 0u;
+                    lm[c] = max(lm[c], key[v][c]);
+                }
+                const int e0 = v * 128 + lane4;
+                if (whole(v)) {
+                    *reinterpret_cast<float4*>(vbuf + e0) = make_float4(x[v][0], x[v][1], x[v][2], x[v][3]);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) b[c] = (e0 + c < E) ? __ldg(a.bias + e0 + c) : 0.0f;
+                    for (int c = 0; c < 4; ++c)
+                        if (inside(v, c)) vbuf[e0 + c] = x[v][c];
                 }
             }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (e0 + c < E) {
-                    const float s = sigmoid_f32(val[v][c]);
-                    key[v][c] = key_of(a.bias ? __fadd_rn(s, b[c]) : s);
-                    val[v][c] = s;
+            kmax = __reduce_max_sync(kFull, max(max(lm[0], lm[1]), max(lm[2], lm[3])));
+            const float m = float_of(kmax);
+            // exp(x - max) in place over the row buffer: a rolled loop keeps the
+            // code short (the row's chunks all run through the same instructions)
+            float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 2
+            for (int v = 0; v < NV; ++v) {
+                const int e0 = v * 128 + lane4;
+                if (whole(v)) {
+                    float4 q = *reinterpret_cast<const float4*>(vbuf + e0);
+                    q.x = exp_nonpos(__fsub_rn(q.x, m));
+                    q.y = exp_nonpos(__fsub_rn(q.y, m));
+                    q.z = exp_nonpos(__fsub_rn(q.z, m));
+                    q.w = exp_nonpos(__fsub_rn(q.w, m));
+                    sum[0] = __fadd_rn(sum[0], q.x);
+                    sum[1] = __fadd_rn(sum[1], q.y);
+                    sum[2] = __fadd_rn(sum[2], q.z);
+                    sum[3] = __fadd_rn(sum[3], q.w);
+                    *reinterpret_cast<float4*>(vbuf + e0) = q;
                 } else {
-                    key[v][c] = 0u;
-                    val[v][c] = 0.0f;
+                    for (int c = 0; c < 4; ++c)
+                        if (inside(v, c)) {
+                            const float ev = exp_nonpos(__fsub_rn(vbuf[e0 + c], m));
+                            vbuf[e0 + c] = ev;
+                            sum[c] = __fadd_rn(sum[c], ev);
+                        }
                 }
             }
+            vmul = __frcp_rn(warp_sum(__fadd_rn(__fadd_rn(sum[0], sum[1]), __fadd_rn(sum[2], sum[3]))));
+        } else {
+            uint32_t lm[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const int e0 = v * 128 + lane4;
+                float b[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                if (a.bias) {
+                    if (a.vec && whole(v)) {
+                        const float4 q = __ldg(reinterpret_cast<const float4*>(a.bias + e0));
+                        b[0] = q.x; b[1] = q.y; b[2] = q.z; b[3] = q.w;
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) b[c] = inside(v, c) ? __ldg(a.bias + e0 + c) : 0.0f;
+                    }
+                }
+                float sv[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    sv[c] = sigmoid_f32(x[v][c]);
+                    key[v][c] = inside(v, c) ? key_of(a.bias ? __fadd_rn(sv[c], b[c]) : sv[c]) : 0u;
+                    lm[c] = max(lm[c], key[v][c]);
+                }
+                if (whole(v)) {
+                    *reinterpret_cast<float4*>(vbuf + e0) = make_float4(sv[0], sv[1], sv[2], sv[3]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        if (inside(v, c)) vbuf[e0 + c] = sv[c];
+                }
+            }
+            kmax = __reduce_max_sync(kFull, max(max(lm[0], lm[1]), max(lm[2], lm[3])));
         }
     }
 
-    // 3. group limit (keys staged through shared memory)
+    // 2. group limit (keys staged through shared memory)
     if (a.n_group > 0) {
         uint32_t* sk = reinterpret_cast<uint32_t*>(wsm + L.keys);
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            const int e0 = (v * 32 + lane) * 4;
-            if (e0 + 4 <= E) {
+            const int e0 = v * 128 + lane4;
+            if (whole(v)) {
                 *reinterpret_cast<uint4*>(sk + e0) = make_uint4(key[v][0], key[v][1], key[v][2], key[v][3]);
             } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    if (e0 + c < E) sk[e0 + c] = key[v][c];
+                    if (inside(v, c)) sk[e0 + c] = key[v][c];
             }
         }
         __syncwarp();
@@ -231,70 +270,66 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
         else if (m <= 4) group_limit<4>(sk, E, a.n_group, a.topk_group, m, lane);
         else group_limit<8>(sk, E, a.n_group, a.topk_group, m, lane);
         __syncwarp();
+        uint32_t lmax = 0u;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            const int e0 = (v * 32 + lane) * 4;
-            if (e0 + 4 <= E) {
+            const int e0 = v * 128 + lane4;
+            if (whole(v)) {
                 const uint4 q = *reinterpret_cast<const uint4*>(sk + e0);
                 key[v][0] = q.x; key[v][1] = q.y; key[v][2] = q.z; key[v][3] = q.w;
             } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    if (e0 + c < E) key[v][c] = sk[e0 + c];
+                    if (inside(v, c)) key[v][c] = sk[e0 + c];
             }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) lmax = max(lmax, key[v][c]);
         }
+        kmax = __reduce_max_sync(kFull, lmax);
         __syncwarp();
     }
 
-    // 4. selection
-    uint32_t K = 0u, I = 0u;  // last winner (SELECT path membership test)
+    // 3. selection
+    uint32_t K = 0u, I = 0u;
+    bool partial_ties = false;  // SELECT: some keys equal to the last winner's key lost
     if (!SELECT) {
         // k_r rounds of arg-max; a winner's key becomes 1 (below every real key,
-        // above the 0 of padding / dropped groups), which also marks it as chosen.
+        // above the 0 of padding / dropped groups), which also marks it chosen.
         for (int j = 0; j < k_r; ++j) {
             uint32_t best = 0u, bidx = 0xffffffffu;
-            float bv = 0.0f;
 #pragma unroll
             for (int v = 0; v < NV; ++v)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const bool gt = key[v][c] > best;
                     best = gt ? key[v][c] : best;
-                    bidx = gt ? static_cast<uint32_t>((v * 32 + lane) * 4 + c) : bidx;
-                    bv = gt ? val[v][c] : bv;
+                    bidx = gt ? static_cast<uint32_t>(v * 128 + lane4 + c) : bidx;
                 }
             const uint32_t wmax = __reduce_max_sync(kFull, best);
             const uint32_t widx = __reduce_min_sync(kFull, best == wmax ? bidx : 0xffffffffu);
-            const float wv = __shfl_sync(kFull, bv, (widx >> 2) & 31u);
             if (lane == 0) {
                 win_idx[j] = widx;
-                win_val[j] = wv;
+                win_val[j] = __fmul_rn(vbuf[min(widx, static_cast<uint32_t>(E - 1))], vmul);
             }
 #pragma unroll
             for (int v = 0; v < NV; ++v)
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    if (static_cast<uint32_t>((v * 32 + lane) * 4 + c) == widx) key[v][c] = 1u;
+                    key[v][c] = (static_cast<uint32_t>(v * 128 + lane4 + c) == widx) ? 1u : key[v][c];
         }
     } else {
-        unsigned long long* cand = reinterpret_cast<unsigned long long*>(wsm + L.cand_comp);
-        float* cval = reinterpret_cast<float*>(wsm + L.cand_val);
+        unsigned long long* cand = reinterpret_cast<unsigned long long*>(wsm + L.cand);
         const uint32_t cap = static_cast<uint32_t>(a.stop);
-        uint32_t lmax = 0u, lmin = 0xffffffffu, lcnt = 0u;
-#pragma unroll
+        const uint32_t n_valid = static_cast<uint32_t>(a.n_group > 0 ? a.topk_group * (E / a.n_group) : E);
+        uint32_t ln[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};  // min over non-zero keys:
+#pragma unroll                                                                  // (k - 1) wraps 0 to the top
         for (int v = 0; v < NV; ++v)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint32_t k = key[v][c];
-                lmax = max(lmax, k);
-                lmin = (k != 0u) ? min(lmin, k) : lmin;
-                lcnt += (k != 0u);
-            }
-        const uint32_t kmax = __reduce_max_sync(kFull, lmax);
-        uint32_t lo = __reduce_min_sync(kFull, lmin);
-        uint32_t hi = kmax + 1u;               // count(key >= hi) == 0
-        uint32_t cnt_lo = __reduce_add_sync(kFull, lcnt), lane_lo = lcnt;
-        uint32_t cnt_hi = 0u, lane_hi = 0u;
+            for (int c = 0; c < 4; ++c) ln[c] = min(ln[c], key[v][c] - 1u);
+        uint32_t lo = __reduce_min_sync(kFull, min(min(ln[0], ln[1]), min(ln[2], ln[3]))) + 1u;
+        uint32_t hi = kmax + 1u;  // count(key >= hi) == 0
+        uint32_t cnt_lo = n_valid, cnt_hi = 0u;
+        int lane_lo = -1, lane_hi = 0;  // per-lane counts at lo / hi (-1: not yet counted)
         // Invariant: count(key >= lo) = cnt_lo >= k_r > count(key >= hi) = cnt_hi.
         for (int it = 0; it < 64 && cnt_lo > cap && hi - lo > 1u; ++it) {
             const uint32_t umid = lo + ((hi - lo) >> 1);
@@ -304,32 +339,41 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
                 const uint32_t km = key_of(fm);
                 if (km > lo && km < hi) mid = km;
             }
-            uint32_t c = 0u;
+            uint32_t cq[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
             for (int v = 0; v < NV; ++v)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) c += (key[v][q] >= mid);
+                for (int q = 0; q < 4; ++q) cq[q] += (key[v][q] >= mid);
+            const uint32_t c = (cq[0] + cq[1]) + (cq[2] + cq[3]);
             const uint32_t tot = __reduce_add_sync(kFull, c);
             if (tot >= static_cast<uint32_t>(k_r)) {
-                lo = mid; cnt_lo = tot; lane_lo = c;
+                lo = mid; cnt_lo = tot; lane_lo = static_cast<int>(c);
             } else {
-                hi = mid; cnt_hi = tot; lane_hi = c;
+                hi = mid; cnt_hi = tot; lane_hi = static_cast<int>(c);
             }
         }
+        auto comp = [&](uint32_t k, int v, int c) {
+            return (static_cast<unsigned long long>(k) << 32) |
+                   static_cast<uint32_t>(~static_cast<uint32_t>(v * 128 + lane4 + c));
+        };
         uint32_t n;
         if (cnt_lo <= cap) {
             // candidates: every key >= lo
-            uint32_t pos = warp_exclusive_scan(lane_lo, lane);
+            if (lane_lo < 0) {
+                uint32_t c = 0u;
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) c += (key[v][q] >= lo);
+                lane_lo = static_cast<int>(c);
+            }
+            uint32_t pos = warp_exclusive_scan(static_cast<uint32_t>(lane_lo), lane);
 #pragma unroll
             for (int v = 0; v < NV; ++v)
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     if (key[v][c] >= lo) {
-                        if (pos < cap) {
-                            cand[pos] = (static_cast<unsigned long long>(key[v][c]) << 32) |
-                                        static_cast<uint32_t>(~static_cast<uint32_t>((v * 32 + lane) * 4 + c));
-                            cval[pos] = val[v][c];
-                        }
+                        if (pos < cap) cand[pos] = comp(key[v][c], v, c);
                         ++pos;
                     }
             n = cnt_lo;
@@ -337,17 +381,13 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
             // hi == lo + 1: the k_r-th key is exactly lo. Take every key >= hi
             // (fewer than k_r), then keys equal to lo in index order.
             const uint32_t lim = static_cast<uint32_t>(k_r);
-            uint32_t pos = warp_exclusive_scan(lane_hi, lane);
+            uint32_t pos = warp_exclusive_scan(static_cast<uint32_t>(lane_hi), lane);
 #pragma unroll
             for (int v = 0; v < NV; ++v)
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     if (key[v][c] >= hi) {
-                        if (pos < lim) {
-                            cand[pos] = (static_cast<unsigned long long>(key[v][c]) << 32) |
-                                        static_cast<uint32_t>(~static_cast<uint32_t>((v * 32 + lane) * 4 + c));
-                            cval[pos] = val[v][c];
-                        }
+                        if (pos < lim) cand[pos] = comp(key[v][c], v, c);
                         ++pos;
                     }
             uint32_t base = cnt_hi;
@@ -362,16 +402,13 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     if (key[v][c] == lo) {
-                        if (p < lim) {
-                            cand[p] = (static_cast<unsigned long long>(lo) << 32) |
-                                      static_cast<uint32_t>(~static_cast<uint32_t>((v * 32 + lane) * 4 + c));
-                            cval[p] = val[v][c];
-                        }
+                        if (p < lim) cand[p] = comp(lo, v, c);
                         ++p;
                     }
                 base += tot;
             }
             n = min(base, lim);
+            partial_ties = true;
         }
         n = min(n, cap);
         __syncwarp();
@@ -381,70 +418,87 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
             const unsigned long long c0 = (i0 < n) ? cand[i0] : 0ull;
             const unsigned long long c1 = (i1 < n) ? cand[i1] : 0ull;
             uint32_t r0 = 0u, r1 = 0u;
+#pragma unroll 8
             for (uint32_t q = 0; q < n; ++q) {
                 const unsigned long long cq = cand[q];
                 r0 += (cq > c0);
                 r1 += (cq > c1);
             }
-            if (i0 < n && r0 < static_cast<uint32_t>(k_r)) {
-                win_idx[r0] = ~static_cast<uint32_t>(c0);
-                win_val[r0] = cval[i0];
-                if (r0 == static_cast<uint32_t>(k_r - 1)) {
-                    scal[0] = static_cast<uint32_t>(c0 >> 32);
-                    scal[1] = ~static_cast<uint32_t>(c0);
-                }
-            }
-            if (i1 < n && r1 < static_cast<uint32_t>(k_r)) {
-                win_idx[r1] = ~static_cast<uint32_t>(c1);
-                win_val[r1] = cval[i1];
-                if (r1 == static_cast<uint32_t>(k_r - 1)) {
-                    scal[0] = static_cast<uint32_t>(c1 >> 32);
-                    scal[1] = ~static_cast<uint32_t>(c1);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t i = h ? i1 : i0;
+                const uint32_t r = h ? r1 : r0;
+                const unsigned long long cc = h ? c1 : c0;
+                if (i < n && r <= static_cast<uint32_t>(k_r)) {
+                    const uint32_t idx = ~static_cast<uint32_t>(cc);
+                    const uint32_t kk = static_cast<uint32_t>(cc >> 32);
+                    if (r < static_cast<uint32_t>(k_r)) {
+                        win_idx[r] = idx;
+                        win_val[r] = __fmul_rn(vbuf[min(idx, static_cast<uint32_t>(E - 1))], vmul);
+                        if (r == static_cast<uint32_t>(k_r - 1)) {
+                            scal[0] = kk;
+                            scal[1] = idx;
+                        }
+                    } else {
+                        scal[2] = kk;  // the best loser's key
+                    }
                 }
             }
         }
         __syncwarp();
         K = scal[0];
         I = scal[1];
+        // some key equal to K lost only if the best loser (when there is one) ties K
+        partial_ties = partial_ties || (n > static_cast<uint32_t>(k_r) && scal[2] == K);
     }
     __syncwarp();
 
-    // 5. weights
+    // 4. weights
     float wsum = 0.0f;
     for (int j = lane; j < k_r; j += 32) wsum = __fadd_rn(wsum, win_val[j]);
     wsum = warp_sum(wsum);
     const float scale = a.renorm ? (wsum > 0.0f ? __fdiv_rn(a.scaling, wsum) : 0.0f) : a.scaling;
 
-    // 6. emit the dense rows (compact outputs: emit_compact)
+    // 5. emit the dense rows (compact outputs: emit_compact)
     if (a.probs || a.map || a.inter) {
         InT* prow = a.probs ? static_cast<InT*>(a.probs) + static_cast<size_t>(t) * E : nullptr;
         uint8_t* mrow = a.map ? a.map + static_cast<size_t>(t) * E : nullptr;
         float* irow = a.inter ? a.inter + static_cast<size_t>(t) * E : nullptr;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            const int e0 = (v * 32 + lane) * 4;
+            const int e0 = v * 128 + lane4;
             if (e0 >= E) continue;
-            float p4[4];
+            float s4[4], p4[4];
+            if (whole(v)) {
+                const float4 q = *reinterpret_cast<const float4*>(vbuf + e0);
+                s4[0] = q.x; s4[1] = q.y; s4[2] = q.z; s4[3] = q.w;
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) s4[c] = inside(v, c) ? vbuf[e0 + c] : 0.0f;
+            }
             uint32_t m4 = 0u;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const uint32_t idx = static_cast<uint32_t>(e0 + c);
                 const uint32_t k = key[v][c];
-                const bool member = SELECT ? (k > K || (k == K && idx <= I)) : (k == 1u);
-                p4[c] = member ? __fmul_rn(val[v][c], scale) : 0.0f;
+                bool member;
+                if (!SELECT) member = (k == 1u);
+                else if (!partial_ties) member = (k >= K);
+                else member = (k > K) || (k == K && static_cast<uint32_t>(e0 + c) <= I);
+                s4[c] = __fmul_rn(s4[c], vmul);
+                p4[c] = __fmul_rn(s4[c], member ? scale : 0.0f);
                 m4 |= (member ? 1u : 0u) << (8 * c);
             }
-            if (a.vec && e0 + 4 <= E) {
+            if (a.vec && whole(v)) {
                 if (prow) store4<InT>(prow + e0, p4);
                 if (mrow) *reinterpret_cast<uint32_t*>(mrow + e0) = m4;
-                if (irow) *reinterpret_cast<float4*>(irow + e0) = make_float4(val[v][0], val[v][1], val[v][2], val[v][3]);
+                if (irow) *reinterpret_cast<float4*>(irow + e0) = make_float4(s4[0], s4[1], s4[2], s4[3]);
             } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    if (e0 + c >= E) break;
+                    if (!inside(v, c)) break;
                     if (prow) store_scalar<InT>(prow + e0 + c, p4[c]);
                     if (mrow) mrow[e0 + c] = static_cast<uint8_t>((m4 >> (8 * c)) & 1u);
-                    if (irow) irow[e0 + c] = val[v][c];
+                    if (irow) irow[e0 + c] = s4[c];
                 }
             }
         }
@@ -453,7 +507,8 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
 }
 
 // Compact outputs of one row from the winner list: routed slots in selection
-// order, then the shared experts E..E+n_shared-1 with shared_weight.
+// order, then the shared experts E..E+n_shared-1 with shared_weight. `scale`
+// is route_row's return value (score -> weight).
 __device__ __forceinline__ void emit_compact(const RouteArgs& a, const unsigned char* wsm,
                                              const WarpLayout& L, float scale, int lane,
                                              int32_t* idx_row, float* w_row)
