@@ -167,6 +167,33 @@ int moe_sort(const int32_t* topk_idx, const float* topk_w, int T, int topk, int 
              mr_stream_t stream);
 
 /*
+ * moe_sort_noalloc -- moe_sort without a workspace argument, for callers that cannot
+ * allocate device memory: code that is handed only a stream and its tensors (an
+ * inference-engine plugin or custom op with no allocator handle), or code that must
+ * not call cudaMalloc/cudaFree because those synchronise the device or are not
+ * allowed at that point. The pages have no counterpart; this is a convenience of
+ * this library.
+ *
+ * Same arguments, layout, outputs and errors as moe_sort, minus workspace/ws_bytes.
+ * Its scratch (the per-chunk expert-count table, moe_sort_workspace_bytes() bytes)
+ * is a file-scope device array of MR_SORT_NOALLOC_SCRATCH_BYTES inside the library,
+ * held on every GPU that loads the library until the process exits; a call whose
+ * table would not fit returns MR_EUNSUPPORTED before anything is enqueued. The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * The first call on a device looks up the array's device address (a
+ * cudaGetSymbolAddress with that device current) and caches it: make that first
+ * call outside any stream capture. All calls on a device share the one array and
+ * every call rewrites the part it uses, so nothing needs clearing between calls, but
+ * calls whose work overlaps on the GPU (different streams, no ordering) race on it
+ * and give wrong results: order them, or use moe_sort with separate workspaces.
+ */
+#define MR_SORT_NOALLOC_SCRATCH_BYTES (1u << 20)
+int moe_sort_noalloc(const int32_t* topk_idx, const float* topk_w, int T, int topk, int E_tot,
+                     int block_m, int32_t* sorted_token_ids, float* sorted_weights,
+                     int32_t* expert_ids, int32_t* num_tokens_post_pad, int32_t* status,
+                     mr_stream_t stream);
+
+/*
  * moe_router_fused_fwd_sort -- moe_router_fwd (compact outputs) followed by moe_sort
  * over E_tot = E + n_shared experts ([FLY] fused top-k + sorting). For
  * T <= MR_MAX_FUSED_TOKENS and E <= MR_MAX_FUSED_EXPERTS it is ONE launch of one CTA;

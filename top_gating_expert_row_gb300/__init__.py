@@ -50,6 +50,7 @@ _SIGS = {
     "moe_sort_capacity": ([_I, _I, _I, _I], _SZ),
     "moe_sort_workspace_bytes": ([_I, _I, _I, _I], _SZ),
     "moe_sort": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
+    "moe_sort_noalloc": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_router_fused_workspace_bytes": ([_PP, _I], _SZ),
     "moe_router_fused_fwd_sort": ([_PP, _P, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], _I),
     "moe_router_strerror": ([_I], ctypes.c_char_p),
@@ -190,6 +191,20 @@ def moe_sort(topk_idx, topk_w, T, topk, E_tot, block_m, sorted_token_ids, sorted
     return _ok(_lib.moe_sort(_ptr(topk_idx), _ptr(topk_w), T, topk, E_tot, block_m, _ptr(sorted_token_ids),
                              _ptr(sorted_weights), _ptr(expert_ids), _ptr(num_tokens_post_pad),
                              _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)), "moe_sort")
+
+
+def moe_sort_noalloc(topk_idx, topk_w, T, topk, E_tot, block_m, sorted_token_ids, sorted_weights, expert_ids,
+                     num_tokens_post_pad, status=None, stream=None) -> int:
+    """moe_sort without a workspace: for callers that cannot allocate device
+    memory. Its scratch is a fixed device array inside the library (see
+    include/moe_router.h); calls that overlap on the GPU race on it."""
+    return _ok(_lib.moe_sort_noalloc(_ptr(topk_idx), _ptr(topk_w), T, topk, E_tot, block_m,
+                                     _ptr(sorted_token_ids), _ptr(sorted_weights), _ptr(expert_ids),
+                                     _ptr(num_tokens_post_pad), _ptr(status), _stream(stream)),
+               "moe_sort_noalloc")
+
+
+MR_SORT_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
 def moe_router_fused_workspace_bytes(p, block_m) -> int:

@@ -226,6 +226,34 @@ int check_sort(int T, int topk, int E_tot, int block_m)
 }
 }  // namespace
 
+// ---- allocation-free sort: scratch in a file-scope device array ----------------------------------
+
+// Scratch of moe_sort_noalloc: the per-chunk expert-count table that moe_sort
+// keeps in its caller's workspace. Every GPU that loads the library holds this
+// array until the process exits; all calls on a device share it.
+static __device__ __align__(256) uint32_t g_sort_scratch[MR_SORT_NOALLOC_SCRATCH_BYTES / 4];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {nullptr};
+
+// Device address of g_sort_scratch on the current device. In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device with that device current and cached. Returns nullptr on failure.
+void* sort_scratch_address()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_sort_scratch) != cudaSuccess) return nullptr;
+        g_scratch_ptr[dev] = ptr;
+    }
+    return g_scratch_ptr[dev];
+}
+}  // namespace
+
 }  // namespace mr
 
 using namespace mr;
@@ -345,6 +373,25 @@ int moe_sort(const int32_t* topk_idx, const float* topk_w, int T, int topk, int 
     if (ws_bytes < sort_ws_bytes(N, E_tot) || !aligned(workspace, 4)) return MR_EINVAL;
     return from_cuda(launch_sort(topk_idx, topk_w, static_cast<int>(N), E_tot, block_m, sorted_token_ids,
                                  sorted_weights, expert_ids, num_tokens_post_pad, static_cast<uint32_t*>(workspace),
+                                 status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_sort_noalloc(const int32_t* topk_idx, const float* topk_w, int T, int topk, int E_tot, int block_m,
+                     int32_t* sorted_token_ids, float* sorted_weights, int32_t* expert_ids,
+                     int32_t* num_tokens_post_pad, int32_t* status, mr_stream_t stream)
+{
+    int rc = check_sort(T, topk, E_tot, block_m);
+    if (rc != MR_OK) return rc;
+    if (!sorted_token_ids || !expert_ids || !num_tokens_post_pad) return MR_EINVAL;
+    if (T > 0 && !topk_idx) return MR_EINVAL;
+    const long long N = static_cast<long long>(T) * topk;
+    if (sort_ws_bytes(N, E_tot) > MR_SORT_NOALLOC_SCRATCH_BYTES) return MR_EUNSUPPORTED;
+    // The count table is fully rewritten by every call, so nothing in the
+    // scratch has to start at zero.
+    void* scratch = sort_scratch_address();
+    if (!scratch) return MR_ECUDA;
+    return from_cuda(launch_sort(topk_idx, topk_w, static_cast<int>(N), E_tot, block_m, sorted_token_ids,
+                                 sorted_weights, expert_ids, num_tokens_post_pad, static_cast<uint32_t*>(scratch),
                                  status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
