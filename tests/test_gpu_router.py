@@ -134,12 +134,12 @@ FULL = [synth.large_softmax(k) for k in synth.LARGE_TOPKS] + [synth.large_e_soft
 @pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
 def test_full_size_sampled_rows(mr, orc, w):
     """The full workload in the benchmark's launch configuration; the oracle
-    checks 300 sampled rows one by one."""
+    checks 2048 sampled rows one by one."""
     x, b, xg, bg = gpu_inputs(w)
     dense = w.n_group == 0
     out = gpu_route(mr, w, xg, bg, 0, dense=dense)
     torch.cuda.synchronize()
-    rows = sample_rows(w.T, 300)
+    rows = sample_rows(w.T, 2048)
     check_fwd(out, oracle_route(orc, w, x, b, rows), w, rows=rows, what=w.name)
     # properties over every row: topk distinct, routing_map consistent with topk_idx
     idx = out["topk_idx"][:, : w.topk - w.n_shared].long()
@@ -148,6 +148,26 @@ def test_full_size_sampled_rows(mr, orc, w):
     if dense:
         m = torch.zeros(w.T, w.E, dtype=torch.uint8, device="cuda").scatter_(1, idx, 1)
         assert torch.equal(m, out["routing_map"])
+
+
+@pytest.mark.parametrize("path", [ARGMAX, SELECT], ids=["argmax", "select"])
+@pytest.mark.parametrize("E,k,fn", [(512, 36, SM), (512, 22, SG), (2304, 36, SM), (384, 8, SG)])
+def test_rows_of_varying_scale_every_row(mr, orc, E, k, fn, path):
+    """Many rows per warp (T=8192 on the persistent grid), with per-row scales from
+    1e-3 to 1e2, shifts and occasional constant rows, so the threshold a warp carries
+    from one row to the next is often wrong; every row is checked."""
+    T = 8192
+    g = torch.Generator().manual_seed(4)
+    x = torch.randn(T, E, generator=g)
+    scale = 10.0 ** (torch.rand(T, 1, generator=g) * 5 - 3)
+    shift = torch.randn(T, 1, generator=g) * 5
+    x = x * scale + shift
+    x[::97] = 0.25  # constant rows: all ties
+    x = x.contiguous()
+    w = W("varying", T, E, k, fn, renorm=1)
+    out = gpu_route(mr, w, x.cuda(), None, path)
+    torch.cuda.synchronize()
+    check_fwd(out, oracle_route(orc, w, x, None), w, what=f"varying E={E} k={k}")
 
 
 BWD_CASES = [synth.tiny(), W("e512_k22", 300, 512, 22, sigma=2.0), W("e512_k22_sig", 300, 512, 22, SG),

@@ -81,6 +81,32 @@ __device__ __forceinline__ float exp_nonpos(float x)
     return __int_as_float(__float_as_int(p) + (__float2int_rn(nf) << 23));
 }
 
+// exp(x) for x <= 0 where only the value matters (softmax numerators), in
+// about eight instructions: e^x = 2^n * 2^f with n = rint(x*log2 e) and
+// f = x*log2 e - n computed from a two-part log2 e (f = fma(x, L2E_HI, -n),
+// then + x*L2E_LO), so f in [-1/2, 1/2] carries no error from rounding
+// x*log2 e; 2^f comes from the hardware base-2 exponential (relative error
+// about 2^-22), 2^n is an exponent add. x is clamped at -87 (2^n stays normal;
+// below that the result is exp(-87) ~ 1.6e-38 instead of smaller).
+constexpr float kLog2eHi = kLog2e;
+constexpr float kLog2eLo = static_cast<float>(1.0 / kLn2 - static_cast<double>(kLog2e));
+
+__device__ __forceinline__ float exp2_hw(float f)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(f));
+    return y;
+}
+
+__device__ __forceinline__ float exp_value(float x)
+{
+    x = fmaxf(x, -87.0f);
+    const float n = rintf(__fmul_rn(x, kLog2eHi));
+    float f = __fmaf_rn(x, kLog2eHi, -n);
+    f = __fmaf_rn(x, kLog2eLo, f);
+    return __int_as_float(__float_as_int(exp2_hw(f)) + (__float2int_rn(n) << 23));
+}
+
 // Logistic function 1 / (1 + exp(-x)), IEEE add and correctly rounded
 // reciprocal (the same number as an IEEE divide of 1 by the sum).
 __device__ __forceinline__ float sigmoid_f32(float x)
@@ -190,6 +216,25 @@ template <>
 __device__ __forceinline__ void store_scalar<__nv_bfloat16>(__nv_bfloat16* p, float v)
 {
     *p = __float2bfloat16_rn(v);
+}
+
+// Four consecutive values with the streaming (evict-first) cache hint.
+template <typename OutT>
+__device__ __forceinline__ void store4_stream(OutT* p, const float (&v)[4]);
+template <>
+__device__ __forceinline__ void store4_stream<float>(float* p, const float (&v)[4])
+{
+    __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+}
+template <>
+__device__ __forceinline__ void store4_stream<__nv_bfloat16>(__nv_bfloat16* p, const float (&v)[4])
+{
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
+    uint2 q;
+    q.x = *reinterpret_cast<const uint32_t*>(&a);
+    q.y = *reinterpret_cast<const uint32_t*>(&b);
+    __stcs(reinterpret_cast<uint2*>(p), q);
 }
 
 template <typename OutT>

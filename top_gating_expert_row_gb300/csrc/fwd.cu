@@ -10,6 +10,7 @@
 //                    pairs in shared memory (FlyDSL PR 582, fused top-k gating
 //                    + MoE sorting at decode sizes)
 #include "internal.h"
+#include "route_wide.cuh"
 #include "sort.cuh"
 
 #ifndef MR_SCORE_FN
@@ -46,15 +47,46 @@ __global__ void __launch_bounds__(kFwdThreads, fwd_min_blocks(NV)) k_router_fwd(
     unsigned char* wsm = smem + static_cast<size_t>(warp) * L.bytes;
     const int stride = gridDim.x * nw;
     const uint32_t row_bytes = static_cast<uint32_t>(a.E) * sizeof(InT);
+    uint32_t warm = 0u;  // threshold carried from this warp's previous row
     for (int t = blockIdx.x * nw + warp; t < a.T; t += stride) {
         // the warp's next row streams into L2 while this one is computed
         if (a.prefetch && lane == 0 && t + stride < a.T)
             prefetch_l2(static_cast<const InT*>(a.logits) + static_cast<size_t>(t + stride) * a.E, row_bytes);
-        const float scale = route_row<kScore, InT, NV, SELECT>(a, t, wsm, L, lane);
+        const float scale = route_row<kScore, InT, NV, SELECT>(a, t, wsm, L, lane, warm);
         if (a.topk_idx || a.topk_w) {
             const size_t o = static_cast<size_t>(t) * a.topk;
             emit_compact(a, wsm, L, scale, lane, a.topk_idx ? a.topk_idx + o : nullptr,
                          a.topk_w ? a.topk_w + o : nullptr);
+        }
+        __syncwarp();
+    }
+}
+
+// Wide rows (E > 1024): the row lives in shared memory, one warp per row.
+template <bool SELECT, bool FULL>
+__global__ void __launch_bounds__(kWideThreads) k_router_fwd_wide(RouteArgs a)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nw = blockDim.x >> 5;
+    const WideLayout L = wide_layout(a.k_r, a.stop, a.E, SELECT, kScore == kSigmoid && !a.inter);
+    unsigned char* wsm = smem + static_cast<size_t>(warp) * L.bytes;
+    const int stride = gridDim.x * nw;
+    const uint32_t row_bytes = static_cast<uint32_t>(a.E) * sizeof(InT);
+    uint32_t warm = 0u;
+    for (int t = blockIdx.x * nw + warp; t < a.T; t += stride) {
+        if (a.prefetch && lane == 0 && t + stride < a.T)
+            prefetch_l2(static_cast<const InT*>(a.logits) + static_cast<size_t>(t + stride) * a.E, row_bytes);
+        const float scale = route_row_wide<kScore, InT, SELECT, FULL>(a, t, wsm, L, lane, warm);
+        if (a.topk_idx || a.topk_w) {
+            const size_t o = static_cast<size_t>(t) * a.topk;
+            const uint32_t* win_idx = reinterpret_cast<const uint32_t*>(wsm + L.win_idx);
+            const float* win_val = reinterpret_cast<const float*>(wsm + L.win_val);
+            for (int j = lane; j < a.topk; j += 32) {
+                const bool routed = j < a.k_r;
+                if (a.topk_idx) a.topk_idx[o + j] = routed ? static_cast<int32_t>(win_idx[j]) : a.E + (j - a.k_r);
+                if (a.topk_w) a.topk_w[o + j] = routed ? __fmul_rn(win_val[j], scale) : a.shared_weight;
+            }
         }
         __syncwarp();
     }
@@ -85,7 +117,8 @@ __global__ void __launch_bounds__(kFusedThreads) k_fused_decode(RouteArgs a, Sor
     for (int e = tid; e < E_tot; e += nt) mask[e] = 0u;
     if (warp < a.T) {
         unsigned char* wsm = smem + static_cast<size_t>(warp) * L.bytes;
-        const float scale = route_row<kScore, InT, NV, SELECT>(a, warp, wsm, L, lane);
+        uint32_t warm = 0u;
+        const float scale = route_row<kScore, InT, NV, SELECT>(a, warp, wsm, L, lane, warm);
         const size_t o = static_cast<size_t>(warp) * a.topk;
         emit_compact(a, wsm, L, scale, lane, s_idx + o, s_w + o);
         if (a.topk_idx || a.topk_w)
@@ -167,8 +200,6 @@ FwdFn fwd_kernel(int nv_idx)
         case 4: return k_router_fwd<4, SELECT>;
         case 6: return k_router_fwd<6, SELECT>;
         case 8: return k_router_fwd<8, SELECT>;
-        case 12: return k_router_fwd<12, SELECT>;
-        case 18: return k_router_fwd<18, SELECT>;
     }
     return nullptr;
 }
@@ -191,6 +222,20 @@ FusedFn fused_kernel(int nv_idx)
 
 int MR_CAT(launch_fwd, MR_SUFFIX)(const RouteArgs& a, int nv_idx, bool select, cudaStream_t st)
 {
+    if (kNvBuckets[nv_idx] > kRegisterMaxNv) {
+        const bool full = a.vec && a.E % 128 == 0;
+        const FwdFn f = select ? (full ? k_router_fwd_wide<true, true> : k_router_fwd_wide<true, false>)
+                               : (full ? k_router_fwd_wide<false, true> : k_router_fwd_wide<false, false>);
+        const WideLayout L = wide_layout(a.k_r, a.stop, a.E, select, kScore == kSigmoid && !a.inter);
+        const size_t smem = static_cast<size_t>(L.bytes) * (kWideThreads / 32);
+        int err = ensure_smem(reinterpret_cast<const void*>(f), smem);
+        if (err != cudaSuccess) return err;
+        const long long ctas_needed = (static_cast<long long>(a.T) + kWideThreads / 32 - 1) / (kWideThreads / 32);
+        const int grid = persistent_grid(reinterpret_cast<const void*>(f), kWideThreads, smem, ctas_needed);
+        if (grid <= 0) return cudaErrorInvalidConfiguration;
+        f<<<grid, kWideThreads, smem, st>>>(a);
+        return cudaGetLastError();
+    }
     const FwdFn f = select ? fwd_kernel<true>(nv_idx) : fwd_kernel<false>(nv_idx);
     if (!f) return cudaErrorInvalidValue;
     const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, select, a.n_group > 0);

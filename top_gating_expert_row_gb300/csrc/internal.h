@@ -31,6 +31,10 @@ inline int nv_index(int E)
 
 // The one-CTA fused decode kernel keeps rows up to this many chunks (E <= 1024).
 constexpr int kFusedMaxNv = 8;
+// The forward keeps rows of up to this many chunks in registers (E <= 1024);
+// wider rows take the shared-memory routine, two warps per CTA.
+constexpr int kRegisterMaxNv = 8;
+constexpr int kWideThreads = 64;
 
 struct SortArgs {
     int32_t* ids;

@@ -136,7 +136,7 @@ __device__ void group_limit(uint32_t* skeys, int E, int G, int gk, int m, int la
 // ---------------------------------------------------------------------------
 template <int SCORE, typename InT, int NV, bool SELECT>
 __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned char* wsm,
-                                           const WarpLayout& L, int lane)
+                                           const WarpLayout& L, int lane, uint32_t& warm)
 {
     float* vbuf = reinterpret_cast<float*>(wsm + L.vbuf);
     uint32_t* win_idx = reinterpret_cast<uint32_t*>(wsm + L.win_idx);
@@ -188,18 +188,19 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
             }
             kmax = __reduce_max_sync(kFull, max(max(lm[0], lm[1]), max(lm[2], lm[3])));
             const float m = float_of(kmax);
-            // exp(x - max) in place over the row buffer: a rolled loop keeps the
-            // code short (the row's chunks all run through the same instructions)
+            // exp(x - max) in place over the row buffer (exp_value: only the value
+            // matters here); a rolled loop keeps the code short (the row's chunks
+            // all run through the same instructions)
             float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 2
             for (int v = 0; v < NV; ++v) {
                 const int e0 = v * 128 + lane4;
                 if (whole(v)) {
                     float4 q = *reinterpret_cast<const float4*>(vbuf + e0);
-                    q.x = exp_nonpos(__fsub_rn(q.x, m));
-                    q.y = exp_nonpos(__fsub_rn(q.y, m));
-                    q.z = exp_nonpos(__fsub_rn(q.z, m));
-                    q.w = exp_nonpos(__fsub_rn(q.w, m));
+                    q.x = exp_value(__fsub_rn(q.x, m));
+                    q.y = exp_value(__fsub_rn(q.y, m));
+                    q.z = exp_value(__fsub_rn(q.z, m));
+                    q.w = exp_value(__fsub_rn(q.w, m));
                     sum[0] = __fadd_rn(sum[0], q.x);
                     sum[1] = __fadd_rn(sum[1], q.y);
                     sum[2] = __fadd_rn(sum[2], q.z);
@@ -208,7 +209,7 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
                 } else {
                     for (int c = 0; c < 4; ++c)
                         if (inside(v, c)) {
-                            const float ev = exp_nonpos(__fsub_rn(vbuf[e0 + c], m));
+                            const float ev = exp_value(__fsub_rn(vbuf[e0 + c], m));
                             vbuf[e0 + c] = ev;
                             sum[c] = __fadd_rn(sum[c], ev);
                         }
@@ -321,16 +322,40 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
         unsigned long long* cand = reinterpret_cast<unsigned long long*>(wsm + L.cand);
         const uint32_t cap = static_cast<uint32_t>(a.stop);
         const uint32_t n_valid = static_cast<uint32_t>(a.n_group > 0 ? a.topk_group * (E / a.n_group) : E);
-        uint32_t ln[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};  // min over non-zero keys:
-#pragma unroll                                                                  // (k - 1) wraps 0 to the top
-        for (int v = 0; v < NV; ++v)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) ln[c] = min(ln[c], key[v][c] - 1u);
-        uint32_t lo = __reduce_min_sync(kFull, min(min(ln[0], ln[1]), min(ln[2], ln[3]))) + 1u;
-        uint32_t hi = kmax + 1u;  // count(key >= hi) == 0
+        // Invariant: count(key >= lo) = cnt_lo >= k_r > count(key >= hi) = cnt_hi.
+        // lo starts at 1, below every real key (count = n_valid); the row minimum
+        // is only computed when the bisection needs a real lower end.
+        uint32_t lo = 1u, hi = kmax + 1u;
         uint32_t cnt_lo = n_valid, cnt_hi = 0u;
         int lane_lo = -1, lane_hi = 0;  // per-lane counts at lo / hi (-1: not yet counted)
-        // Invariant: count(key >= lo) = cnt_lo >= k_r > count(key >= hi) = cnt_hi.
+        auto count_ge = [&](uint32_t piv) {
+            uint32_t cq[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) cq[q] += (key[v][q] >= piv);
+            return (cq[0] + cq[1]) + (cq[2] + cq[3]);
+        };
+        auto split = [&](uint32_t piv) {
+            const uint32_t c = count_ge(piv);
+            const uint32_t tot = __reduce_add_sync(kFull, c);
+            if (tot >= static_cast<uint32_t>(k_r)) {
+                lo = piv; cnt_lo = tot; lane_lo = static_cast<int>(c);
+            } else {
+                hi = piv; cnt_hi = tot; lane_hi = static_cast<int>(c);
+            }
+        };
+        // warm start: the previous row's threshold (rows of one batch are alike,
+        // so it usually leaves between k_r and `stop` candidates in one pass)
+        if (cnt_lo > cap && warm > lo && warm < hi) split(warm);
+        if (cnt_lo > cap && lo == 1u) {
+            uint32_t ln[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) ln[c] = min(ln[c], key[v][c] - 1u);  // 0 wraps to the top
+            lo = __reduce_min_sync(kFull, min(min(ln[0], ln[1]), min(ln[2], ln[3]))) + 1u;
+        }
         for (int it = 0; it < 64 && cnt_lo > cap && hi - lo > 1u; ++it) {
             const uint32_t umid = lo + ((hi - lo) >> 1);
             uint32_t mid = umid;
@@ -339,18 +364,7 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
                 const uint32_t km = key_of(fm);
                 if (km > lo && km < hi) mid = km;
             }
-            uint32_t cq[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-            for (int v = 0; v < NV; ++v)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) cq[q] += (key[v][q] >= mid);
-            const uint32_t c = (cq[0] + cq[1]) + (cq[2] + cq[3]);
-            const uint32_t tot = __reduce_add_sync(kFull, c);
-            if (tot >= static_cast<uint32_t>(k_r)) {
-                lo = mid; cnt_lo = tot; lane_lo = static_cast<int>(c);
-            } else {
-                hi = mid; cnt_hi = tot; lane_hi = static_cast<int>(c);
-            }
+            split(mid);
         }
         auto comp = [&](uint32_t k, int v, int c) {
             return (static_cast<unsigned long long>(k) << 32) |
@@ -411,6 +425,8 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
             partial_ties = true;
         }
         n = min(n, cap);
+        const uint32_t warm_rank = min(n - 1u, static_cast<uint32_t>(k_r + k_r / 2));
+        if (lane == 0) scal[3] = lo;
         __syncwarp();
         // exact rank of each candidate in selection order
         for (uint32_t b = 0; b < n; b += 64) {
@@ -429,7 +445,7 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
                 const uint32_t i = h ? i1 : i0;
                 const uint32_t r = h ? r1 : r0;
                 const unsigned long long cc = h ? c1 : c0;
-                if (i < n && r <= static_cast<uint32_t>(k_r)) {
+                if (i < n) {
                     const uint32_t idx = ~static_cast<uint32_t>(cc);
                     const uint32_t kk = static_cast<uint32_t>(cc >> 32);
                     if (r < static_cast<uint32_t>(k_r)) {
@@ -439,15 +455,17 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
                             scal[0] = kk;
                             scal[1] = idx;
                         }
-                    } else {
+                    } else if (r == static_cast<uint32_t>(k_r)) {
                         scal[2] = kk;  // the best loser's key
                     }
+                    if (r == warm_rank) scal[3] = kk;
                 }
             }
         }
         __syncwarp();
         K = scal[0];
         I = scal[1];
+        warm = scal[3];
         // some key equal to K lost only if the best loser (when there is one) ties K
         partial_ties = partial_ties || (n > static_cast<uint32_t>(k_r) && scal[2] == K);
     }

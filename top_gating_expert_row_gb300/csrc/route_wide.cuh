@@ -1,0 +1,444 @@
+// One token row of the router forward for wide rows (E > 1024), computed by
+// one warp with the row held in shared memory.
+//
+// Same steps and results as route_row (route.cuh), laid out for a short
+// instruction stream: the selection keys (and, for sigmoid, the scores) live in
+// a per-warp shared-memory row padded to whole 128-element chunks, and every
+// per-element pass is one small loop over the lane's chunks. With the row in
+// registers the fully unrolled passes over E=2304 keys made the code larger
+// than the instruction caches, so warps stalled on instruction fetch; here the
+// whole routine is a few hundred instructions.
+//
+// Scores never take shared memory when the intermediate output is requested:
+// the scores pass writes them (softmax: the unnormalised numerators) straight
+// into the caller's intermediate row, and the emit pass reads them back from
+// L2 and overwrites them with the final values. The row is rewritten in L2
+// before it is evicted, so DRAM sees one write, and each warp needs only its
+// 9 KB of keys (E = 2304), which keeps twice as many warps resident as a
+// second shared row would. Without the intermediate output, softmax recomputes
+// exp(x - max) from the key (the key map is invertible) and sigmoid keeps its
+// scores in a shared row.
+#pragma once
+
+#include "route.cuh"
+
+namespace mr {
+
+// Per-warp shared memory of the wide routine.
+//   kbuf   keys, nv*128 u32 (positions >= E hold 0, "not a candidate")
+//   vbuf   sigmoid scores when there is no intermediate output, nv*128 fp32
+//   win_*, cand, scal as in WarpLayout
+struct WideLayout {
+    int kbuf, vbuf, win_idx, win_val, cand, scal, bytes;
+};
+
+__host__ __device__ inline WideLayout wide_layout(int k_r, int stop, int E, bool select, bool keep_scores)
+{
+    WideLayout L;
+    const int padded = (E + 127) / 128 * 128;
+    int o = 0;
+    L.kbuf = o; o += padded * 4;
+    L.vbuf = o; o += keep_scores ? padded * 4 : 0;
+    L.win_idx = o; o += align16(k_r * 4);
+    L.win_val = o; o += align16(k_r * 4);
+    L.cand = o; o += select ? align16(stop * 8) : 0;
+    L.scal = o; o += 16;
+    L.bytes = o;
+    return L;
+}
+
+// FULL: every chunk is whole and vector-aligned (a.vec and E % 128 == 0), so the
+// per-chunk edge handling compiles away.
+template <int SCORE, typename InT, bool SELECT, bool FULL>
+__device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsigned char* wsm,
+                                                const WideLayout& L, int lane, uint32_t& warm)
+{
+    uint32_t* kbuf = reinterpret_cast<uint32_t*>(wsm + L.kbuf);
+    float* vbuf = reinterpret_cast<float*>(wsm + L.vbuf);
+    uint32_t* win_idx = reinterpret_cast<uint32_t*>(wsm + L.win_idx);
+    float* win_val = reinterpret_cast<float*>(wsm + L.win_val);
+    uint32_t* scal = reinterpret_cast<uint32_t*>(wsm + L.scal);
+    const int E = a.E;
+    const int k_r = a.k_r;
+    const int nv = (E + 127) >> 7;
+    const int lane4 = lane * 4;
+    const InT* row = static_cast<const InT*>(a.logits) + static_cast<size_t>(t) * E;
+    auto whole = [&](int v) { return FULL || v * 128 + lane4 + 4 <= E; };
+    const bool vec = FULL || a.vec;
+    // every pass below touches only the lane's own chunks (v*128 + 4*lane .. +3)
+    auto k4 = [&](int v) -> uint4& { return *reinterpret_cast<uint4*>(kbuf + v * 128 + lane4); };
+
+    float* irow0 = a.inter ? a.inter + static_cast<size_t>(t) * E : nullptr;  // score scratch + output
+    // 1. load (8 chunks in flight), selection keys, sigmoid scores
+    uint32_t lm = 0u;
+    float m = 0.0f;    // softmax: the row max
+    float vmul = 1.0f; // score = stored/recomputed value * vmul
+    for (int v0 = 0; v0 < nv; v0 += 8) {
+        float x[8][4];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int v = v0 + u;
+            const int e0 = v * 128 + lane4;
+            if (v < nv) {
+                if (vec && whole(v)) {
+                    load4<InT>(row + e0, x[u]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) x[u][c] = (e0 + c < E) ? load_scalar<InT>(row + e0 + c) : 0.0f;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int v = v0 + u;
+            const int e0 = v * 128 + lane4;
+            if (v >= nv) continue;
+            uint32_t kk[4];
+            if (SCORE == kSoftmax) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) kk[c] = (FULL || e0 + c < E) ? key_of(x[u][c]) : 0u;
+            } else {
+                float b[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                if (a.bias) {
+                    if (vec && whole(v)) {
+                        const float4 q = __ldg(reinterpret_cast<const float4*>(a.bias + e0));
+                        b[0] = q.x; b[1] = q.y; b[2] = q.z; b[3] = q.w;
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) b[c] = (e0 + c < E) ? __ldg(a.bias + e0 + c) : 0.0f;
+                    }
+                }
+                float sv[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    sv[c] = (FULL || e0 + c < E) ? sigmoid_f32(x[u][c]) : 0.0f;
+                    kk[c] = (FULL || e0 + c < E) ? key_of(a.bias ? __fadd_rn(sv[c], b[c]) : sv[c]) : 0u;
+                }
+                if (irow0) {
+                    if (vec && whole(v)) {
+                        *reinterpret_cast<float4*>(irow0 + e0) = make_float4(sv[0], sv[1], sv[2], sv[3]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            if (e0 + c < E) irow0[e0 + c] = sv[c];
+                    }
+                } else {
+                    *reinterpret_cast<float4*>(vbuf + e0) = make_float4(sv[0], sv[1], sv[2], sv[3]);
+                }
+            }
+            lm = max(lm, max(max(kk[0], kk[1]), max(kk[2], kk[3])));
+            k4(v) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+        }
+    }
+    uint32_t kmax = __reduce_max_sync(kFull, lm);
+    if (SCORE == kSoftmax) {
+        m = float_of(kmax);
+        float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+        for (int v = 0; v < nv; ++v) {
+            const uint4 q = k4(v);
+            // padding keys are 0: their numerator is dropped (computed, then selected away)
+            const float e0 = exp_value(__fsub_rn(float_of(q.x), m));
+            const float e1 = exp_value(__fsub_rn(float_of(q.y), m));
+            const float e2 = exp_value(__fsub_rn(float_of(q.z), m));
+            const float e3 = exp_value(__fsub_rn(float_of(q.w), m));
+            const float4 e = FULL ? make_float4(e0, e1, e2, e3)
+                                  : make_float4(q.x ? e0 : 0.0f, q.y ? e1 : 0.0f, q.z ? e2 : 0.0f, q.w ? e3 : 0.0f);
+            sum[0] = __fadd_rn(sum[0], e.x);
+            sum[1] = __fadd_rn(sum[1], e.y);
+            sum[2] = __fadd_rn(sum[2], e.z);
+            sum[3] = __fadd_rn(sum[3], e.w);
+            if (irow0) {
+                const int o = v * 128 + lane4;
+                if (vec && whole(v)) {
+                    *reinterpret_cast<float4*>(irow0 + o) = e;
+                } else {
+                    const float ev[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        if (o + c < E) irow0[o + c] = ev[c];
+                }
+            }
+        }
+        vmul = __frcp_rn(warp_sum(__fadd_rn(__fadd_rn(sum[0], sum[1]), __fadd_rn(sum[2], sum[3]))));
+    }
+    __syncwarp();  // scores written by one lane are read by another below
+    // a winner's score: softmax recomputes it from the key; sigmoid reads it back
+    auto score_of = [&](uint32_t idx, uint32_t key) {
+        if (SCORE == kSoftmax) return __fmul_rn(exp_value(__fsub_rn(float_of(key), m)), vmul);
+        const uint32_t i = min(idx, static_cast<uint32_t>(E - 1));
+        return irow0 ? __ldcg(irow0 + i) : vbuf[i];
+    };
+
+    // 2. group limit, directly on the shared keys
+    if (a.n_group > 0) {
+        __syncwarp();
+        const int mg = k_r / a.topk_group;
+        if (mg <= 1) group_limit<1>(kbuf, E, a.n_group, a.topk_group, mg, lane);
+        else if (mg <= 2) group_limit<2>(kbuf, E, a.n_group, a.topk_group, mg, lane);
+        else if (mg <= 4) group_limit<4>(kbuf, E, a.n_group, a.topk_group, mg, lane);
+        else group_limit<8>(kbuf, E, a.n_group, a.topk_group, mg, lane);
+        __syncwarp();
+        lm = 0u;
+        for (int v = 0; v < nv; ++v) {
+            const uint4 q = k4(v);
+            lm = max(lm, max(max(q.x, q.y), max(q.z, q.w)));
+        }
+        kmax = __reduce_max_sync(kFull, lm);
+    }
+
+    // 3. selection
+    uint32_t K = 0u, I = 0u;
+    bool partial_ties = false;
+    if (!SELECT) {
+        // k_r rounds of arg-max; round j only considers keys that come after the
+        // previous winner in selection order (keys stay intact: softmax scores
+        // are recomputed from them)
+        uint32_t Kp = 0xffffffffu, Ip = 0xffffffffu;
+        for (int j = 0; j < k_r; ++j) {
+            uint32_t best = 0u, bidx = 0xffffffffu;
+            for (int v = 0; v < nv; ++v) {
+                const uint4 q = k4(v);
+                const uint32_t e0 = static_cast<uint32_t>(v * 128 + lane4);
+                const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const bool after = kq[c] < Kp || (kq[c] == Kp && e0 + c > Ip);
+                    if (after && kq[c] > best) {
+                        best = kq[c];
+                        bidx = e0 + c;
+                    }
+                }
+            }
+            const uint32_t wmax = __reduce_max_sync(kFull, best);
+            const uint32_t widx = __reduce_min_sync(kFull, best == wmax ? bidx : 0xffffffffu);
+            if (lane == 0 && widx < static_cast<uint32_t>(E)) {
+                win_idx[j] = widx;
+                win_val[j] = score_of(widx, wmax);
+            }
+            Kp = wmax;
+            Ip = widx;
+        }
+        K = Kp;
+        I = Ip;
+        partial_ties = true;
+    } else {
+        unsigned long long* cand = reinterpret_cast<unsigned long long*>(wsm + L.cand);
+        const uint32_t cap = static_cast<uint32_t>(a.stop);
+        const uint32_t n_valid = static_cast<uint32_t>(a.n_group > 0 ? a.topk_group * (E / a.n_group) : E);
+        uint32_t lo = 1u, hi = kmax + 1u;
+        uint32_t cnt_lo = n_valid, cnt_hi = 0u;
+        int lane_lo = -1, lane_hi = 0;
+        auto count_ge = [&](uint32_t piv) {
+            uint32_t c0 = 0u, c1 = 0u;
+#pragma unroll 4
+            for (int v = 0; v < nv; ++v) {
+                const uint4 q = k4(v);
+                c0 += (q.x >= piv) + (q.y >= piv);
+                c1 += (q.z >= piv) + (q.w >= piv);
+            }
+            return c0 + c1;
+        };
+        // Invariant: count(key >= lo) = cnt_lo >= k_r > count(key >= hi) = cnt_hi.
+        // Pivots: the previous row's threshold first, then value-space midpoints,
+        // then key-space midpoints (at most 64 rounds in all).
+        for (int it = -1; it < 64 && cnt_lo > cap && hi - lo > 1u; ++it) {
+            uint32_t piv;
+            if (it < 0) {
+                if (!(warm > lo && warm < hi)) continue;
+                piv = warm;
+            } else {
+                if (lo == 1u) {  // a real lower end: the row's smallest key
+                    uint32_t ln = 0xffffffffu;
+                    for (int v = 0; v < nv; ++v) {
+                        const uint4 q = k4(v);
+                        ln = min(ln, min(min(q.x - 1u, q.y - 1u), min(q.z - 1u, q.w - 1u)));  // 0 wraps to the top
+                    }
+                    lo = __reduce_min_sync(kFull, ln) + 1u;
+                    if (!(cnt_lo > cap && hi - lo > 1u)) break;
+                }
+                piv = lo + ((hi - lo) >> 1);
+                if (it < 8) {
+                    const float fm = __fadd_rn(__fmul_rn(float_of(lo), 0.5f), __fmul_rn(float_of(hi - 1u), 0.5f));
+                    const uint32_t km = key_of(fm);
+                    if (km > lo && km < hi) piv = km;
+                }
+            }
+            const uint32_t c = count_ge(piv);
+            const uint32_t tot = __reduce_add_sync(kFull, c);
+            if (tot >= static_cast<uint32_t>(k_r)) {
+                lo = piv; cnt_lo = tot; lane_lo = static_cast<int>(c);
+            } else {
+                hi = piv; cnt_hi = tot; lane_hi = static_cast<int>(c);
+            }
+        }
+        auto comp = [&](uint32_t k, uint32_t idx) {
+            return (static_cast<unsigned long long>(k) << 32) | static_cast<uint32_t>(~idx);
+        };
+        uint32_t n;
+        if (cnt_lo <= cap) {
+            if (lane_lo < 0) lane_lo = static_cast<int>(count_ge(lo));
+            uint32_t pos = warp_exclusive_scan(static_cast<uint32_t>(lane_lo), lane);
+#pragma unroll 2
+            for (int v = 0; v < nv; ++v) {
+                const uint4 q = k4(v);
+                const uint32_t e0 = static_cast<uint32_t>(v * 128 + lane4);
+                const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const bool in = kq[c] >= lo;
+                    if (in && pos < cap) cand[pos] = comp(kq[c], e0 + c);
+                    pos += in ? 1u : 0u;
+                }
+            }
+            n = cnt_lo;
+        } else {
+            // hi == lo + 1: the k_r-th key is lo; take keys >= hi, then keys == lo
+            // in index order
+            const uint32_t lim = static_cast<uint32_t>(k_r);
+            uint32_t pos = warp_exclusive_scan(static_cast<uint32_t>(lane_hi), lane);
+            uint32_t base = cnt_hi;
+            for (int v = 0; v < nv; ++v) {
+                const uint4 q = k4(v);
+                const uint32_t e0 = static_cast<uint32_t>(v * 128 + lane4);
+                const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+                uint32_t m4 = 0u;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (kq[c] >= hi) {
+                        if (pos < lim) cand[pos] = comp(kq[c], e0 + c);
+                        ++pos;
+                    }
+                    m4 += (kq[c] == lo);
+                }
+                const uint32_t off = warp_exclusive_scan(m4, lane);
+                const uint32_t tot = __shfl_sync(kFull, off + m4, 31);
+                uint32_t p = base + off;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (kq[c] == lo) {
+                        if (p < lim) cand[p] = comp(lo, e0 + c);
+                        ++p;
+                    }
+                base += tot;
+            }
+            n = min(base, lim);
+            partial_ties = true;
+        }
+        n = min(n, cap);
+        const uint32_t warm_rank = min(n - 1u, static_cast<uint32_t>(k_r + k_r / 4));
+        if (lane == 0) scal[3] = lo;
+        __syncwarp();
+        for (uint32_t b = 0; b < n; b += 64) {
+            const uint32_t i0 = b + lane, i1 = b + 32 + lane;
+            const unsigned long long c0 = (i0 < n) ? cand[i0] : 0ull;
+            const unsigned long long c1 = (i1 < n) ? cand[i1] : 0ull;
+            uint32_t r0 = 0u, r1 = 0u;
+#pragma unroll 8
+            for (uint32_t q = 0; q < n; ++q) {
+                const unsigned long long cq = cand[q];
+                r0 += (cq > c0);
+                r1 += (cq > c1);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t i = h ? i1 : i0;
+                const uint32_t r = h ? r1 : r0;
+                const unsigned long long cc = h ? c1 : c0;
+                if (i < n) {
+                    const uint32_t idx = ~static_cast<uint32_t>(cc);
+                    const uint32_t kk = static_cast<uint32_t>(cc >> 32);
+                    if (r < static_cast<uint32_t>(k_r)) {
+                        win_idx[r] = idx;
+                        win_val[r] = score_of(idx, kk);
+                        if (r == static_cast<uint32_t>(k_r - 1)) {
+                            scal[0] = kk;
+                            scal[1] = idx;
+                        }
+                    } else if (r == static_cast<uint32_t>(k_r)) {
+                        scal[2] = kk;
+                    }
+                    if (r == warm_rank) scal[3] = kk;
+                }
+            }
+        }
+        __syncwarp();
+        K = scal[0];
+        I = scal[1];
+        warm = scal[3];
+        partial_ties = partial_ties || (n > static_cast<uint32_t>(k_r) && scal[2] == K);
+    }
+    __syncwarp();
+
+    // 4. weights
+    float wsum = 0.0f;
+    for (int j = lane; j < k_r; j += 32) wsum = __fadd_rn(wsum, win_val[j]);
+    wsum = warp_sum(wsum);
+    const float scale = a.renorm ? (wsum > 0.0f ? __fdiv_rn(a.scaling, wsum) : 0.0f) : a.scaling;
+
+    // 5. dense rows
+    if (a.probs || a.map || a.inter) {
+        InT* prow = a.probs ? static_cast<InT*>(a.probs) + static_cast<size_t>(t) * E : nullptr;
+        uint8_t* mrow = a.map ? a.map + static_cast<size_t>(t) * E : nullptr;
+        float* irow = a.inter ? a.inter + static_cast<size_t>(t) * E : nullptr;
+#pragma unroll 4
+        for (int v = 0; v < nv; ++v) {
+            const int e0 = v * 128 + lane4;
+            if (!FULL && e0 >= E) continue;
+            const uint4 q = k4(v);
+            const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+            float s4[4], p4[4];
+            const bool vw = vec && whole(v);
+            if (irow) {  // the scores pass left them in the intermediate row
+                if (vw) {
+                    const float4 sq = __ldcg(reinterpret_cast<const float4*>(irow + e0));
+                    s4[0] = sq.x; s4[1] = sq.y; s4[2] = sq.z; s4[3] = sq.w;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) s4[c] = (e0 + c < E) ? __ldcg(irow + e0 + c) : 0.0f;
+                }
+                if (SCORE == kSoftmax) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) s4[c] = __fmul_rn(s4[c], vmul);
+                }
+            } else if (SCORE == kSoftmax) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float ev = __fmul_rn(exp_value(__fsub_rn(float_of(kq[c]), m)), vmul);
+                    s4[c] = kq[c] ? ev : 0.0f;
+                }
+            } else {
+                const float4 sq = *reinterpret_cast<const float4*>(vbuf + e0);
+                s4[0] = sq.x; s4[1] = sq.y; s4[2] = sq.z; s4[3] = sq.w;
+            }
+            uint32_t m4 = 0u;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t k = kq[c];
+                bool member;
+                if (!partial_ties) member = (k >= K);
+                else member = (k > K) || (k == K && static_cast<uint32_t>(e0 + c) <= I);
+                p4[c] = __fmul_rn(s4[c], member ? scale : 0.0f);
+                m4 |= (member ? 1u : 0u) << (8 * c);
+            }
+            // (normal stores: the backward usually reads these rows next, from L2)
+            const bool wi = irow && SCORE == kSoftmax;  // sigmoid scores are final already
+            if (vw) {
+                if (prow) store4<InT>(prow + e0, p4);
+                if (mrow) *reinterpret_cast<uint32_t*>(mrow + e0) = m4;
+                if (wi) *reinterpret_cast<float4*>(irow + e0) = make_float4(s4[0], s4[1], s4[2], s4[3]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (e0 + c >= E) break;
+                    if (prow) store_scalar<InT>(prow + e0 + c, p4[c]);
+                    if (mrow) mrow[e0 + c] = static_cast<uint8_t>((m4 >> (8 * c)) & 1u);
+                    if (wi) irow[e0 + c] = s4[c];
+                }
+            }
+        }
+    }
+    return scale;
+}
+
+}  // namespace mr
