@@ -440,6 +440,15 @@ def cpu_baseline(w, rows: int, reps: int = 3) -> dict:
 # ---------------------------------------------------------------------------------------- main
 
 
+# --workload choices for the timed step (the default is the headline workload;
+# the others exist for profiling captures of the same kernels on other shapes)
+STEP_WORKLOADS = {
+    "softmax_T8192_E2304_k36": synth.large_e_softmax,
+    "sigmoid_bias_T8192_E2304_k36": synth.large_e_sigmoid,
+    **{f"softmax_T8192_E512_k{k}": (lambda k=k: synth.large_softmax(k)) for k in synth.LARGE_TOPKS},
+}
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -466,7 +475,9 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "T": w.T, "E": w.E, "topk": w.topk, "score_fn": "softmax",
+            "config": {"workload": WORKLOAD if args.workload == "softmax_T8192_E2304_k36" else args.workload,
+                       "T": w.T, "E": w.E, "topk": w.topk,
+                       "score_fn": "softmax" if w.score_fn == synth.SOFTMAX else "sigmoid",
                        "sample_rows_per_step": rows},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -486,6 +497,8 @@ def main():
     ap.add_argument("--decode-calls", type=int, default=200, help="calls per decode timing loop")
     ap.add_argument("--decode-ts", default=",".join(str(t) for t in synth.DECODE_TS),
                     help="decode token counts, comma separated")
+    ap.add_argument("--workload", choices=sorted(STEP_WORKLOADS), default="softmax_T8192_E2304_k36",
+                    help="workload of the timed step (default: the headline one)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=8192, help="oracle sample size (token rows)")
     ap.add_argument("--ref-seconds", type=float, default=90.0,
@@ -512,7 +525,7 @@ def main():
 
         dist.init_process_group("nccl", device_id=dev)
     stream = torch.cuda.Stream(device=dev)
-    w = synth.large_e_softmax()
+    w = STEP_WORKLOADS[args.workload]()
     launches, _, _ = make_step(mr, w, dev, stream)
     nbytes = step_bytes(w)
     tm = Timer(stream)
@@ -557,7 +570,8 @@ def main():
         ms = tm.mean_ms(name)
         per_kernel[name] = {"us": round(ms * 1e3, 2), "GB/s": round(nb / (ms * 1e-3) / 1e9, 1),
                             "frac_of_peak": round(nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
-                            "page_B300_GB/s": PAGE_B300.get((name, "softmax", w.E, w.topk))}
+                            "page_B300_GB/s": PAGE_B300.get(
+                                (name, "softmax" if w.score_fn == synth.SOFTMAX else "sigmoid", w.E, w.topk))}
     dom = max(per_kernel, key=lambda n: per_kernel[n]["us"])
     dom_ms = tm.mean_ms(dom)
     achieved = nbytes[dom] / (dom_ms * 1e-3) / 1e9
@@ -571,7 +585,9 @@ def main():
     line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "T": w.T, "E": w.E, "topk": w.topk, "score_fn": "softmax",
+            "config": {"workload": WORKLOAD if args.workload == "softmax_T8192_E2304_k36" else args.workload,
+                       "T": w.T, "E": w.E, "topk": w.topk,
+                       "score_fn": "softmax" if w.score_fn == synth.SOFTMAX else "sigmoid",
                        "kernels_per_step": [n for n, _ in launches], "bytes_per_step": sum(nbytes.values()),
                        "l2": "no flush; inputs larger than L2 (each step touches ~565 MB against 129 MB of L2)",
                        "parallelism": f"replicas x{ws} (tokens are independent; no collective)"},

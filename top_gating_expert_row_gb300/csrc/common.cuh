@@ -100,11 +100,16 @@ __device__ __forceinline__ float exp2_hw(float f)
 
 __device__ __forceinline__ float exp_value(float x)
 {
+    // n = rint(x*log2 e) by adding 1.5*2^23: the sum's low mantissa bits hold n
+    // (|n| < 2^22), and since the shifter's own bits vanish when shifted left
+    // by 23, (bits of t) << 23 is exactly n << 23, the exponent increment.
+    constexpr float kShifter = 12582912.0f;  // 1.5 * 2^23
     x = fmaxf(x, -87.0f);
-    const float n = rintf(__fmul_rn(x, kLog2eHi));
+    const float t = __fmaf_rn(x, kLog2eHi, kShifter);
+    const float n = __fsub_rn(t, kShifter);
     float f = __fmaf_rn(x, kLog2eHi, -n);
     f = __fmaf_rn(x, kLog2eLo, f);
-    return __int_as_float(__float_as_int(exp2_hw(f)) + (__float2int_rn(n) << 23));
+    return __int_as_float(__float_as_int(exp2_hw(f)) + (__float_as_int(t) << 23));
 }
 
 // Logistic function 1 / (1 + exp(-x)), IEEE add and correctly rounded
@@ -129,8 +134,9 @@ __device__ __forceinline__ uint32_t key_of(float f)
 
 __device__ __forceinline__ float float_of(uint32_t k)
 {
-    const uint32_t m = (k & 0x80000000u) ? 0x80000000u : 0xffffffffu;
-    return __uint_as_float(k ^ m);
+    // top bit set (non-negative float): flip the top bit; else flip all bits
+    const uint32_t s = static_cast<uint32_t>(static_cast<int32_t>(k) >> 31);
+    return __uint_as_float(k ^ (~s | 0x80000000u));
 }
 
 // ---------------------------------------------------------------------------

@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kFwdThreads, fwd_min_blocks(NV)) k_router_fwd(
 
 // Wide rows (E > 1024): the row lives in shared memory, one warp per row.
 template <bool SELECT, bool FULL>
-__global__ void __launch_bounds__(kWideThreads) k_router_fwd_wide(RouteArgs a)
+__global__ void __launch_bounds__(kWideThreads, kWideMinBlocks) k_router_fwd_wide(RouteArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -35,6 +35,9 @@ constexpr int kFusedMaxNv = 8;
 // wider rows take the shared-memory routine, two warps per CTA.
 constexpr int kRegisterMaxNv = 8;
 constexpr int kWideThreads = 64;
+// Registers are capped so that shared memory, not registers, bounds residency
+// (a 9 KB key row per warp at E = 2304 allows about 22 warps per SM).
+constexpr int kWideMinBlocks = 10;
 
 struct SortArgs {
     int32_t* ids;

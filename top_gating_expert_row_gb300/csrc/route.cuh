@@ -291,8 +291,6 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
     }
 
     // 3. selection
-    uint32_t K = 0u, I = 0u;
-    bool partial_ties = false;  // SELECT: some keys equal to the last winner's key lost
     if (!SELECT) {
         // k_r rounds of arg-max; a winner's key becomes 1 (below every real key,
         // above the 0 of padding / dropped groups), which also marks it chosen.
@@ -422,7 +420,6 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
                 base += tot;
             }
             n = min(base, lim);
-            partial_ties = true;
         }
         n = min(n, cap);
         const uint32_t warm_rank = min(n - 1u, static_cast<uint32_t>(k_r + k_r / 2));
@@ -451,23 +448,13 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
                     if (r < static_cast<uint32_t>(k_r)) {
                         win_idx[r] = idx;
                         win_val[r] = __fmul_rn(vbuf[min(idx, static_cast<uint32_t>(E - 1))], vmul);
-                        if (r == static_cast<uint32_t>(k_r - 1)) {
-                            scal[0] = kk;
-                            scal[1] = idx;
-                        }
-                    } else if (r == static_cast<uint32_t>(k_r)) {
-                        scal[2] = kk;  // the best loser's key
                     }
                     if (r == warm_rank) scal[3] = kk;
                 }
             }
         }
         __syncwarp();
-        K = scal[0];
-        I = scal[1];
         warm = scal[3];
-        // some key equal to K lost only if the best loser (when there is one) ties K
-        partial_ties = partial_ties || (n > static_cast<uint32_t>(k_r) && scal[2] == K);
     }
     __syncwarp();
 
@@ -477,7 +464,9 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
     wsum = warp_sum(wsum);
     const float scale = a.renorm ? (wsum > 0.0f ? __fdiv_rn(a.scaling, wsum) : 0.0f) : a.scaling;
 
-    // 5. emit the dense rows (compact outputs: emit_compact)
+    // 5. dense rows: intermediate = s; probs and routing_map are written as zero
+    //    vectors and the k_r winners are patched in afterwards (compact outputs:
+    //    emit_compact)
     if (a.probs || a.map || a.inter) {
         InT* prow = a.probs ? static_cast<InT*>(a.probs) + static_cast<size_t>(t) * E : nullptr;
         uint8_t* mrow = a.map ? a.map + static_cast<size_t>(t) * E : nullptr;
@@ -486,38 +475,33 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
         for (int v = 0; v < NV; ++v) {
             const int e0 = v * 128 + lane4;
             if (e0 >= E) continue;
-            float s4[4], p4[4];
-            if (whole(v)) {
-                const float4 q = *reinterpret_cast<const float4*>(vbuf + e0);
-                s4[0] = q.x; s4[1] = q.y; s4[2] = q.z; s4[3] = q.w;
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) s4[c] = inside(v, c) ? vbuf[e0 + c] : 0.0f;
-            }
-            uint32_t m4 = 0u;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint32_t k = key[v][c];
-                bool member;
-                if (!SELECT) member = (k == 1u);
-                else if (!partial_ties) member = (k >= K);
-                else member = (k > K) || (k == K && static_cast<uint32_t>(e0 + c) <= I);
-                s4[c] = __fmul_rn(s4[c], vmul);
-                p4[c] = __fmul_rn(s4[c], member ? scale : 0.0f);
-                m4 |= (member ? 1u : 0u) << (8 * c);
-            }
             if (a.vec && whole(v)) {
-                if (prow) store4<InT>(prow + e0, p4);
-                if (mrow) *reinterpret_cast<uint32_t*>(mrow + e0) = m4;
-                if (irow) *reinterpret_cast<float4*>(irow + e0) = make_float4(s4[0], s4[1], s4[2], s4[3]);
+                if (irow) {
+                    const float4 q = *reinterpret_cast<const float4*>(vbuf + e0);
+                    *reinterpret_cast<float4*>(irow + e0) =
+                        make_float4(__fmul_rn(q.x, vmul), __fmul_rn(q.y, vmul), __fmul_rn(q.z, vmul), __fmul_rn(q.w, vmul));
+                }
+                if (prow) {
+                    const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    store4<InT>(prow + e0, z);
+                }
+                if (mrow) *reinterpret_cast<uint32_t*>(mrow + e0) = 0u;
             } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     if (!inside(v, c)) break;
-                    if (prow) store_scalar<InT>(prow + e0 + c, p4[c]);
-                    if (mrow) mrow[e0 + c] = static_cast<uint8_t>((m4 >> (8 * c)) & 1u);
-                    if (irow) irow[e0 + c] = s4[c];
+                    if (irow) irow[e0 + c] = __fmul_rn(vbuf[e0 + c], vmul);
+                    if (prow) store_scalar<InT>(prow + e0 + c, 0.0f);
+                    if (mrow) mrow[e0 + c] = 0;
                 }
+            }
+        }
+        __syncwarp();  // the winners' writes below land after the zeros above
+        if (prow || mrow) {
+            for (int j = lane; j < k_r; j += 32) {
+                const uint32_t idx = min(win_idx[j], static_cast<uint32_t>(E - 1));
+                if (prow) store_scalar<InT>(prow + idx, __fmul_rn(win_val[j], scale));
+                if (mrow) mrow[idx] = 1;
             }
         }
     }

@@ -188,8 +188,6 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
     }
 
     // 3. selection
-    uint32_t K = 0u, I = 0u;
-    bool partial_ties = false;
     if (!SELECT) {
         // k_r rounds of arg-max; round j only considers keys that come after the
         // previous winner in selection order (keys stay intact: softmax scores
@@ -219,9 +217,6 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
             Kp = wmax;
             Ip = widx;
         }
-        K = Kp;
-        I = Ip;
-        partial_ties = true;
     } else {
         unsigned long long* cand = reinterpret_cast<unsigned long long*>(wsm + L.cand);
         const uint32_t cap = static_cast<uint32_t>(a.stop);
@@ -323,7 +318,6 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
                 base += tot;
             }
             n = min(base, lim);
-            partial_ties = true;
         }
         n = min(n, cap);
         const uint32_t warm_rank = min(n - 1u, static_cast<uint32_t>(k_r + k_r / 4));
@@ -351,22 +345,13 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
                     if (r < static_cast<uint32_t>(k_r)) {
                         win_idx[r] = idx;
                         win_val[r] = score_of(idx, kk);
-                        if (r == static_cast<uint32_t>(k_r - 1)) {
-                            scal[0] = kk;
-                            scal[1] = idx;
-                        }
-                    } else if (r == static_cast<uint32_t>(k_r)) {
-                        scal[2] = kk;
                     }
                     if (r == warm_rank) scal[3] = kk;
                 }
             }
         }
         __syncwarp();
-        K = scal[0];
-        I = scal[1];
         warm = scal[3];
-        partial_ties = partial_ties || (n > static_cast<uint32_t>(k_r) && scal[2] == K);
     }
     __syncwarp();
 
@@ -376,65 +361,47 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
     wsum = warp_sum(wsum);
     const float scale = a.renorm ? (wsum > 0.0f ? __fdiv_rn(a.scaling, wsum) : 0.0f) : a.scaling;
 
-    // 5. dense rows
+    // 5. dense rows: intermediate = s; probs and routing_map are written as zero
+    //    vectors and the k_r winners are patched in afterwards, so no per-element
+    //    membership test is needed
     if (a.probs || a.map || a.inter) {
         InT* prow = a.probs ? static_cast<InT*>(a.probs) + static_cast<size_t>(t) * E : nullptr;
         uint8_t* mrow = a.map ? a.map + static_cast<size_t>(t) * E : nullptr;
         float* irow = a.inter ? a.inter + static_cast<size_t>(t) * E : nullptr;
+        // sigmoid scores in the intermediate row are final already
+        const bool fix_inter = irow && SCORE == kSoftmax;
 #pragma unroll 4
         for (int v = 0; v < nv; ++v) {
             const int e0 = v * 128 + lane4;
             if (!FULL && e0 >= E) continue;
-            const uint4 q = k4(v);
-            const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
-            float s4[4], p4[4];
-            const bool vw = vec && whole(v);
-            if (irow) {  // the scores pass left them in the intermediate row
-                if (vw) {
-                    const float4 sq = __ldcg(reinterpret_cast<const float4*>(irow + e0));
-                    s4[0] = sq.x; s4[1] = sq.y; s4[2] = sq.z; s4[3] = sq.w;
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) s4[c] = (e0 + c < E) ? __ldcg(irow + e0 + c) : 0.0f;
+            if (vec && whole(v)) {
+                if (fix_inter) {
+                    float4 q = __ldcg(reinterpret_cast<const float4*>(irow + e0));
+                    q.x = __fmul_rn(q.x, vmul); q.y = __fmul_rn(q.y, vmul);
+                    q.z = __fmul_rn(q.z, vmul); q.w = __fmul_rn(q.w, vmul);
+                    *reinterpret_cast<float4*>(irow + e0) = q;
                 }
-                if (SCORE == kSoftmax) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) s4[c] = __fmul_rn(s4[c], vmul);
+                if (prow) {
+                    const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    store4<InT>(prow + e0, z);
                 }
-            } else if (SCORE == kSoftmax) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float ev = __fmul_rn(exp_value(__fsub_rn(float_of(kq[c]), m)), vmul);
-                    s4[c] = kq[c] ? ev : 0.0f;
-                }
-            } else {
-                const float4 sq = *reinterpret_cast<const float4*>(vbuf + e0);
-                s4[0] = sq.x; s4[1] = sq.y; s4[2] = sq.z; s4[3] = sq.w;
-            }
-            uint32_t m4 = 0u;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint32_t k = kq[c];
-                bool member;
-                if (!partial_ties) member = (k >= K);
-                else member = (k > K) || (k == K && static_cast<uint32_t>(e0 + c) <= I);
-                p4[c] = __fmul_rn(s4[c], member ? scale : 0.0f);
-                m4 |= (member ? 1u : 0u) << (8 * c);
-            }
-            // (normal stores: the backward usually reads these rows next, from L2)
-            const bool wi = irow && SCORE == kSoftmax;  // sigmoid scores are final already
-            if (vw) {
-                if (prow) store4<InT>(prow + e0, p4);
-                if (mrow) *reinterpret_cast<uint32_t*>(mrow + e0) = m4;
-                if (wi) *reinterpret_cast<float4*>(irow + e0) = make_float4(s4[0], s4[1], s4[2], s4[3]);
+                if (mrow) *reinterpret_cast<uint32_t*>(mrow + e0) = 0u;
             } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     if (e0 + c >= E) break;
-                    if (prow) store_scalar<InT>(prow + e0 + c, p4[c]);
-                    if (mrow) mrow[e0 + c] = static_cast<uint8_t>((m4 >> (8 * c)) & 1u);
-                    if (wi) irow[e0 + c] = s4[c];
+                    if (fix_inter) irow[e0 + c] = __fmul_rn(__ldcg(irow + e0 + c), vmul);
+                    if (prow) store_scalar<InT>(prow + e0 + c, 0.0f);
+                    if (mrow) mrow[e0 + c] = 0;
                 }
+            }
+        }
+        __syncwarp();  // the winners' writes below land after the zeros above
+        if (prow || mrow) {
+            for (int j = lane; j < k_r; j += 32) {
+                const uint32_t idx = min(win_idx[j], static_cast<uint32_t>(E - 1));
+                if (prow) store_scalar<InT>(prow + idx, __fmul_rn(win_val[j], scale));
+                if (mrow) mrow[idx] = 1;
             }
         }
     }
