@@ -421,7 +421,8 @@ int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int
     const int k_r = p->topk - p->n_shared;
     if (p->T <= MR_MAX_FUSED_TOKENS && kNvBuckets[nv] <= kFusedMaxNv) {
         RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, topk_idx, topk_w);
-        SortArgs s{sorted_token_ids, sorted_weights, expert_ids, num_tokens_post_pad, E_tot, block_m};
+        SortArgs s{sorted_token_ids, sorted_weights, expert_ids, num_tokens_post_pad, E_tot, block_m,
+                   log2_if_pow2(block_m)};
         // a one-CTA decode launch is bound by instruction fetch on a cold SM: the
         // arg-max path has the shorter code, so it is the default up to k_r = 32
         const bool sel = g_path.force == 2 || (g_path.force == 0 && k_r > 32);

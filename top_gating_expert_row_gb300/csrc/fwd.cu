@@ -120,10 +120,17 @@ __global__ void __launch_bounds__(kFusedThreads) k_fused_decode(RouteArgs a, Sor
         uint32_t warm = 0u;
         const float scale = route_row<kScore, InT, NV, SELECT>(a, warp, wsm, L, lane, warm);
         const size_t o = static_cast<size_t>(warp) * a.topk;
-        emit_compact(a, wsm, L, scale, lane, s_idx + o, s_w + o);
-        if (a.topk_idx || a.topk_w)
-            emit_compact(a, wsm, L, scale, lane, a.topk_idx ? a.topk_idx + o : nullptr,
-                         a.topk_w ? a.topk_w + o : nullptr);
+        const uint32_t* win_idx = reinterpret_cast<const uint32_t*>(wsm + L.win_idx);
+        const float* win_val = reinterpret_cast<const float*>(wsm + L.win_val);
+        for (int j = lane; j < a.topk; j += 32) {  // compact outputs, to shared and global
+            const bool routed = j < a.k_r;
+            const int32_t id = routed ? static_cast<int32_t>(win_idx[j]) : a.E + (j - a.k_r);
+            const float wv = routed ? __fmul_rn(win_val[j], scale) : a.shared_weight;
+            s_idx[o + j] = id;
+            s_w[o + j] = wv;
+            if (a.topk_idx) a.topk_idx[o + j] = id;
+            if (a.topk_w) a.topk_w[o + j] = wv;
+        }
     }
     __syncthreads();
     if (warp < a.T) {
@@ -135,22 +142,27 @@ __global__ void __launch_bounds__(kFusedThreads) k_fused_decode(RouteArgs a, Sor
     }
     __syncthreads();
     // one warp: padded counts -> exclusive offsets, block -> expert map
+    // (a power-of-two block_m, the usual case, pads with a mask, not a division)
     if (warp == 0) {
+        const int sh = s.bm_shift;
+        auto nblocks = [&](uint32_t c) {
+            return sh >= 0 ? (c + bm - 1) >> sh : (c + bm - 1) / static_cast<uint32_t>(bm);
+        };
         const int per = (E_tot + 31) / 32;
         const int e0 = lane * per;
         uint32_t local = 0u;
         for (int i = 0; i < per; ++i)
-            if (e0 + i < E_tot) local += (__popc(mask[e0 + i]) + bm - 1) / bm * bm;
-        uint32_t run = warp_exclusive_scan(local, lane);
+            if (e0 + i < E_tot) local += nblocks(__popc(mask[e0 + i]));
+        uint32_t run = warp_exclusive_scan(local, lane);  // in blocks
         for (int i = 0; i < per; ++i) {
             const int e = e0 + i;
             if (e >= E_tot) break;
-            const uint32_t c = __popc(mask[e]);
-            off[e] = run;
-            const int nb = static_cast<int>((c + bm - 1) / bm);
-            for (int b = 0; b < nb; ++b) blk[run / bm + b] = e;
-            run += nb * bm;
+            const uint32_t nb = nblocks(__popc(mask[e]));
+            off[e] = run * bm;
+            for (uint32_t b = 0; b < nb; ++b) blk[run + b] = e;
+            run += nb;
         }
+        run *= bm;
         if (lane == 31) {
             off[E_tot] = run;
             *s.num_post_pad = static_cast<int32_t>(run);

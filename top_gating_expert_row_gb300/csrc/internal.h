@@ -46,7 +46,16 @@ struct SortArgs {
     int32_t* num_post_pad;
     int E_tot;
     int block_m;
+    int bm_shift;  // log2(block_m) when block_m is a power of two, else -1
 };
+
+inline int log2_if_pow2(int x)
+{
+    if (x <= 0 || (x & (x - 1))) return -1;
+    int s = 0;
+    while ((1 << s) < x) ++s;
+    return s;
+}
 
 // Shared memory of the fused decode kernel after the warp regions: the T*topk
 // pairs, one token bitmask per expert, the padded offsets and the

@@ -384,8 +384,8 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
             for (int v = 0; v < NV; ++v)
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    if (key[v][c] >= lo) {
-                        if (pos < cap) cand[pos] = comp(key[v][c], v, c);
+                    if (key[v][c] >= lo) {  // exact counts keep pos below cnt_lo <= cap
+                        cand[pos] = comp(key[v][c], v, c);
                         ++pos;
                     }
             n = cnt_lo;

@@ -281,8 +281,10 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
                 const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
+                    // positions come from exact counts of these same keys, so
+                    // pos stays below cnt_lo <= cap
                     const bool in = kq[c] >= lo;
-                    if (in && pos < cap) cand[pos] = comp(kq[c], e0 + c);
+                    if (in) cand[pos] = comp(kq[c], e0 + c);
                     pos += in ? 1u : 0u;
                 }
             }
