@@ -134,29 +134,39 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
     if (SCORE == kSoftmax) {
         m = float_of(kmax);
         float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 4
-        for (int v = 0; v < nv; ++v) {
-            const uint4 q = k4(v);
-            // padding keys are 0: their numerator is dropped (computed, then selected away)
-            const float e0 = exp_value(__fsub_rn(float_of(q.x), m));
-            const float e1 = exp_value(__fsub_rn(float_of(q.y), m));
-            const float e2 = exp_value(__fsub_rn(float_of(q.z), m));
-            const float e3 = exp_value(__fsub_rn(float_of(q.w), m));
-            const float4 e = FULL ? make_float4(e0, e1, e2, e3)
-                                  : make_float4(q.x ? e0 : 0.0f, q.y ? e1 : 0.0f, q.z ? e2 : 0.0f, q.w ? e3 : 0.0f);
-            sum[0] = __fadd_rn(sum[0], e.x);
-            sum[1] = __fadd_rn(sum[1], e.y);
-            sum[2] = __fadd_rn(sum[2], e.z);
-            sum[3] = __fadd_rn(sum[3], e.w);
-            if (irow0) {
-                const int o = v * 128 + lane4;
-                if (vec && whole(v)) {
-                    *reinterpret_cast<float4*>(irow0 + o) = e;
-                } else {
-                    const float ev[4] = {e.x, e.y, e.z, e.w};
+        // batches of 4 chunks, keys loaded first: with generic pointers the
+        // compiler cannot move a later shared load above an earlier global store
+        for (int v0 = 0; v0 < nv; v0 += 4) {
+            uint4 qb[4];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        if (o + c < E) irow0[o + c] = ev[c];
+            for (int u = 0; u < 4; ++u)
+                qb[u] = (v0 + u < nv) ? k4(v0 + u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int v = v0 + u;
+                if (v >= nv) break;
+                const uint4 q = qb[u];
+                // padding keys are 0: their numerator is dropped (computed, then selected away)
+                const float e0 = exp_value(__fsub_rn(float_of(q.x), m));
+                const float e1 = exp_value(__fsub_rn(float_of(q.y), m));
+                const float e2 = exp_value(__fsub_rn(float_of(q.z), m));
+                const float e3 = exp_value(__fsub_rn(float_of(q.w), m));
+                const float4 e = FULL ? make_float4(e0, e1, e2, e3)
+                                      : make_float4(q.x ? e0 : 0.0f, q.y ? e1 : 0.0f, q.z ? e2 : 0.0f, q.w ? e3 : 0.0f);
+                sum[0] = __fadd_rn(sum[0], e.x);
+                sum[1] = __fadd_rn(sum[1], e.y);
+                sum[2] = __fadd_rn(sum[2], e.z);
+                sum[3] = __fadd_rn(sum[3], e.w);
+                if (irow0) {
+                    const int o = v * 128 + lane4;
+                    if (vec && whole(v)) {
+                        *reinterpret_cast<float4*>(irow0 + o) = e;
+                    } else {
+                        const float ev[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            if (o + c < E) irow0[o + c] = ev[c];
+                    }
                 }
             }
         }
@@ -274,18 +284,23 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
         if (cnt_lo <= cap) {
             if (lane_lo < 0) lane_lo = static_cast<int>(count_ge(lo));
             uint32_t pos = warp_exclusive_scan(static_cast<uint32_t>(lane_lo), lane);
-#pragma unroll 2
-            for (int v = 0; v < nv; ++v) {
-                const uint4 q = k4(v);
-                const uint32_t e0 = static_cast<uint32_t>(v * 128 + lane4);
-                const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+            for (int v0 = 0; v0 < nv; v0 += 4) {
+                uint4 qb[4];  // keys first (see the exp pass)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    // positions come from exact counts of these same keys, so
-                    // pos stays below cnt_lo <= cap
-                    const bool in = kq[c] >= lo;
-                    if (in) cand[pos] = comp(kq[c], e0 + c);
-                    pos += in ? 1u : 0u;
+                for (int u = 0; u < 4; ++u)
+                    qb[u] = (v0 + u < nv) ? k4(v0 + u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t e0 = static_cast<uint32_t>((v0 + u) * 128 + lane4);
+                    const uint32_t kq[4] = {qb[u].x, qb[u].y, qb[u].z, qb[u].w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        // positions come from exact counts of these same keys, so
+                        // pos stays below cnt_lo <= cap (padding keys 0 never pass)
+                        const bool in = kq[c] >= lo;
+                        if (in) cand[pos] = comp(kq[c], e0 + c);
+                        pos += in ? 1u : 0u;
+                    }
                 }
             }
             n = cnt_lo;
@@ -372,29 +387,55 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
         float* irow = a.inter ? a.inter + static_cast<size_t>(t) * E : nullptr;
         // sigmoid scores in the intermediate row are final already
         const bool fix_inter = irow && SCORE == kSoftmax;
-#pragma unroll 4
-        for (int v = 0; v < nv; ++v) {
-            const int e0 = v * 128 + lane4;
-            if (!FULL && e0 >= E) continue;
-            if (vec && whole(v)) {
-                if (fix_inter) {
-                    float4 q = __ldcg(reinterpret_cast<const float4*>(irow + e0));
-                    q.x = __fmul_rn(q.x, vmul); q.y = __fmul_rn(q.y, vmul);
-                    q.z = __fmul_rn(q.z, vmul); q.w = __fmul_rn(q.w, vmul);
-                    *reinterpret_cast<float4*>(irow + e0) = q;
-                }
-                if (prow) {
-                    const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                    store4<InT>(prow + e0, z);
-                }
-                if (mrow) *reinterpret_cast<uint32_t*>(mrow + e0) = 0u;
-            } else {
+        if (FULL) {
+            // batches of 4 chunks: all loads first (the output rows might alias
+            // for the compiler, so it would not hoist them past the stores)
+            for (int v0 = 0; v0 < nv; v0 += 4) {
+                float4 q[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (e0 + c >= E) break;
-                    if (fix_inter) irow[e0 + c] = __fmul_rn(__ldcg(irow + e0 + c), vmul);
-                    if (prow) store_scalar<InT>(prow + e0 + c, 0.0f);
-                    if (mrow) mrow[e0 + c] = 0;
+                for (int u = 0; u < 4; ++u)
+                    if (fix_inter && v0 + u < nv)
+                        q[u] = __ldcg(reinterpret_cast<const float4*>(irow + (v0 + u) * 128 + lane4));
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (v0 + u >= nv) break;
+                    const int e0 = (v0 + u) * 128 + lane4;
+                    if (fix_inter) {
+                        q[u].x = __fmul_rn(q[u].x, vmul); q[u].y = __fmul_rn(q[u].y, vmul);
+                        q[u].z = __fmul_rn(q[u].z, vmul); q[u].w = __fmul_rn(q[u].w, vmul);
+                        *reinterpret_cast<float4*>(irow + e0) = q[u];
+                    }
+                    if (prow) {
+                        const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        store4<InT>(prow + e0, z);
+                    }
+                    if (mrow) *reinterpret_cast<uint32_t*>(mrow + e0) = 0u;
+                }
+            }
+        } else {
+            for (int v = 0; v < nv; ++v) {
+                const int e0 = v * 128 + lane4;
+                if (e0 >= E) continue;
+                if (vec && whole(v)) {
+                    if (fix_inter) {
+                        float4 q = __ldcg(reinterpret_cast<const float4*>(irow + e0));
+                        q.x = __fmul_rn(q.x, vmul); q.y = __fmul_rn(q.y, vmul);
+                        q.z = __fmul_rn(q.z, vmul); q.w = __fmul_rn(q.w, vmul);
+                        *reinterpret_cast<float4*>(irow + e0) = q;
+                    }
+                    if (prow) {
+                        const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        store4<InT>(prow + e0, z);
+                    }
+                    if (mrow) *reinterpret_cast<uint32_t*>(mrow + e0) = 0u;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        if (e0 + c >= E) break;
+                        if (fix_inter) irow[e0 + c] = __fmul_rn(__ldcg(irow + e0 + c), vmul);
+                        if (prow) store_scalar<InT>(prow + e0 + c, 0.0f);
+                        if (mrow) mrow[e0 + c] = 0;
+                    }
                 }
             }
         }
