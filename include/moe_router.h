@@ -48,7 +48,9 @@ typedef enum {
     MR_EINVAL = 1,       /* bad argument: null required pointer, size or option out of range */
     MR_EUNSUPPORTED = 2, /* valid on the pages but outside this library's limits (below) */
     MR_ECUDA = 3,        /* a CUDA launch or query failed */
-    MR_ERANGE = 4        /* (device status word only) an expert id outside [0, E_tot) was dropped */
+    MR_ERANGE = 4,       /* (device status word only) an expert id outside [0, E_tot) was dropped */
+    MR_ETIMEOUT = 8      /* (device status word only) a bounded in-kernel wait gave up; the
+                            outputs of the call that reported it are not valid */
 } mr_status;
 
 typedef enum { MR_SOFTMAX = 0, MR_SIGMOID = 1 } mr_score_fn;
@@ -223,6 +225,17 @@ const char* moe_router_strerror(int code);
  * concurrent calls. Returns MR_EINVAL for a negative threshold or unknown force_path.
  */
 int moe_router_set_topk_path(int select_threshold, int force_path);
+
+/*
+ * The library's per-device status word. Kernels that wait on an asynchronous copy
+ * (the forward on rows staged in shared memory) bound every wait; if one gives up,
+ * the kernel OR-s MR_ETIMEOUT into this word and stops. This call enqueues, on
+ * `stream`, a copy of the current device's word into *out (a device int32) and, if
+ * clear != 0, resets the word to 0 after copying it. Asynchronous like every other
+ * call: *out is valid once the stream reaches this point.
+ * Returns MR_EINVAL for a NULL out, MR_ECUDA on a failed launch.
+ */
+int moe_router_device_status(int32_t* out, int clear, mr_stream_t stream);
 
 /* Diagnostics (not part of the routing path):
  * moe_router_expf evaluates the library's device fp32 exponential on n values

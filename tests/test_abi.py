@@ -52,9 +52,13 @@ def test_binding_wraps_every_symbol(lib):
 
 
 def test_strerror(lib):
-    for code in range(5):
+    for code in (0, 1, 2, 3, 4, 8):
         assert lib.strerror(code).startswith("MR_")
     assert "unknown" in lib.strerror(99)
+
+
+def test_device_status_rejects_null_output(lib):
+    assert lib._lib.moe_router_device_status(None, 0, None) == lib.MR_EINVAL
 
 
 def _p(lib, **kw):

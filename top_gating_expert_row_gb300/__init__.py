@@ -22,7 +22,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoerouter.so")
 
-MR_OK, MR_EINVAL, MR_EUNSUPPORTED, MR_ECUDA, MR_ERANGE = 0, 1, 2, 3, 4
+MR_OK, MR_EINVAL, MR_EUNSUPPORTED, MR_ECUDA, MR_ERANGE, MR_ETIMEOUT = 0, 1, 2, 3, 4, 8
 MR_SOFTMAX, MR_SIGMOID = 0, 1
 MR_F32, MR_BF16 = 0, 1
 MR_MAX_FUSED_TOKENS = 16
@@ -57,6 +57,7 @@ _SIGS = {
     "moe_router_set_topk_path": ([_I, _I], _I),
     "moe_router_expf": ([_P, _P, _I, _P], _I),
     "moe_router_noop": ([_P], _I),
+    "moe_router_device_status": ([_P, _I, _P], _I),
 }
 
 
@@ -234,6 +235,18 @@ def moe_router_expf(x, y, stream=None) -> int:
 
 def moe_router_noop(stream=None) -> int:
     return _ok(_lib.moe_router_noop(_stream(stream)), "moe_router_noop")
+
+
+def moe_router_device_status(out, clear: bool = False, stream=None) -> int:
+    return _ok(_lib.moe_router_device_status(_ptr(out), 1 if clear else 0, _stream(stream)),
+               "moe_router_device_status")
+
+
+def device_status(clear: bool = False) -> int:
+    """The library's device status word on the current device (0, or MR_ETIMEOUT bits)."""
+    out = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe_router_device_status(out, clear)
+    return int(out.item())
 
 
 # ------------------------------------------------------------------- allocating helpers

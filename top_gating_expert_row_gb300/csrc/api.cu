@@ -123,6 +123,40 @@ int launch_noop(cudaStream_t st)
     return cudaGetLastError();
 }
 
+// ---- device status word ------------------------------------------------------------------------
+
+static_assert(kStatusTimeout == MR_ETIMEOUT, "device timeout bit and the C ABI's code must agree");
+
+// The library's status word on each device: kernels whose waits are bounded
+// OR MR_ETIMEOUT into it when one gives up.
+static __device__ uint32_t g_device_status;
+
+__global__ void k_take_status(uint32_t* word, int32_t* out, int clear)
+{
+    out[0] = static_cast<int32_t>(*word);
+    if (clear) *word = 0u;
+}
+
+namespace {
+std::mutex g_status_mu;
+void* g_status_ptr[64] = {nullptr};
+
+// Device address of g_device_status on the current device, looked up once per
+// device and cached (nullptr on failure).
+uint32_t* device_status_address()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = ptr;
+    }
+    return static_cast<uint32_t*>(g_status_ptr[dev]);
+}
+}  // namespace
+
 // ---- top-k path configuration -----------------------------------------------------------------
 
 namespace {
@@ -202,6 +236,7 @@ RouteArgs route_args(const mr_router_params* p, const void* logits, void* probs,
     a.scaling = p->scaling;
     a.shared_weight = p->shared_weight;
     a.stop = select_stop(a.k_r);
+    a.status = device_status_address();
     const uintptr_t in_al = p->in_dtype == MR_BF16 ? 8 : 16;
     a.vec = (p->E % 4 == 0) && aligned(logits, in_al) && aligned(probs, in_al) && aligned(inter, 16) &&
             aligned(map, 4) && aligned(p->bias, 16);
@@ -268,6 +303,7 @@ const char* moe_router_strerror(int code)
         case MR_EUNSUPPORTED: return "MR_EUNSUPPORTED: outside the library's supported limits";
         case MR_ECUDA: return "MR_ECUDA: CUDA launch or query failed";
         case MR_ERANGE: return "MR_ERANGE: expert id out of range (dropped)";
+        case MR_ETIMEOUT: return "MR_ETIMEOUT: a bounded in-kernel wait gave up (outputs not valid)";
     }
     return "unknown moe_router status";
 }
@@ -458,5 +494,14 @@ int moe_router_expf(const float* x, float* y, int n, mr_stream_t stream)
 }
 
 int moe_router_noop(mr_stream_t stream) { return from_cuda(launch_noop(reinterpret_cast<cudaStream_t>(stream))); }
+
+int moe_router_device_status(int32_t* out, int clear, mr_stream_t stream)
+{
+    if (!out) return MR_EINVAL;
+    uint32_t* word = device_status_address();
+    if (!word) return MR_ECUDA;
+    k_take_status<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(word, out, clear);
+    return from_cuda(cudaGetLastError());
+}
 
 }  // extern "C"

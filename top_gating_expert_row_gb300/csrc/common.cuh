@@ -183,6 +183,66 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
 }
 
 // ---------------------------------------------------------------------------
+// Bulk global -> shared copies completing on an mbarrier (the TMA engine, 1-D
+// form). Addresses 16-byte aligned, sizes a multiple of 16 bytes.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared accesses before later
+// async-proxy (bulk copy) writes to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_load_row(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// One wait attempt of at most about 1 us (the suspend-time hint, in ns).
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(1000u)
+        : "memory");
+    return ok != 0;
+}
+
+// Status bit a kernel OR-s into the library's device status word when a bounded
+// wait gives up (the C ABI's MR_ETIMEOUT).
+constexpr uint32_t kStatusTimeout = 8u;
+
+// Bounded wait (about a second at most) for phase `parity` of the barrier:
+// false if it gave up.
+constexpr uint32_t kWaitLimit = 1u << 20;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < kWaitLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// ---------------------------------------------------------------------------
 // Element access for logits (fp32 or bf16 storage, fp32 compute).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
@@ -210,6 +270,24 @@ template <>
 __device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, float (&x)[4])
 {
     const uint2 q = __ldcs(reinterpret_cast<const uint2*>(p));
+    x[0] = bf16_bits_to_f32(q.x & 0xffffu); x[1] = bf16_bits_to_f32(q.x >> 16);
+    x[2] = bf16_bits_to_f32(q.y & 0xffffu); x[3] = bf16_bits_to_f32(q.y >> 16);
+}
+
+// Four consecutive elements, starting at element e0 (a multiple of 4), of a row
+// held raw in shared memory at `base`.
+template <typename InT>
+__device__ __forceinline__ void load4_shared(const unsigned char* base, int e0, float (&x)[4]);
+template <>
+__device__ __forceinline__ void load4_shared<float>(const unsigned char* base, int e0, float (&x)[4])
+{
+    const float4 q = *reinterpret_cast<const float4*>(base + static_cast<size_t>(e0) * 4);
+    x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
+}
+template <>
+__device__ __forceinline__ void load4_shared<__nv_bfloat16>(const unsigned char* base, int e0, float (&x)[4])
+{
+    const uint2 q = *reinterpret_cast<const uint2*>(base + static_cast<size_t>(e0) * 2);
     x[0] = bf16_bits_to_f32(q.x & 0xffffu); x[1] = bf16_bits_to_f32(q.x >> 16);
     x[2] = bf16_bits_to_f32(q.y & 0xffffu); x[3] = bf16_bits_to_f32(q.y >> 16);
 }

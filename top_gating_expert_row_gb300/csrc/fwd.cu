@@ -73,11 +73,39 @@ __global__ void __launch_bounds__(kWideThreads, kWideMinBlocks) k_router_fwd_wid
     unsigned char* wsm = smem + static_cast<size_t>(warp) * L.bytes;
     const int stride = gridDim.x * nw;
     const uint32_t row_bytes = static_cast<uint32_t>(a.E) * sizeof(InT);
+    const InT* rows = static_cast<const InT*>(a.logits);
     uint32_t warm = 0u;
-    for (int t = blockIdx.x * nw + warp; t < a.T; t += stride) {
+    // FULL rows are staged in shared memory by bulk copies: the first one here,
+    // each next one while the previous row writes its outputs
+    Stage st;
+    st.bar = reinterpret_cast<uint64_t*>(wsm + L.bar);
+    st.bytes = row_bytes;
+    st.off = sizeof(InT) == 4 ? 0u : static_cast<uint32_t>(a.E) * 2u;
+    st.next = nullptr;
+    uint32_t phase = 0u;
+    int t = blockIdx.x * nw + warp;
+    if (FULL) {
+        if (lane == 0) mbar_init(st.bar, 1);
+        __syncwarp();
+        if (lane == 0 && t < a.T) bulk_load_row(wsm + L.kbuf + st.off, rows + static_cast<size_t>(t) * a.E, row_bytes,
+                                                st.bar);
+    }
+    for (; t < a.T; t += stride) {
         if (a.prefetch && lane == 0 && t + stride < a.T)
-            prefetch_l2(static_cast<const InT*>(a.logits) + static_cast<size_t>(t + stride) * a.E, row_bytes);
-        const float scale = route_row_wide<kScore, InT, SELECT, FULL>(a, t, wsm, L, lane, warm);
+            prefetch_l2(rows + static_cast<size_t>(t + stride) * a.E, row_bytes);
+        if (FULL) {
+            const bool ok = __all_sync(kFull, mbar_wait(st.bar, phase));
+            if (!ok) {
+                // the copy did not land within the wait limit: report it, give
+                // the copy one more bounded wait, and stop (no further rows)
+                if (lane == 0 && a.status) atomicOr(a.status, kStatusTimeout);
+                mbar_wait(st.bar, phase);
+                return;
+            }
+            phase ^= 1u;
+            st.next = t + stride < a.T ? rows + static_cast<size_t>(t + stride) * a.E : nullptr;
+        }
+        const float scale = route_row_wide<kScore, InT, SELECT, FULL>(a, t, wsm, L, lane, warm, st);
         if (a.topk_idx || a.topk_w) {
             const size_t o = static_cast<size_t>(t) * a.topk;
             const uint32_t* win_idx = reinterpret_cast<const uint32_t*>(wsm + L.win_idx);
@@ -235,7 +263,8 @@ FusedFn fused_kernel(int nv_idx)
 int MR_CAT(launch_fwd, MR_SUFFIX)(const RouteArgs& a, int nv_idx, bool select, cudaStream_t st)
 {
     if (kNvBuckets[nv_idx] > kRegisterMaxNv) {
-        const bool full = a.vec && a.E % 128 == 0;
+        // whole chunks and 16-byte aligned rows: the rows can be staged by bulk copies
+        const bool full = a.vec && a.prefetch && a.E % 128 == 0;
         const FwdFn f = select ? (full ? k_router_fwd_wide<true, true> : k_router_fwd_wide<true, false>)
                                : (full ? k_router_fwd_wide<false, true> : k_router_fwd_wide<false, false>);
         const WideLayout L = wide_layout(a.k_r, a.stop, a.E, select, kScore == kSigmoid && !a.inter);

@@ -25,11 +25,24 @@
 namespace mr {
 
 // Per-warp shared memory of the wide routine.
-//   kbuf   keys, nv*128 u32 (positions >= E hold 0, "not a candidate")
+//   kbuf   keys, nv*128 u32 (positions >= E hold 0, "not a candidate"); with
+//          staging it first receives the raw row (fp32 at its start, bf16 in
+//          its upper half) and the load pass turns it into keys in place
 //   vbuf   sigmoid scores when there is no intermediate output, nv*128 fp32
 //   win_*, cand, scal as in WarpLayout
+//   bar    mbarrier on which the staging copy completes
 struct WideLayout {
-    int kbuf, vbuf, win_idx, win_val, cand, scal, bytes;
+    int kbuf, vbuf, win_idx, win_val, cand, scal, bar, bytes;
+};
+
+// Staging of the next row: while a warp finishes row t (weights and dense
+// outputs, which no longer read kbuf) the bulk-copy engine brings row `next`
+// into kbuf, so the next row's load pass reads shared memory.
+struct Stage {
+    uint64_t* bar;
+    const void* next;  // nullptr: no next row for this warp
+    uint32_t bytes;    // row bytes (E * element size)
+    uint32_t off;      // byte offset of the raw row inside kbuf
 };
 
 __host__ __device__ inline WideLayout wide_layout(int k_r, int stop, int E, bool select, bool keep_scores)
@@ -43,15 +56,17 @@ __host__ __device__ inline WideLayout wide_layout(int k_r, int stop, int E, bool
     L.win_val = o; o += align16(k_r * 4);
     L.cand = o; o += select ? align16(stop * 8) : 0;
     L.scal = o; o += 16;
+    L.bar = o; o += 16;
     L.bytes = o;
     return L;
 }
 
 // FULL: every chunk is whole and vector-aligned (a.vec and E % 128 == 0), so the
-// per-chunk edge handling compiles away.
+// per-chunk edge handling compiles away; rows are then staged in shared memory
+// by the bulk-copy engine (the caller has waited for this row's copy).
 template <int SCORE, typename InT, bool SELECT, bool FULL>
 __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsigned char* wsm,
-                                                const WideLayout& L, int lane, uint32_t& warm)
+                                                const WideLayout& L, int lane, uint32_t& warm, const Stage& st)
 {
     uint32_t* kbuf = reinterpret_cast<uint32_t*>(wsm + L.kbuf);
     float* vbuf = reinterpret_cast<float*>(wsm + L.vbuf);
@@ -80,7 +95,9 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
             const int v = v0 + u;
             const int e0 = v * 128 + lane4;
             if (v < nv) {
-                if (vec && whole(v)) {
+                if (FULL) {
+                    load4_shared<InT>(wsm + L.kbuf + st.off, e0, x[u]);
+                } else if (vec && whole(v)) {
                     load4<InT>(row + e0, x[u]);
                 } else {
 #pragma unroll
@@ -88,6 +105,9 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
                 }
             }
         }
+        // bf16 staging: keys of a batch overwrite raw elements that other lanes
+        // read in this same batch (never in a later one)
+        if (FULL && sizeof(InT) == 2) __syncwarp();
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int v = v0 + u;
@@ -370,7 +390,11 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
         __syncwarp();
         warm = scal[3];
     }
+    // kbuf is free from here on: stage the next row into it. The proxy fence
+    // orders this lane's generic accesses to kbuf before the copy's writes.
+    if (FULL && st.next) fence_proxy_async_smem();
     __syncwarp();
+    if (FULL && st.next && lane == 0) bulk_load_row(wsm + L.kbuf + st.off, st.next, st.bytes, st.bar);
 
     // 4. weights
     float wsum = 0.0f;
