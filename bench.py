@@ -576,7 +576,8 @@ def main():
     dom_ms = tm.mean_ms(dom)
     achieved = nbytes[dom] / (dom_ms * 1e-3) / 1e9
     traffic = profiled_traffic() if dom == "fwd" else None
-    roofline = {"kernel": {"fwd": "k_router_fwd", "bwd": "k_router_bwd", "aux_fwd": "k_router_fwd (aux scores)",
+    fwd_kernel = "k_router_fwd_wide" if w.E > 1024 else "k_router_fwd"
+    roofline = {"kernel": {"fwd": fwd_kernel, "bwd": "k_router_bwd", "aux_fwd": f"{fwd_kernel} (aux scores)",
                            "aux_bwd": "k_router_bwd (aux scores)"}[dom],
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / pk["hbm_gbs"], 3), "peak_source": pk["source"] + " (hbm_gbs)",
