@@ -84,6 +84,12 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
     auto k4 = [&](int v) -> uint4& { return *reinterpret_cast<uint4*>(kbuf + v * 128 + lane4); };
 
     float* irow0 = a.inter ? a.inter + static_cast<size_t>(t) * E : nullptr;  // score scratch + output
+    // The previous row's threshold key, when there is one, is tested while the
+    // keys are made: cw = this lane's count of keys >= warm (0 is never a key
+    // of a real element, so warm = 0 means none).
+    const bool has_warm = SELECT && a.n_group == 0 && warm >= 2u;
+    const uint32_t wpiv = has_warm ? warm : 0xffffffffu;
+    uint32_t cw = 0u;
     // 1. load (8 chunks in flight), selection keys, sigmoid scores
     uint32_t lm = 0u;
     float m = 0.0f;    // softmax: the row max
@@ -147,22 +153,36 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
                 }
             }
             lm = max(lm, max(max(kk[0], kk[1]), max(kk[2], kk[3])));
+            if (SELECT) cw += (kk[0] >= wpiv) + (kk[1] >= wpiv) + (kk[2] >= wpiv) + (kk[3] >= wpiv);
             k4(v) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
         }
     }
     uint32_t kmax = __reduce_max_sync(kFull, lm);
+    // warm tested: its count decides whether it already bounds the candidates
+    const bool warm_tested = has_warm && wpiv <= kmax;
+    const uint32_t cnt_w = warm_tested ? __reduce_add_sync(kFull, cw) : 0u;
+    const uint32_t cap = static_cast<uint32_t>(a.stop);
+    // softmax: with k_r <= count(key >= warm) <= cap the candidates are known
+    // now and the exp pass below writes them out as it reads the keys
+    const bool fused_pick = SCORE == kSoftmax && warm_tested && cnt_w >= static_cast<uint32_t>(k_r) && cnt_w <= cap;
+    unsigned long long* cand = reinterpret_cast<unsigned long long*>(wsm + L.cand);
+    auto comp = [&](uint32_t k, uint32_t idx) {
+        return (static_cast<unsigned long long>(k) << 32) | static_cast<uint32_t>(~idx);
+    };
     if (SCORE == kSoftmax) {
         m = float_of(kmax);
+        uint32_t cpos = fused_pick ? warp_exclusive_scan(cw, lane) : 0u;
         float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        // batches of 4 chunks, keys loaded first: with generic pointers the
-        // compiler cannot move a later shared load above an earlier global store
-        for (int v0 = 0; v0 < nv; v0 += 4) {
-            uint4 qb[4];
+        // batches of kExpBatch chunks, keys loaded first: with generic pointers
+        // the compiler cannot move a later shared load above an earlier global store
+        constexpr int kExpBatch = 2;
+        for (int v0 = 0; v0 < nv; v0 += kExpBatch) {
+            uint4 qb[kExpBatch];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < kExpBatch; ++u)
                 qb[u] = (v0 + u < nv) ? k4(v0 + u) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kExpBatch; ++u) {
                 const int v = v0 + u;
                 if (v >= nv) break;
                 const uint4 q = qb[u];
@@ -177,6 +197,16 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
                 sum[1] = __fadd_rn(sum[1], e.y);
                 sum[2] = __fadd_rn(sum[2], e.z);
                 sum[3] = __fadd_rn(sum[3], e.w);
+                if (SELECT && fused_pick) {
+                    const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+                    const uint32_t e0i = static_cast<uint32_t>(v * 128 + lane4);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const bool in = kq[c] >= wpiv;
+                        if (in) cand[cpos] = comp(kq[c], e0i + c);
+                        cpos += in ? 1u : 0u;
+                    }
+                }
                 if (irow0) {
                     const int o = v * 128 + lane4;
                     if (vec && whole(v)) {
@@ -248,12 +278,17 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
             Ip = widx;
         }
     } else {
-        unsigned long long* cand = reinterpret_cast<unsigned long long*>(wsm + L.cand);
-        const uint32_t cap = static_cast<uint32_t>(a.stop);
         const uint32_t n_valid = static_cast<uint32_t>(a.n_group > 0 ? a.topk_group * (E / a.n_group) : E);
         uint32_t lo = 1u, hi = kmax + 1u;
         uint32_t cnt_lo = n_valid, cnt_hi = 0u;
         int lane_lo = -1, lane_hi = 0;
+        if (warm_tested) {  // the count made with the keys is the first bisection step
+            if (cnt_w >= static_cast<uint32_t>(k_r)) {
+                lo = wpiv; cnt_lo = cnt_w; lane_lo = static_cast<int>(cw);
+            } else {
+                hi = wpiv; cnt_hi = cnt_w; lane_hi = static_cast<int>(cw);
+            }
+        }
         auto count_ge = [&](uint32_t piv) {
             uint32_t c0 = 0u, c1 = 0u;
 #pragma unroll 4
@@ -267,7 +302,7 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
         // Invariant: count(key >= lo) = cnt_lo >= k_r > count(key >= hi) = cnt_hi.
         // Pivots: the previous row's threshold first, then value-space midpoints,
         // then key-space midpoints (at most 64 rounds in all).
-        for (int it = -1; it < 64 && cnt_lo > cap && hi - lo > 1u; ++it) {
+        for (int it = warm_tested ? 0 : -1; it < 64 && cnt_lo > cap && hi - lo > 1u; ++it) {
             uint32_t piv;
             if (it < 0) {
                 if (!(warm > lo && warm < hi)) continue;
@@ -297,11 +332,10 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
                 hi = piv; cnt_hi = tot; lane_hi = static_cast<int>(c);
             }
         }
-        auto comp = [&](uint32_t k, uint32_t idx) {
-            return (static_cast<unsigned long long>(k) << 32) | static_cast<uint32_t>(~idx);
-        };
         uint32_t n;
-        if (cnt_lo <= cap) {
+        if (fused_pick) {
+            n = cnt_lo;  // written by the exp pass
+        } else if (cnt_lo <= cap) {
             if (lane_lo < 0) lane_lo = static_cast<int>(count_ge(lo));
             uint32_t pos = warp_exclusive_scan(static_cast<uint32_t>(lane_lo), lane);
             for (int v0 = 0; v0 < nv; v0 += 4) {
