@@ -112,6 +112,22 @@ __device__ __forceinline__ float exp_value(float x)
     return __int_as_float(__float_as_int(exp2_hw(f)) + (__float_as_int(t) << 23));
 }
 
+// exp_value on two values at once: the same operations, with the floating-point
+// ones issued as packed fp32x2 instructions (each lane of a packed op rounds
+// exactly as the scalar op), so each result is bit-identical to exp_value's.
+__device__ __forceinline__ float2 exp_value2(float2 x)
+{
+    constexpr float kShifter = 12582912.0f;  // 1.5 * 2^23
+    x.x = fmaxf(x.x, -87.0f);
+    x.y = fmaxf(x.y, -87.0f);
+    const float2 t = __ffma2_rn(x, make_float2(kLog2eHi, kLog2eHi), make_float2(kShifter, kShifter));
+    const float2 n = __fadd2_rn(t, make_float2(-kShifter, -kShifter));
+    float2 f = __ffma2_rn(x, make_float2(kLog2eHi, kLog2eHi), make_float2(-n.x, -n.y));
+    f = __ffma2_rn(x, make_float2(kLog2eLo, kLog2eLo), f);
+    return make_float2(__int_as_float(__float_as_int(exp2_hw(f.x)) + (__float_as_int(t.x) << 23)),
+                       __int_as_float(__float_as_int(exp2_hw(f.y)) + (__float_as_int(t.y) << 23)));
+}
+
 // Logistic function 1 / (1 + exp(-x)), IEEE add and correctly rounded
 // reciprocal (the same number as an IEEE divide of 1 by the sum).
 __device__ __forceinline__ float sigmoid_f32(float x)

@@ -172,7 +172,8 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
     if (SCORE == kSoftmax) {
         m = float_of(kmax);
         uint32_t cpos = fused_pick ? warp_exclusive_scan(cw, lane) : 0u;
-        float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float2 sum01 = make_float2(0.0f, 0.0f), sum23 = make_float2(0.0f, 0.0f);
+        const float2 negm = make_float2(-m, -m);
         // batches of kExpBatch chunks, keys loaded first: with generic pointers
         // the compiler cannot move a later shared load above an earlier global store
         constexpr int kExpBatch = 2;
@@ -186,17 +187,15 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
                 const int v = v0 + u;
                 if (v >= nv) break;
                 const uint4 q = qb[u];
-                // padding keys are 0: their numerator is dropped (computed, then selected away)
-                const float e0 = exp_value(__fsub_rn(float_of(q.x), m));
-                const float e1 = exp_value(__fsub_rn(float_of(q.y), m));
-                const float e2 = exp_value(__fsub_rn(float_of(q.z), m));
-                const float e3 = exp_value(__fsub_rn(float_of(q.w), m));
-                const float4 e = FULL ? make_float4(e0, e1, e2, e3)
-                                      : make_float4(q.x ? e0 : 0.0f, q.y ? e1 : 0.0f, q.z ? e2 : 0.0f, q.w ? e3 : 0.0f);
-                sum[0] = __fadd_rn(sum[0], e.x);
-                sum[1] = __fadd_rn(sum[1], e.y);
-                sum[2] = __fadd_rn(sum[2], e.z);
-                sum[3] = __fadd_rn(sum[3], e.w);
+                // padding keys are 0: their numerator is dropped (computed, then selected away);
+                // x - m is computed as x + (-m), the same IEEE result
+                const float2 e01 = exp_value2(__fadd2_rn(make_float2(float_of(q.x), float_of(q.y)), negm));
+                const float2 e23 = exp_value2(__fadd2_rn(make_float2(float_of(q.z), float_of(q.w)), negm));
+                const float4 e = FULL ? make_float4(e01.x, e01.y, e23.x, e23.y)
+                                      : make_float4(q.x ? e01.x : 0.0f, q.y ? e01.y : 0.0f, q.z ? e23.x : 0.0f,
+                                                    q.w ? e23.y : 0.0f);
+                sum01 = __fadd2_rn(sum01, make_float2(e.x, e.y));
+                sum23 = __fadd2_rn(sum23, make_float2(e.z, e.w));
                 if (SELECT && fused_pick) {
                     const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
                     const uint32_t e0i = static_cast<uint32_t>(v * 128 + lane4);
@@ -220,7 +219,7 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
                 }
             }
         }
-        vmul = __frcp_rn(warp_sum(__fadd_rn(__fadd_rn(sum[0], sum[1]), __fadd_rn(sum[2], sum[3]))));
+        vmul = __frcp_rn(warp_sum(__fadd_rn(__fadd_rn(sum01.x, sum01.y), __fadd_rn(sum23.x, sum23.y))));
     }
     __syncwarp();  // scores written by one lane are read by another below
     // a winner's score: softmax recomputes it from the key; sigmoid reads it back
@@ -459,9 +458,9 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
                     if (v0 + u >= nv) break;
                     const int e0 = (v0 + u) * 128 + lane4;
                     if (fix_inter) {
-                        q[u].x = __fmul_rn(q[u].x, vmul); q[u].y = __fmul_rn(q[u].y, vmul);
-                        q[u].z = __fmul_rn(q[u].z, vmul); q[u].w = __fmul_rn(q[u].w, vmul);
-                        *reinterpret_cast<float4*>(irow + e0) = q[u];
+                        const float2 xy = __fmul2_rn(make_float2(q[u].x, q[u].y), make_float2(vmul, vmul));
+                        const float2 zw = __fmul2_rn(make_float2(q[u].z, q[u].w), make_float2(vmul, vmul));
+                        *reinterpret_cast<float4*>(irow + e0) = make_float4(xy.x, xy.y, zw.x, zw.y);
                     }
                     if (prow) {
                         const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
