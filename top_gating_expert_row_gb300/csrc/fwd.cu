@@ -91,7 +91,9 @@ __global__ void __launch_bounds__(kWideThreads, kWideMinBlocks) k_router_fwd_wid
                                                 st.bar);
     }
     for (; t < a.T; t += stride) {
-        if (a.prefetch && lane == 0 && t + stride < a.T)
+        // rows that are not staged stream into L2 one row ahead (staged rows do
+        // not gain from it: their bulk copy is issued about half a row ahead)
+        if (!FULL && a.prefetch && lane == 0 && t + stride < a.T)
             prefetch_l2(rows + static_cast<size_t>(t + stride) * a.E, row_bytes);
         if (FULL) {
             const bool ok = __all_sync(kFull, mbar_wait(st.bar, phase));
