@@ -117,9 +117,11 @@ def _tie_logits(kind, T, E):
 
 @pytest.mark.parametrize("path", [ARGMAX, SELECT], ids=["argmax", "select"])
 @pytest.mark.parametrize("kind", ["integers", "all_equal", "signed_zeros", "saturated_sigmoid", "two_values"])
-@pytest.mark.parametrize("E,k,fn", [(512, 36, SM), (256, 8, SG), (2304, 36, SG), (64, 3, SM)])
-def test_ties_go_to_lower_index(mr, orc, kind, E, k, fn, path):
-    w = W(f"ties_{kind}", 96, E, k, fn, renorm=1)
+@pytest.mark.parametrize("E,k,fn,T", [(512, 36, SM, 96), (256, 8, SG, 96), (2304, 36, SG, 96), (64, 3, SM, 96),
+                                       (2304, 36, SM, 3500)])
+def test_ties_go_to_lower_index(mr, orc, kind, E, k, fn, T, path):
+    # T=3500 gives every CTA of the persistent softmax wide-row grid several rows
+    w = W(f"ties_{kind}", T, E, k, fn, renorm=1)
     x = _tie_logits(kind, w.T, E)
     xg = x.cuda()
     out = gpu_route(mr, w, xg, None, path)

@@ -135,7 +135,9 @@ __device__ void group_limit(uint32_t* skeys, int E, int G, int gk, int m, int la
 // order); returns the factor that turns a score into its weight (dense probs
 // and compact weights are both s * factor, so they agree bit for bit).
 // ---------------------------------------------------------------------------
-template <int SCORE, typename InT, int NV, bool SELECT>
+// FULL: E == 128 * NV and a.vec, so every chunk is whole and vector-aligned and
+// the per-element edge tests compile away.
+template <int SCORE, typename InT, int NV, bool SELECT, bool FULL = false>
 __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned char* wsm,
                                            const WarpLayout& L, int lane, uint32_t& warm)
 {
@@ -148,8 +150,9 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
     const InT* row = static_cast<const InT*>(a.logits) + static_cast<size_t>(t) * E;
     const int lane4 = lane * 4;
     // a chunk (4 consecutive elements) is either whole or partly past E
-    auto whole = [&](int v) { return v * 128 + lane4 + 4 <= E; };
-    auto inside = [&](int v, int c) { return v * 128 + lane4 + c < E; };
+    auto whole = [&](int v) { return FULL || v * 128 + lane4 + 4 <= E; };
+    auto inside = [&](int v, int c) { return FULL || v * 128 + lane4 + c < E; };
+    const bool vec = FULL || a.vec;
 
     uint32_t key[NV][4];
     float vmul = 1.0f;  // vbuf * vmul = s
@@ -161,7 +164,7 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             const int e0 = v * 128 + lane4;
-            if (a.vec && whole(v)) {
+            if (vec && whole(v)) {
                 load4<InT>(row + e0, x[v]);
             } else {
 #pragma unroll
@@ -224,7 +227,7 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
                 const int e0 = v * 128 + lane4;
                 float b[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 if (a.bias) {
-                    if (a.vec && whole(v)) {
+                    if (vec && whole(v)) {
                         const float4 q = __ldg(reinterpret_cast<const float4*>(a.bias + e0));
                         b[0] = q.x; b[1] = q.y; b[2] = q.z; b[3] = q.w;
                     } else {
@@ -475,8 +478,8 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             const int e0 = v * 128 + lane4;
-            if (e0 >= E) continue;
-            if (a.vec && whole(v)) {
+            if (!FULL && e0 >= E) continue;
+            if (vec && whole(v)) {
                 if (irow) {
                     const float4 q = *reinterpret_cast<const float4*>(vbuf + e0);
                     *reinterpret_cast<float4*>(irow + e0) =
