@@ -63,6 +63,13 @@ def _load():
         lib.orc_sort_capacity.restype = ctypes.c_size_t
         lib.orc_sort.argtypes = [P, P] + [i32] * 4 + [P] * 4
         lib.orc_sort.restype = i32
+        i64, f64 = ctypes.c_int64, ctypes.c_double
+        lib.orc_tokens_per_expert.argtypes = [i32, i32, P, P]
+        lib.orc_tokens_per_expert.restype = i32
+        lib.orc_aux_loss_fwd.argtypes = [i32, i32, i32, f64, i64, P, P, P]
+        lib.orc_aux_loss_fwd.restype = i32
+        lib.orc_aux_loss_bwd.argtypes = [i32, i32, i32, f64, i64, P, f64, P]
+        lib.orc_aux_loss_bwd.restype = i32
         _lib = lib
     return _lib
 
@@ -177,3 +184,36 @@ def sort(topk_idx, topk_w, E_tot: int, block_m: int) -> dict:
     n = int(npp[0])
     return dict(sorted_token_ids=ids[:n], sorted_weights=sw[:n], expert_ids=eids[:n // block_m],
                 num_tokens_post_pad=n, dropped=dropped)
+
+
+def tokens_per_expert(routing_map) -> np.ndarray:
+    """Per-expert count of routed rows (column counts of a T x E routing map)."""
+    lib = _load()
+    m = _c(routing_map, np.uint8)
+    T, E = m.shape
+    out = np.empty(E, np.int32)
+    _check(lib.orc_tokens_per_expert(T, E, _p(m), _p(out)), "orc_tokens_per_expert")
+    return out
+
+
+def aux_loss_fwd(probs, tokens_per_expert, topk: int, coeff: float, total_num_tokens: int) -> float:
+    """The aux-loss scalar (switch-style load-balancing loss; see oracle.c)."""
+    lib = _load()
+    p = _c(probs, np.float64)
+    T, E = p.shape
+    c = _c(tokens_per_expert, np.int32)
+    loss = np.empty(1, np.float64)
+    _check(lib.orc_aux_loss_fwd(T, E, topk, coeff, total_num_tokens, _p(p), _p(c), _p(loss)), "orc_aux_loss_fwd")
+    return float(loss[0])
+
+
+def aux_loss_bwd(T: int, tokens_per_expert, topk: int, coeff: float, total_num_tokens: int,
+                 grad_loss: float) -> np.ndarray:
+    """d loss / d probs (T x E)."""
+    lib = _load()
+    c = _c(tokens_per_expert, np.int32)
+    E = c.shape[0]
+    g = np.empty((T, E), np.float64)
+    _check(lib.orc_aux_loss_bwd(T, E, topk, coeff, total_num_tokens, _p(c), grad_loss, _p(g)),
+           "orc_aux_loss_bwd")
+    return g

@@ -454,3 +454,68 @@ int orc_sort(const int32_t* topk_idx, const float* topk_w, int T, int topk, int 
     free(cnt);
     return dropped;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Aux-loss scalar ([TE] fused_moe_aux_loss).                                */
+/* ------------------------------------------------------------------------- */
+/*
+ * READING. [TE] names the fused_moe_aux_loss kernel (it consumes the scores and
+ * routing map of fused_score_for_moe_aux_loss) but prints no formula. It is
+ * read as the load-balancing loss of switch-style routing (Fedus, Zoph and
+ * Shazeer, "Switch Transformers", 2021, the auxiliary loss of section 2.2):
+ * with f_e the fraction of the routed slots that went to expert e and P_e the
+ * mean router probability of expert e,
+ *     loss = coeff * E * sum_e f_e * P_e,
+ *     f_e  = tokens_per_expert[e] / (topk * N),
+ *     P_e  = (sum_t probs[t][e]) / N,
+ * where N = total_num_tokens, the number of tokens the counts and the
+ * probabilities were taken over (it may exceed the T rows given here when the
+ * tokens are spread over several devices). tokens_per_expert is a count, so
+ * the gradient flows only through probs:
+ *     d loss / d probs[t][e] = coeff * E * f_e / N * grad_loss.
+ */
+
+/* tokens_per_expert[e] = number of rows t with routing_map[t][e] != 0. */
+int orc_tokens_per_expert(int T, int E, const uint8_t* routing_map, int32_t* tokens_per_expert)
+{
+    if (T < 0 || E < 1 || (T > 0 && !routing_map) || !tokens_per_expert) return -1;
+    for (int e = 0; e < E; ++e) {
+        int64_t c = 0;
+        for (int t = 0; t < T; ++t) c += routing_map[(size_t)t * E + e] != 0;
+        tokens_per_expert[e] = (int32_t)c;
+    }
+    return 0;
+}
+
+int orc_aux_loss_fwd(int T, int E, int topk, double coeff, int64_t total_num_tokens, const double* probs,
+                     const int32_t* tokens_per_expert, double* loss)
+{
+    if (T < 0 || E < 1 || topk < 1 || total_num_tokens < 1 || (T > 0 && !probs) || !tokens_per_expert ||
+        !loss)
+        return -1;
+    const double N = (double)total_num_tokens;
+    double acc = 0.0;
+    for (int e = 0; e < E; ++e) {
+        double colsum = 0.0;
+        for (int t = 0; t < T; ++t) colsum += probs[(size_t)t * E + e];
+        const double f = (double)tokens_per_expert[e] / ((double)topk * N);
+        const double P = colsum / N;
+        acc += f * P;
+    }
+    *loss = coeff * (double)E * acc;
+    return 0;
+}
+
+int orc_aux_loss_bwd(int T, int E, int topk, double coeff, int64_t total_num_tokens,
+                     const int32_t* tokens_per_expert, double grad_loss, double* grad_probs)
+{
+    if (T < 0 || E < 1 || topk < 1 || total_num_tokens < 1 || !tokens_per_expert || (T > 0 && !grad_probs))
+        return -1;
+    const double N = (double)total_num_tokens;
+    for (int e = 0; e < E; ++e) {
+        const double f = (double)tokens_per_expert[e] / ((double)topk * N);
+        const double g = coeff * (double)E * f / N * grad_loss;
+        for (int t = 0; t < T; ++t) grad_probs[(size_t)t * E + e] = g;
+    }
+    return 0;
+}

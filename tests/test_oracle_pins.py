@@ -411,3 +411,69 @@ def test_sort_capacity_is_tight(orc):
     idx = np.arange(12, dtype=np.int32).reshape(12, 1)
     out = orc.sort(idx, np.ones((12, 1), np.float32), 12, 8)
     assert out["num_tokens_post_pad"] == orc.sort_capacity(12, 1, 12, 8) == 96
+
+
+# --------------------------------------------------------------------------- aux-loss scalar
+
+
+def test_aux_loss_balanced_routing_gives_coeff(orc):
+    # every expert receives topk*T/E of the slots: f_e = 1/E, and softmax rows
+    # sum to one, so sum_e P_e = 1 and the loss is coeff whatever the probs are
+    T, E, k, coeff = 96, 12, 3, 0.01
+    x = synth.logits(T, E, sigma=2.0).float().numpy()
+    probs = orc.aux_scores_fwd(x, k, SM)["scores"]
+    counts = np.full(E, k * T // E, np.int32)
+    assert orc.aux_loss_fwd(probs, counts, k, coeff, T) == pytest.approx(coeff, rel=1e-12)
+    # uniform probabilities with balanced routing: the textbook minimum, coeff
+    assert orc.aux_loss_fwd(np.full((T, E), 1.0 / E), counts, k, coeff, T) == pytest.approx(coeff, rel=1e-12)
+
+
+def test_aux_loss_collapsed_routing_gives_coeff_times_E(orc):
+    # top-1, every token sent to expert 0 with probability one: f_0 = P_0 = 1
+    T, E, coeff = 50, 7, 0.3
+    probs = np.zeros((T, E))
+    probs[:, 0] = 1.0
+    counts = np.zeros(E, np.int32)
+    counts[0] = T
+    assert orc.aux_loss_fwd(probs, counts, 1, coeff, T) == pytest.approx(coeff * E, rel=1e-12)
+
+
+def test_aux_loss_scales_with_the_global_token_count(orc):
+    # the counts and probabilities of this device's rows, normalised by N:
+    # doubling N (the same rows, the rest of the tokens elsewhere) quarters it
+    rng = np.random.default_rng(5)
+    T, E, k = 40, 9, 2
+    probs = rng.random((T, E))
+    counts = rng.integers(0, 30, E).astype(np.int32)
+    a = orc.aux_loss_fwd(probs, counts, k, 0.1, T)
+    assert orc.aux_loss_fwd(probs, counts, k, 0.1, 2 * T) == pytest.approx(a / 4, rel=1e-12)
+
+
+def test_aux_loss_bwd_matches_finite_differences(orc):
+    rng = np.random.default_rng(6)
+    T, E, k, coeff, N, g = 6, 5, 2, 0.05, 11, 1.7
+    probs = rng.random((T, E))
+    counts = rng.integers(0, 9, E).astype(np.int32)
+    grad = orc.aux_loss_bwd(T, counts, k, coeff, N, g)
+    h = 1e-3
+    for t in range(T):
+        for e in range(E):
+            up, dn = probs.copy(), probs.copy()
+            up[t, e] += h
+            dn[t, e] -= h
+            fd = (orc.aux_loss_fwd(up, counts, k, coeff, N) - orc.aux_loss_fwd(dn, counts, k, coeff, N)) / (2 * h)
+            assert g * fd == pytest.approx(grad[t, e], rel=1e-8, abs=1e-14)
+
+
+def test_tokens_per_expert_counts_columns(orc):
+    # a map with a known column pattern: row t routes to experts t % E and (t + 3) % E
+    T, E = 60, 10
+    m = np.zeros((T, E), np.uint8)
+    for t in range(T):
+        m[t, t % E] = 1
+        m[t, (t + 3) % E] = 1
+    assert np.array_equal(orc.tokens_per_expert(m), np.full(E, 2 * T // E, np.int32))
+    # from a real top-k map: the counts add up to T*k
+    x = synth.logits(200, 33).float().numpy()
+    rm = orc.aux_scores_fwd(x, 5, SM)["routing_map"]
+    assert orc.tokens_per_expert(rm).sum() == 200 * 5
