@@ -373,6 +373,45 @@ def prefill_route_sort(mr, dev, stream, reps=20) -> dict:
             "route_plus_sort_us": round(r_us + s_us, 2), "num_tokens_post_pad": npp}
 
 
+def aux_loss_rates(mr, w, dev, stream, reps=50) -> dict:
+    """The aux-loss scalar on the step's aux scores: per-expert counts of the aux
+    routing map, the loss (column sums + final reduction) and its gradient."""
+    _, t, _ = make_step(mr, w, dev, stream)
+    L = mr._lib
+    s = stream.cuda_stream
+    T, E, k = w.T, w.E, w.topk
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    gl = torch.ones(1, dtype=torch.float32, device=dev)
+    grad = torch.empty(T, E, dtype=torch.float32, device=dev)
+    ws = torch.empty(mr.moe_aux_loss_workspace_bytes(T, E), dtype=torch.uint8, device=dev)
+    L.moe_aux_scores_fwd(T, E, k, w.score_fn, w.in_dtype, t["x"].data_ptr(), t["scores"].data_ptr(),
+                         t["amap"].data_ptr(), s)
+    calls = {
+        "tokens_per_expert": lambda: L.moe_tokens_per_expert(T, E, t["amap"].data_ptr(), counts.data_ptr(), s),
+        "loss_fwd": lambda: L.moe_aux_loss_fwd(T, E, k, 0.01, T, t["scores"].data_ptr(), counts.data_ptr(),
+                                               loss.data_ptr(), ws.data_ptr(), ws.numel(), s),
+        "loss_bwd": lambda: L.moe_aux_loss_bwd(T, E, k, 0.01, T, counts.data_ptr(), gl.data_ptr(), grad.data_ptr(), s),
+    }
+    nbytes = {"tokens_per_expert": T * E + E * 4, "loss_fwd": T * E * 4 + E * 4 + 4, "loss_bwd": T * E * 4 + E * 4 + 4}
+    tm = Timer(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            for fn in calls.values():
+                fn()
+        for _ in range(reps):
+            for n, fn in calls.items():
+                tm.around(n, fn)
+    torch.cuda.synchronize()
+    pk = peaks()["hbm_gbs"]
+    out = {"workload": f"T={T} E={E} topk={k} aux scores of the step"}
+    for n in calls:
+        us = tm.mean_ms(n) * 1e3
+        gbs = nbytes[n] / (us * 1e-6) / 1e9
+        out[n] = {"us": round(us, 2), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / pk, 3)}
+    return out
+
+
 def e2e_rate(mr, w, dev, stream, steps=5) -> dict:
     """The same step through the C ABI with host buffers: every step copies the
     inputs from pinned host memory and reads every output back."""
@@ -491,7 +530,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["all", "step", "decode"], default="all",
+    ap.add_argument("--only", choices=["all", "step", "decode", "aux_loss"], default="all",
                     help="step: the timed step only; decode: the decode latency table only "
                          "(both used for profiling captures)")
     ap.add_argument("--decode-calls", type=int, default=200, help="calls per decode timing loop")
@@ -519,6 +558,11 @@ def main():
             ts = tuple(int(t) for t in args.decode_ts.split(","))
             print(json.dumps({"decode": decode_latency(mr, dev, torch.cuda.Stream(device=dev),
                                                        args.decode_calls, ts)}), flush=True)
+        return 0
+    if args.only == "aux_loss":
+        if rank == 0:
+            print(json.dumps({"aux_loss": aux_loss_rates(mr, dev=dev, w=STEP_WORKLOADS[args.workload](),
+                                                         stream=torch.cuda.Stream(device=dev))}), flush=True)
         return 0
     if ws > 1:
         import torch.distributed as dist
@@ -599,6 +643,7 @@ def main():
         if rank == 0:
             line["decode"] = decode_latency(mr, dev, stream, args.decode_calls)
             line["prefill_route_sort"] = prefill_route_sort(mr, dev, stream)
+            line["aux_loss"] = aux_loss_rates(mr, w, dev, stream)
             breakdown = {}
             for wl in [synth.large_softmax(k) for k in synth.LARGE_TOPKS] + [synth.large_e_sigmoid()]:
                 breakdown[wl.name] = time_kernels(mr, wl, dev, stream)

@@ -142,6 +142,39 @@ int moe_aux_scores_bwd(int T, int E, int score_fn, const float* grad_scores, con
                        float* grad_logits, mr_stream_t stream);
 
 /*
+ * The aux-loss scalar ([TE] names fused_moe_aux_loss, which consumes the scores and
+ * routing map above, but prints no formula; it is read as the switch-style
+ * load-balancing loss: coeff * E * sum_e f_e * P_e with f_e the fraction of routed
+ * slots that chose e and P_e the mean probability of e):
+ *   loss = C * sum_e tokens_per_expert[e] * sum_t probs[t][e],
+ *   C = coeff * E / (topk * N^2),  N = total_num_tokens (the token count the counts and
+ *   probabilities were taken over; it may exceed T when tokens span several devices)
+ *   d loss / d probs[t][e] = C * tokens_per_expert[e] * grad_loss
+ *
+ * moe_tokens_per_expert -- tokens_per_expert[e] (int32 [E]) = number of rows t with
+ *   routing_map[t][e] != 0 (routing_map uint8 [T x E]). Overwrites all E entries.
+ * moe_aux_loss_workspace_bytes -- device scratch moe_aux_loss_fwd needs for these
+ *   sizes (per-column partial sums; 0 for T == 0, or for invalid sizes).
+ * moe_aux_loss_fwd -- *loss (one fp32, device) from probs fp32 [T x E] and
+ *   tokens_per_expert int32 [E]. The column sums are Kahan-compensated fp32 in a fixed
+ *   order and the dot product is taken in fp64: the result is deterministic.
+ *   workspace: caller-owned device scratch of at least moe_aux_loss_workspace_bytes(),
+ *   contents ignored on entry.
+ * moe_aux_loss_bwd -- grad_probs fp32 [T x E] from grad_loss (one fp32, device).
+ * All three: MR_EINVAL for a NULL required pointer, T < 0, E < 1, topk < 1,
+ *   total_num_tokens < 1, T*E > INT_MAX or a too-small workspace.
+ */
+int moe_tokens_per_expert(int T, int E, const uint8_t* routing_map, int32_t* tokens_per_expert,
+                          mr_stream_t stream);
+size_t moe_aux_loss_workspace_bytes(int T, int E);
+int moe_aux_loss_fwd(int T, int E, int topk, float coeff, long long total_num_tokens, const float* probs,
+                     const int32_t* tokens_per_expert, float* loss, void* workspace, size_t ws_bytes,
+                     mr_stream_t stream);
+int moe_aux_loss_bwd(int T, int E, int topk, float coeff, long long total_num_tokens,
+                     const int32_t* tokens_per_expert, const float* grad_loss, float* grad_probs,
+                     mr_stream_t stream);
+
+/*
  * moe_sort -- bucket (token, slot) pairs by expert into block_m-padded blocks
  * ([FLY] moe_sorting; layout as consumed by [GEMM]).
  *   cnt[e] = pairs routed to e;  pad[e] = ceil(cnt[e]/block_m)*block_m (0 if empty)

@@ -58,6 +58,10 @@ _SIGS = {
     "moe_router_expf": ([_P, _P, _I, _P], _I),
     "moe_router_noop": ([_P], _I),
     "moe_router_device_status": ([_P, _I, _P], _I),
+    "moe_tokens_per_expert": ([_I, _I, _P, _P, _P], _I),
+    "moe_aux_loss_workspace_bytes": ([_I, _I], _SZ),
+    "moe_aux_loss_fwd": ([_I, _I, _I, ctypes.c_float, ctypes.c_longlong, _P, _P, _P, _P, _SZ, _P], _I),
+    "moe_aux_loss_bwd": ([_I, _I, _I, ctypes.c_float, ctypes.c_longlong, _P, _P, _P, _P], _I),
 }
 
 
@@ -249,6 +253,29 @@ def device_status(clear: bool = False) -> int:
     return int(out.item())
 
 
+def moe_tokens_per_expert(T, E, routing_map, tokens_per_expert, stream=None) -> int:
+    return _ok(_lib.moe_tokens_per_expert(T, E, _ptr(routing_map), _ptr(tokens_per_expert), _stream(stream)),
+               "moe_tokens_per_expert")
+
+
+def moe_aux_loss_workspace_bytes(T: int, E: int) -> int:
+    return int(_lib.moe_aux_loss_workspace_bytes(T, E))
+
+
+def moe_aux_loss_fwd(T, E, topk, coeff, total_num_tokens, probs, tokens_per_expert, loss, workspace,
+                     ws_bytes=None, stream=None) -> int:
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return _ok(_lib.moe_aux_loss_fwd(T, E, topk, coeff, total_num_tokens, _ptr(probs), _ptr(tokens_per_expert),
+                                     _ptr(loss), _ptr(workspace), ws_bytes, _stream(stream)), "moe_aux_loss_fwd")
+
+
+def moe_aux_loss_bwd(T, E, topk, coeff, total_num_tokens, tokens_per_expert, grad_loss, grad_probs,
+                     stream=None) -> int:
+    return _ok(_lib.moe_aux_loss_bwd(T, E, topk, coeff, total_num_tokens, _ptr(tokens_per_expert),
+                                     _ptr(grad_loss), _ptr(grad_probs), _stream(stream)), "moe_aux_loss_bwd")
+
+
 # ------------------------------------------------------------------- allocating helpers
 
 PATH_AUTO, PATH_ARGMAX, PATH_SELECT = 0, 1, 2
@@ -351,3 +378,32 @@ def header_symbols() -> list[str]:
     with open(hdr) as f:
         text = f.read()
     return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(moe_\w+)\s*\(", text, re.M)))
+
+
+def tokens_per_expert(routing_map: torch.Tensor, stream=None) -> torch.Tensor:
+    """Per-expert count of routed rows of a uint8 [T, E] routing map (int32 [E])."""
+    T, E = routing_map.shape
+    out = torch.empty(E, dtype=torch.int32, device=routing_map.device)
+    moe_tokens_per_expert(T, E, routing_map, out, stream)
+    return out
+
+
+def aux_loss(probs: torch.Tensor, tokens_per_expert: torch.Tensor, topk: int, coeff: float,
+             total_num_tokens: int = None, stream=None) -> torch.Tensor:
+    """The aux-loss scalar (one fp32 on the device) of fp32 probs [T, E]."""
+    T, E = probs.shape
+    N = T if total_num_tokens is None else total_num_tokens
+    loss = torch.empty(1, dtype=torch.float32, device=probs.device)
+    ws = torch.empty(max(1, moe_aux_loss_workspace_bytes(T, E)), dtype=torch.uint8, device=probs.device)
+    moe_aux_loss_fwd(T, E, topk, coeff, N, probs, tokens_per_expert, loss, ws, stream=stream)
+    return loss
+
+
+def aux_loss_bwd(grad_loss: torch.Tensor, tokens_per_expert: torch.Tensor, T: int, topk: int, coeff: float,
+                 total_num_tokens: int = None, stream=None) -> torch.Tensor:
+    """d loss / d probs (fp32 [T, E])."""
+    E = tokens_per_expert.numel()
+    N = T if total_num_tokens is None else total_num_tokens
+    g = torch.empty(T, E, dtype=torch.float32, device=tokens_per_expert.device)
+    moe_aux_loss_bwd(T, E, topk, coeff, N, tokens_per_expert, grad_loss, g, stream)
+    return g

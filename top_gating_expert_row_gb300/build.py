@@ -32,6 +32,7 @@ UNITS = [
     ("fwd_s1_d1", "fwd.cu", ["-DMR_SCORE_FN=1", "-DMR_IN_BF16=1"]),
     ("sort", "sort.cu", []),
     ("bwd", "bwd.cu", []),
+    ("aux_loss", "aux_loss.cu", []),
     ("api", "api.cu", []),
 ]
 

@@ -383,6 +383,59 @@ int moe_aux_scores_bwd(int T, int E, int score_fn, const float* grad_scores, con
                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static int check_aux_loss(int T, int E, int topk, long long total_num_tokens)
+{
+    if (T < 0 || E < 1 || topk < 1 || total_num_tokens < 1) return MR_EINVAL;
+    if (static_cast<long long>(T) * E > INT_MAX) return MR_EINVAL;
+    return MR_OK;
+}
+
+static double aux_loss_factor(int E, int topk, float coeff, long long total_num_tokens)
+{
+    const double N = static_cast<double>(total_num_tokens);
+    return static_cast<double>(coeff) * static_cast<double>(E) / (static_cast<double>(topk) * N * N);
+}
+
+int moe_tokens_per_expert(int T, int E, const uint8_t* routing_map, int32_t* tokens_per_expert,
+                          mr_stream_t stream)
+{
+    if (T < 0 || E < 1 || !tokens_per_expert || (T > 0 && !routing_map)) return MR_EINVAL;
+    if (static_cast<long long>(T) * E > INT_MAX) return MR_EINVAL;
+    return from_cuda(launch_tokens_per_expert(routing_map, T, E, tokens_per_expert,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_aux_loss_workspace_bytes(int T, int E)
+{
+    if (T < 0 || E < 1 || static_cast<long long>(T) * E > INT_MAX) return 0;
+    return static_cast<size_t>(aux_chunks(T)) * static_cast<size_t>(E) * sizeof(float);
+}
+
+int moe_aux_loss_fwd(int T, int E, int topk, float coeff, long long total_num_tokens, const float* probs,
+                     const int32_t* tokens_per_expert, float* loss, void* workspace, size_t ws_bytes,
+                     mr_stream_t stream)
+{
+    const int c = check_aux_loss(T, E, topk, total_num_tokens);
+    if (c != MR_OK) return c;
+    if (!tokens_per_expert || !loss || (T > 0 && (!probs || !workspace))) return MR_EINVAL;
+    if (ws_bytes < moe_aux_loss_workspace_bytes(T, E)) return MR_EINVAL;
+    return from_cuda(launch_aux_loss_fwd(probs, tokens_per_expert, T, E,
+                                         aux_loss_factor(E, topk, coeff, total_num_tokens), loss,
+                                         static_cast<float*>(workspace), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_aux_loss_bwd(int T, int E, int topk, float coeff, long long total_num_tokens,
+                     const int32_t* tokens_per_expert, const float* grad_loss, float* grad_probs,
+                     mr_stream_t stream)
+{
+    const int c = check_aux_loss(T, E, topk, total_num_tokens);
+    if (c != MR_OK) return c;
+    if (!tokens_per_expert || !grad_loss || (T > 0 && !grad_probs)) return MR_EINVAL;
+    return from_cuda(launch_aux_loss_bwd(tokens_per_expert, grad_loss, T, E,
+                                         aux_loss_factor(E, topk, coeff, total_num_tokens), grad_probs,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t moe_sort_capacity(int T, int topk, int E_tot, int block_m)
 {
     if (T < 0 || topk < 1 || E_tot < 1 || block_m < 1) return 0;

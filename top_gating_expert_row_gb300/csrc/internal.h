@@ -38,6 +38,9 @@ constexpr int kWideThreads = 64;
 // Registers are capped so that shared memory, not registers, bounds residency
 // (a 9 KB key row per warp at E = 2304 allows about 22 warps per SM).
 constexpr int kWideMinBlocks = 10;
+constexpr int kAuxThreads = 256;        // aux-loss kernels: 8 warps over the rows of one 128-column slab
+constexpr int kAuxRowsPerChunk = 256;   // rows per aux-loss CTA (before the cap on chunks)
+constexpr int kAuxMaxChunks = 256;      // row chunks of the aux-loss forward (workspace = chunks * E floats)
 
 struct SortArgs {
     int32_t* ids;
@@ -90,6 +93,12 @@ int launch_sort(const int32_t* idx, const float* w, int N, int E_tot, int block_
                 float* sw, int32_t* eids, int32_t* npp, uint32_t* ws, int32_t* status,
                 cudaStream_t st);
 int launch_expf(const float* x, float* y, int n, cudaStream_t st);
+int aux_chunks(long long T);
+int launch_aux_loss_fwd(const float* probs, const int32_t* tokens_per_expert, int T, int E, double C, float* loss,
+                        float* partial, cudaStream_t st);
+int launch_aux_loss_bwd(const int32_t* tokens_per_expert, const float* grad_loss, int T, int E, double C,
+                        float* grad_probs, cudaStream_t st);
+int launch_tokens_per_expert(const uint8_t* map, int T, int E, int32_t* out, cudaStream_t st);
 int launch_noop(cudaStream_t st);
 
 inline int sort_chunks(long long N) { return N <= 0 ? 1 : static_cast<int>((N + kSortChunk - 1) / kSortChunk); }
