@@ -159,10 +159,11 @@ int moe_aux_scores_bwd(int T, int E, int score_fn, const float* grad_scores, con
  *   tokens_per_expert int32 [E]. The column sums are Kahan-compensated fp32 in a fixed
  *   order and the dot product is taken in fp64: the result is deterministic.
  *   workspace: caller-owned device scratch of at least moe_aux_loss_workspace_bytes(),
- *   contents ignored on entry.
+ *   16-byte aligned, contents ignored on entry; calls that share a workspace must not
+ *   overlap on the GPU.
  * moe_aux_loss_bwd -- grad_probs fp32 [T x E] from grad_loss (one fp32, device).
  * All three: MR_EINVAL for a NULL required pointer, T < 0, E < 1, topk < 1,
- *   total_num_tokens < 1, T*E > INT_MAX or a too-small workspace.
+ *   total_num_tokens < 1, T*E > INT_MAX, or a too-small or misaligned workspace.
  */
 int moe_tokens_per_expert(int T, int E, const uint8_t* routing_map, int32_t* tokens_per_expert,
                           mr_stream_t stream);

@@ -169,8 +169,10 @@ def test_aux_loss_sizes_and_rejects(lib):
     L = lib._lib
     assert L.moe_aux_loss_workspace_bytes(0, 64) == 0
     assert L.moe_aux_loss_workspace_bytes(-1, 64) == 0
-    assert L.moe_aux_loss_workspace_bytes(8192, 2304) == 32 * 2304 * 4   # 256 rows per chunk
-    assert L.moe_aux_loss_workspace_bytes(10 ** 6, 64) == 256 * 64 * 4   # chunks capped at 256
+    # per-chunk column sums (256 rows per chunk, at most 256 chunks), one fp64 per
+    # 128-column slab, and a counter
+    assert L.moe_aux_loss_workspace_bytes(8192, 2304) == 32 * 2304 * 4 + 18 * 8 + 16
+    assert L.moe_aux_loss_workspace_bytes(10 ** 6, 64) == 256 * 64 * 4 + 1 * 8 + 16
     ws = L.moe_aux_loss_workspace_bytes(100, 8)
     ok = dict(T=100, E=8, topk=2, coeff=0.1, N=100, probs=FAKE, tpe=FAKE, loss=FAKE, ws=FAKE, wsb=ws)
 
@@ -180,7 +182,7 @@ def test_aux_loss_sizes_and_rejects(lib):
                                   a["ws"], a["wsb"], None)
 
     for bad in (dict(T=-1), dict(E=0), dict(topk=0), dict(N=0), dict(probs=None), dict(tpe=None), dict(loss=None),
-                dict(ws=None), dict(wsb=ws - 1), dict(T=1 << 20, E=4096)):
+                dict(ws=None), dict(wsb=ws - 1), dict(T=1 << 20, E=4096), dict(ws=FAKE + 8)):
         assert fwd(**bad) == lib.MR_EINVAL, bad
     assert L.moe_aux_loss_bwd(100, 8, 2, 0.1, 0, FAKE, FAKE, FAKE, None) == lib.MR_EINVAL
     assert L.moe_aux_loss_bwd(100, 8, 2, 0.1, 100, None, FAKE, FAKE, None) == lib.MR_EINVAL

@@ -408,7 +408,7 @@ int moe_tokens_per_expert(int T, int E, const uint8_t* routing_map, int32_t* tok
 size_t moe_aux_loss_workspace_bytes(int T, int E)
 {
     if (T < 0 || E < 1 || static_cast<long long>(T) * E > INT_MAX) return 0;
-    return static_cast<size_t>(aux_chunks(T)) * static_cast<size_t>(E) * sizeof(float);
+    return aux_workspace_bytes(T, E);
 }
 
 int moe_aux_loss_fwd(int T, int E, int topk, float coeff, long long total_num_tokens, const float* probs,
@@ -419,9 +419,10 @@ int moe_aux_loss_fwd(int T, int E, int topk, float coeff, long long total_num_to
     if (c != MR_OK) return c;
     if (!tokens_per_expert || !loss || (T > 0 && (!probs || !workspace))) return MR_EINVAL;
     if (ws_bytes < moe_aux_loss_workspace_bytes(T, E)) return MR_EINVAL;
+    if (T > 0 && !aligned(workspace, 16)) return MR_EINVAL;
     return from_cuda(launch_aux_loss_fwd(probs, tokens_per_expert, T, E,
-                                         aux_loss_factor(E, topk, coeff, total_num_tokens), loss,
-                                         static_cast<float*>(workspace), reinterpret_cast<cudaStream_t>(stream)));
+                                         aux_loss_factor(E, topk, coeff, total_num_tokens), loss, workspace,
+                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_aux_loss_bwd(int T, int E, int topk, float coeff, long long total_num_tokens,

@@ -39,7 +39,8 @@ struct Kahan {
 };
 
 __global__ void __launch_bounds__(kAuxThreads) k_aux_colsum(const float* __restrict__ probs, int T, int E,
-                                                            int rows_per_chunk, int vec, float* __restrict__ partial)
+                                                            int rows_per_chunk, int vec, float* __restrict__ partial,
+                                                            unsigned int* done)
 {
     __shared__ float red[kAuxWarps][128];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -58,14 +59,15 @@ __global__ void __launch_bounds__(kAuxThreads) k_aux_colsum(const float* __restr
             for (int c = 0; c < 4; ++c) x[c] = col0 + c < E ? __ldcs(p + c) : 0.0f;
         }
     };
-    // rows t0 + warp, + 8, ...; four rows in flight per warp
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *done = 0u;  // for k_aux_loss_final
+    // rows t0 + warp, + 8, ...; eight rows in flight per warp
     int t = t0 + warp;
-    for (; t + 3 * kAuxWarps < t1; t += 4 * kAuxWarps) {
-        float x[4][4];
+    for (; t + 7 * kAuxWarps < t1; t += 8 * kAuxWarps) {
+        float x[8][4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) load(t + u * kAuxWarps, x[u]);
+        for (int u = 0; u < 8; ++u) load(t + u * kAuxWarps, x[u]);
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < 8; ++u)
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[c].add(x[u][c]);
     }
@@ -89,27 +91,52 @@ __global__ void __launch_bounds__(kAuxThreads) k_aux_colsum(const float* __restr
     }
 }
 
-__global__ void __launch_bounds__(1024) k_aux_loss_final(const float* __restrict__ partial, int R, int E,
-                                                         const int32_t* __restrict__ tokens_per_expert, double C,
-                                                         float* loss)
+// One CTA per 128-column slab: the slab's column sums (chunks in a fixed
+// order), their dot product with the counts in fp64, written to `dots`; the
+// CTA that finishes last (a counter, no waiting) adds the slab results in slab
+// order and writes the loss.
+__global__ void __launch_bounds__(kAuxThreads) k_aux_loss_final(const float* __restrict__ partial, int R, int E,
+                                                                const int32_t* __restrict__ tokens_per_expert,
+                                                                double C, double* dots, unsigned int* done,
+                                                                float* loss)
 {
-    __shared__ double red[32];
+    __shared__ float red[kAuxWarps][128];
+    __shared__ bool last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    double acc = 0.0;
-    for (int col = threadIdx.x; col < E; col += blockDim.x) {
-        Kahan k;
-        for (int r = 0; r < R; ++r) k.add(partial[static_cast<size_t>(r) * E + col]);
-        acc += static_cast<double>(k.s) * static_cast<double>(tokens_per_expert[col]);
+    const int col0 = blockIdx.x * 128 + lane * 4;
+    Kahan acc[4];
+    for (int r = warp; r < R; r += kAuxWarps) {
+        const float* p = partial + static_cast<size_t>(r) * E + col0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if (col0 + c < E) acc[c].add(__ldcg(p + c));
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
-    if (lane == 0) red[warp] = acc;
+    for (int c = 0; c < 4; ++c) red[warp][lane * 4 + c] = acc[c].s;
     __syncthreads();
     if (warp == 0) {
-        double v = lane < static_cast<int>(blockDim.x >> 5) ? red[lane] : 0.0;
+        double d = 0.0;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-        if (lane == 0) loss[0] = static_cast<float>(v * C);
+        for (int c = 0; c < 4; ++c) {
+            if (col0 + c >= E) break;
+            Kahan k;
+            for (int w = 0; w < kAuxWarps; ++w) k.add(red[w][lane * 4 + c]);
+            d += static_cast<double>(k.s) * static_cast<double>(tokens_per_expert[col0 + c]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(kFull, d, o);
+        if (lane == 0) {
+            dots[blockIdx.x] = d;
+            __threadfence();
+            last = atomicAdd(done, 1u) == gridDim.x - 1;
+        }
+    }
+    __syncthreads();
+    if (last && threadIdx.x == 0) {
+        __threadfence();
+        double v = 0.0;
+        for (unsigned int b = 0; b < gridDim.x; ++b) v += __ldcg(dots + b);
+        loss[0] = static_cast<float>(v * C);
     }
 }
 
@@ -128,10 +155,19 @@ __global__ void __launch_bounds__(kAuxThreads) k_aux_loss_bwd(const int32_t* __r
     for (int c = 0; c < 4; ++c)
         f[c] = col0 + c < E ? static_cast<float>(C * static_cast<double>(tokens_per_expert[col0 + c]) * g) : 0.0f;
     const bool whole = vec && col0 + 4 <= E;
-    for (int t = t0 + warp; t < t1; t += kAuxWarps) {
+    const float4 f4 = make_float4(f[0], f[1], f[2], f[3]);
+    int t = t0 + warp;
+    if (whole) {
+        for (; t + 3 * kAuxWarps < t1; t += 4 * kAuxWarps) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                *reinterpret_cast<float4*>(grad_probs + static_cast<size_t>(t + u * kAuxWarps) * E + col0) = f4;
+        }
+    }
+    for (; t < t1; t += kAuxWarps) {
         float* p = grad_probs + static_cast<size_t>(t) * E + col0;
         if (whole) {
-            *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<float4*>(p) = f4;
         } else {
 #pragma unroll
             for (int c = 0; c < 4; ++c)
@@ -140,58 +176,93 @@ __global__ void __launch_bounds__(kAuxThreads) k_aux_loss_bwd(const int32_t* __r
     }
 }
 
+// Counts: a CTA covers a 512-column slab (lane l on columns 16l..16l+15, one
+// 16-byte load per row) of a chunk of rows, eight rows in flight per warp; the
+// warps' counts are added in shared memory and then once per column into `out`.
 __global__ void __launch_bounds__(kAuxThreads) k_tokens_per_expert(const uint8_t* __restrict__ map, int T, int E,
                                                                    int rows_per_chunk, int vec, int32_t* out)
 {
-    __shared__ uint32_t red[kAuxWarps][128];
+    __shared__ uint32_t red[kAuxWarps][512];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int col0 = blockIdx.x * 128 + lane * 4;
+    const int col0 = blockIdx.x * 512 + lane * 16;
     const int t0 = blockIdx.y * rows_per_chunk;
     const int t1 = min(T, t0 + rows_per_chunk);
-    const bool whole = vec && col0 + 4 <= E;
-    uint32_t cnt[4] = {0u, 0u, 0u, 0u};
-    for (int t = t0 + warp; t < t1; t += kAuxWarps) {
+    const bool whole = vec && col0 + 16 <= E;
+    uint32_t cnt[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) cnt[c] = 0u;
+    auto add = [&](const uint4& q) {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) cnt[4 * i + b] += ((w[i] >> (8 * b)) & 0xffu) != 0u;
+    };
+    int t = t0 + warp;
+    if (whole) {
+        for (; t + 7 * kAuxWarps < t1; t += 8 * kAuxWarps) {
+            uint4 q[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                q[u] = __ldcs(reinterpret_cast<const uint4*>(map + static_cast<size_t>(t + u * kAuxWarps) * E + col0));
+#pragma unroll
+            for (int u = 0; u < 8; ++u) add(q[u]);
+        }
+    }
+    for (; t < t1; t += kAuxWarps) {
         const uint8_t* p = map + static_cast<size_t>(t) * E + col0;
         if (whole) {
-            const uint32_t w = __ldcs(reinterpret_cast<const unsigned int*>(p));
-#pragma unroll
-            for (int c = 0; c < 4; ++c) cnt[c] += ((w >> (8 * c)) & 0xffu) != 0u;
+            add(__ldcs(reinterpret_cast<const uint4*>(p)));
         } else {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) cnt[c] += (col0 + c < E && p[c] != 0) ? 1u : 0u;
+            for (int c = 0; c < 16; ++c) cnt[c] += (col0 + c < E && p[c] != 0) ? 1u : 0u;
         }
     }
 #pragma unroll
-    for (int c = 0; c < 4; ++c) red[warp][lane * 4 + c] = cnt[c];
+    for (int c = 0; c < 16; ++c) red[warp][lane * 16 + c] = cnt[c];
     __syncthreads();
-    if (warp == 0) {
+    for (int i = threadIdx.x; i < 512; i += kAuxThreads) {
+        const int col = blockIdx.x * 512 + i;
+        if (col >= E) break;
+        uint32_t sum = 0u;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            if (col0 + c >= E) break;
-            uint32_t s = 0u;
-            for (int w = 0; w < kAuxWarps; ++w) s += red[w][lane * 4 + c];
-            if (s) atomicAdd(reinterpret_cast<unsigned int*>(out + col0 + c), s);
-        }
+        for (int w = 0; w < kAuxWarps; ++w) sum += red[w][i];
+        if (sum) atomicAdd(reinterpret_cast<unsigned int*>(out + col), sum);
     }
 }
 
 }  // namespace
 
-int aux_chunks(long long T) { return static_cast<int>(T <= 0 ? 0 : std::min<long long>((T + kAuxRowsPerChunk - 1) / kAuxRowsPerChunk, kAuxMaxChunks)); }
+int aux_chunks(long long T)
+{
+    return static_cast<int>(T <= 0 ? 0
+                                   : std::min<long long>((T + kAuxRowsPerChunk - 1) / kAuxRowsPerChunk, kAuxMaxChunks));
+}
+
+size_t aux_workspace_bytes(long long T, int E)
+{
+    if (T <= 0) return 0;
+    const size_t slabs = static_cast<size_t>((E + 127) / 128);
+    const size_t part = (static_cast<size_t>(aux_chunks(T)) * E * sizeof(float) + 15) / 16 * 16;
+    return part + slabs * sizeof(double) + 16;
+}
 
 int launch_aux_loss_fwd(const float* probs, const int32_t* tokens_per_expert, int T, int E, double C, float* loss,
-                        float* partial, cudaStream_t st)
+                        void* workspace, cudaStream_t st)
 {
+    if (T <= 0) return cudaMemsetAsync(loss, 0, sizeof(float), st);
     const int R = aux_chunks(T);
     const int S = (E + 127) / 128;
-    if (R > 0) {
-        const int rows = (T + R - 1) / R;
-        const int vec = (E % 4 == 0) && (reinterpret_cast<uintptr_t>(probs) % 16 == 0);
-        k_aux_colsum<<<dim3(S, R), kAuxThreads, 0, st>>>(probs, T, E, rows, vec, partial);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    k_aux_loss_final<<<1, 1024, 0, st>>>(partial, R, E, tokens_per_expert, C, loss);
+    float* partial = static_cast<float*>(workspace);
+    const size_t part = (static_cast<size_t>(R) * E * sizeof(float) + 15) / 16 * 16;
+    double* dots = reinterpret_cast<double*>(static_cast<unsigned char*>(workspace) + part);
+    unsigned int* done = reinterpret_cast<unsigned int*>(dots + S);
+    const int rows = (T + R - 1) / R;
+    const int vec = (E % 4 == 0) && (reinterpret_cast<uintptr_t>(probs) % 16 == 0);
+    k_aux_colsum<<<dim3(S, R), kAuxThreads, 0, st>>>(probs, T, E, rows, vec, partial, done);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_aux_loss_final<<<S, kAuxThreads, 0, st>>>(partial, R, E, tokens_per_expert, C, dots, done, loss);
     return cudaGetLastError();
 }
 
@@ -211,10 +282,11 @@ int launch_tokens_per_expert(const uint8_t* map, int T, int E, int32_t* out, cud
 {
     cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(E) * sizeof(int32_t), st);
     if (e != cudaSuccess || T <= 0) return e;
-    const int R = std::min((T + kAuxRowsPerChunk - 1) / kAuxRowsPerChunk, 4096);
+    constexpr int kRows = 128;
+    const int R = std::min((T + kRows - 1) / kRows, 8192);
     const int rows = (T + R - 1) / R;
-    const int S = (E + 127) / 128;
-    const int vec = (E % 4 == 0) && (reinterpret_cast<uintptr_t>(map) % 4 == 0);
+    const int S = (E + 511) / 512;
+    const int vec = (E % 16 == 0) && (reinterpret_cast<uintptr_t>(map) % 16 == 0);
     k_tokens_per_expert<<<dim3(S, R), kAuxThreads, 0, st>>>(map, T, E, rows, vec, out);
     return cudaGetLastError();
 }

@@ -94,8 +94,9 @@ int launch_sort(const int32_t* idx, const float* w, int N, int E_tot, int block_
                 cudaStream_t st);
 int launch_expf(const float* x, float* y, int n, cudaStream_t st);
 int aux_chunks(long long T);
+size_t aux_workspace_bytes(long long T, int E);
 int launch_aux_loss_fwd(const float* probs, const int32_t* tokens_per_expert, int T, int E, double C, float* loss,
-                        float* partial, cudaStream_t st);
+                        void* workspace, cudaStream_t st);
 int launch_aux_loss_bwd(const int32_t* tokens_per_expert, const float* grad_loss, int T, int E, double C,
                         float* grad_probs, cudaStream_t st);
 int launch_tokens_per_expert(const uint8_t* map, int T, int E, int32_t* out, cudaStream_t st);
