@@ -110,3 +110,24 @@ def test_repeated_calls_are_bit_identical(mr):
     b = mr.aux_loss(probs, counts, k, 0.01)
     torch.cuda.synchronize()
     assert a.view(torch.int32).item() == b.view(torch.int32).item()
+
+
+def test_counts_treat_any_nonzero_byte_as_routed(mr, orc):
+    g = torch.Generator().manual_seed(13)
+    T, E = 777, 2304
+    vals = torch.tensor([0, 0, 0, 1, 2, 128, 255], dtype=torch.uint8)
+    m = vals[torch.randint(0, len(vals), (T, E), generator=g)]
+    got = mr.tokens_per_expert(m.cuda())
+    torch.cuda.synchronize()
+    assert_equal(got, orc.tokens_per_expert(m.numpy()), "tokens_per_expert (0..255 bytes)")
+
+
+def test_counts_over_long_row_chunks(mr, orc):
+    # 2^24 rows of 16 experts: 2048 rows per CTA, 256 per thread, so the
+    # byte-wide counters are flushed into the 32-bit ones along the way
+    T, E = 1 << 24, 16
+    g = torch.Generator().manual_seed(14)
+    m = torch.randint(0, 2, (T, E), generator=g, dtype=torch.uint8)
+    got = mr.tokens_per_expert(m.cuda())
+    torch.cuda.synchronize()
+    assert_equal(got, orc.tokens_per_expert(m.numpy()), "tokens_per_expert (long chunks)")

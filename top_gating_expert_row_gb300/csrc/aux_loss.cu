@@ -105,11 +105,21 @@ __global__ void __launch_bounds__(kAuxThreads) k_aux_loss_final(const float* __r
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col0 = blockIdx.x * 128 + lane * 4;
     Kahan acc[4];
-    for (int r = warp; r < R; r += kAuxWarps) {
-        const float* p = partial + static_cast<size_t>(r) * E + col0;
+    // four chunks per warp at a time, all loads issued before the adds
+    for (int r0 = warp; r0 < R; r0 += 4 * kAuxWarps) {
+        float x[4][4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            if (col0 + c < E) acc[c].add(__ldcg(p + c));
+        for (int u = 0; u < 4; ++u) {
+            const int r = r0 + u * kAuxWarps;
+            const float* p = partial + static_cast<size_t>(r) * E + col0;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) x[u][c] = (r < R && col0 + c < E) ? __ldcg(p + c) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (r0 + u * kAuxWarps < R)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[c].add(x[u][c]);
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c) red[warp][lane * 4 + c] = acc[c].s;
@@ -191,12 +201,29 @@ __global__ void __launch_bounds__(kAuxThreads) k_tokens_per_expert(const uint8_t
     uint32_t cnt[16];
 #pragma unroll
     for (int c = 0; c < 16; ++c) cnt[c] = 0u;
+    // Counting in SIMD-within-a-register form: each byte is folded to 0/1 and
+    // four bytes are added at once into byte-wide counters (packed[i]), which
+    // are moved into cnt before any of them can reach 256.
+    uint32_t packed[4] = {0u, 0u, 0u, 0u};
+    int held = 0;  // rows added into packed since the last flush
+    auto flush = [&]() {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) cnt[4 * i + b] += (packed[i] >> (8 * b)) & 0xffu;
+            packed[i] = 0u;
+        }
+        held = 0;
+    };
     auto add = [&](const uint4& q) {
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) cnt[4 * i + b] += ((w[i] >> (8 * b)) & 0xffu) != 0u;
+        for (int i = 0; i < 4; ++i) {
+            uint32_t f = w[i] | (w[i] >> 4);
+            f |= f >> 2;
+            f |= f >> 1;
+            packed[i] += f & 0x01010101u;
+        }
     };
     int t = t0 + warp;
     if (whole) {
@@ -207,17 +234,21 @@ __global__ void __launch_bounds__(kAuxThreads) k_tokens_per_expert(const uint8_t
                 q[u] = __ldcs(reinterpret_cast<const uint4*>(map + static_cast<size_t>(t + u * kAuxWarps) * E + col0));
 #pragma unroll
             for (int u = 0; u < 8; ++u) add(q[u]);
+            held += 8;
+            if (held > 240) flush();
         }
     }
     for (; t < t1; t += kAuxWarps) {
         const uint8_t* p = map + static_cast<size_t>(t) * E + col0;
         if (whole) {
             add(__ldcs(reinterpret_cast<const uint4*>(p)));
+            if (++held > 240) flush();
         } else {
 #pragma unroll
             for (int c = 0; c < 16; ++c) cnt[c] += (col0 + c < E && p[c] != 0) ? 1u : 0u;
         }
     }
+    flush();
 #pragma unroll
     for (int c = 0; c < 16; ++c) red[warp][lane * 16 + c] = cnt[c];
     __syncthreads();
