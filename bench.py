@@ -81,10 +81,15 @@ def peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
+# the sources the wide forward kernel is compiled from (its traffic figure is
+# void once any of them changes)
+FWD_SOURCES = ("common.cuh", "route.cuh", "route_wide.cuh", "internal.h", "fwd.cu")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "top_gating_expert_row_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in FWD_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -207,7 +212,10 @@ def make_step(mr, w, dev, stream):
     P = ctypes.byref(cp)
     ptr = {n: (v.data_ptr() if v is not None else None) for n, v in t.items()}
 
-    def chk(rc, what):
+    # The launches pass raw device pointers, so they must keep the tensors (and
+    # the params, which hold the bias) alive: every launch goes through chk,
+    # whose default argument holds them for as long as any launch exists.
+    def chk(rc, what, _owned=(t, p, cp)):
         if rc != 0:
             raise RuntimeError(f"{what}: {mr.strerror(rc)}")
 
@@ -228,27 +236,34 @@ def step_bytes(w, kinds=("fwd", "bwd", "aux_fwd", "aux_bwd")) -> dict:
     return {kd: kernel_bytes(kd, w.T, w.E, w.topk, ib) for kd in kinds}
 
 
-def time_kernels(mr, w, dev, stream, reps=20, warmup=3) -> dict:
-    launches, _, _ = make_step(mr, w, dev, stream)
-    tm = Timer(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            for _, fn in launches:
+def time_kernels(mr, w, dev, stream, calls=20, replays=5) -> dict:
+    """Per-kernel device time of one workload's step kernels. A kernel of these
+    sizes runs for tens of µs, about as long as a Python launch, so each kernel
+    is timed as a CUDA-graph replay of `calls` back-to-back calls that rotate
+    over enough buffer sets (more than 3x L2 in all) that every call reads its
+    inputs from HBM."""
+    per_set = None
+    sets = []
+    while not sets or len(sets) * per_set < 3 * 129 * 2 ** 20 or len(sets) < 2:
+        launches, t, _ = make_step(mr, w, dev, stream)
+        per_set = sum(v.numel() * v.element_size() for v in t.values() if v is not None)
+        with torch.cuda.stream(stream):
+            for _, fn in launches:  # valid bwd / aux inputs in every set
                 fn()
-        for _ in range(reps):
-            for name, fn in launches:
-                tm.around(name, fn)
+        sets.append(dict(launches))  # each launch owns its set's tensors (see make_step)
     torch.cuda.synchronize()
     out = {}
     fn_name = "softmax" if w.score_fn == synth.SOFTMAX else "sigmoid"
     for name, nb in step_bytes(w).items():
-        ms = tm.mean_ms(name)
-        gbs = nb / (ms * 1e-3) / 1e9
-        d = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1)}
+        it = iter(range(10 ** 9))
+        us = graph_us(lambda: sets[next(it) % len(sets)][name](), stream, calls, replays)
+        gbs = nb / (us * 1e-6) / 1e9
+        d = {"us": round(us, 2), "GB/s": round(gbs, 1)}
         page = PAGE_B300.get((name, fn_name, w.E, w.topk))
         if page:
             d["page_B300_GB/s"] = page
         out[name] = d
+    out["timing"] = f"CUDA graph, {calls} calls per replay over {len(sets)} buffer sets ({len(sets) * per_set >> 20} MB)"
     return out
 
 
@@ -334,6 +349,26 @@ def decode_latency(mr, dev, stream, n_calls=200, Ts=synth.DECODE_TS) -> dict:
     return res
 
 
+def graph_us(fn, stream, calls=20, replays=5) -> float:
+    """Mean device time of fn() in µs: `calls` back-to-back calls captured into a
+    CUDA graph on `stream`, replayed `replays` times between two events."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(calls):
+            fn()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        g.replay()
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(replays):
+            g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / (calls * replays)
+
+
 def prefill_route_sort(mr, dev, stream, reps=20) -> dict:
     """T=16384, E=384+1 shared, topk=9, bf16 sigmoid + bias, 8 groups keep 4, block_m=64."""
     w = synth.prefill_grouped()
@@ -351,7 +386,6 @@ def prefill_route_sort(mr, dev, stream, reps=20) -> dict:
     ws = torch.empty(mr.moe_sort_workspace_bytes(w.T, w.topk, w.E_tot, w.block_m), dtype=torch.uint8, device=dev)
     a = [bufs[n].data_ptr() for n in ("sorted_token_ids", "sorted_weights", "expert_ids", "num_tokens_post_pad")]
     s = stream.cuda_stream
-    tm = Timer(stream)
     route = lambda: L.moe_router_fwd(P, x.data_ptr(), None, None, None, idx.data_ptr(), wt.data_ptr(), s)  # noqa
     srt = lambda: L.moe_sort(idx.data_ptr(), wt.data_ptr(), w.T, w.topk, w.E_tot, w.block_m, a[0], a[1], a[2],  # noqa
                              a[3], ws.data_ptr(), ws.numel(), None, s)
@@ -359,18 +393,17 @@ def prefill_route_sort(mr, dev, stream, reps=20) -> dict:
         for _ in range(3):
             route()
             srt()
-        for _ in range(reps):
-            tm.around("route", route)
-            tm.around("sort", srt)
     torch.cuda.synchronize()
-    r_us = tm.mean_ms("route") * 1e3
-    s_us = tm.mean_ms("sort") * 1e3
+    # tens of µs per call, close to the cost of a Python launch: timed as CUDA-graph replays
+    r_us = graph_us(route, stream, reps)
+    s_us = graph_us(srt, stream, reps)
     rb = w.T * w.E * 2 + w.T * w.topk * 8 + w.E * 4
     npp = int(bufs["num_tokens_post_pad"].item())
     sb = w.T * w.topk * 8 + npp * 8 + (npp // w.block_m) * 4 + 4
     return {"workload": w.name, "route_us": round(r_us, 2), "sort_us": round(s_us, 2),
             "route_GB/s": round(rb / (r_us * 1e-6) / 1e9, 1), "sort_GB/s": round(sb / (s_us * 1e-6) / 1e9, 1),
-            "route_plus_sort_us": round(r_us + s_us, 2), "num_tokens_post_pad": npp}
+            "route_plus_sort_us": round(r_us + s_us, 2), "num_tokens_post_pad": npp,
+            "timing": "CUDA graph, 20 calls per replay"}
 
 
 def aux_loss_rates(mr, w, dev, stream, reps=50) -> dict:
@@ -404,58 +437,68 @@ def aux_loss_rates(mr, w, dev, stream, reps=50) -> dict:
     pk = peaks()["hbm_gbs"]
     out = {"workload": f"T={T} E={E} topk={k} aux scores of the step", "timing": "CUDA graph, 20 calls per replay"}
     for n, fn in calls.items():
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for _ in range(20):
-                fn()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            g.replay()
-            torch.cuda.synchronize()
-            a.record(stream)
-            for _ in range(max(1, reps // 10)):
-                g.replay()
-            b.record(stream)
-        torch.cuda.synchronize()
-        us = a.elapsed_time(b) * 1e3 / (20 * max(1, reps // 10))
+        us = graph_us(fn, stream, 20, max(1, reps // 10))
         gbs = nbytes[n] / (us * 1e-6) / 1e9
         out[n] = {"us": round(us, 2), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / pk, 3)}
     return out
 
 
-def e2e_rate(mr, w, dev, stream, steps=5) -> dict:
-    """The same step through the C ABI with host buffers: every step copies the
-    inputs from pinned host memory and reads every output back."""
-    launches, t, _ = make_step(mr, w, dev, stream)
-    host_in = {n: t[n].cpu().pin_memory() for n in ("x", "g")}
+def e2e_rate(mr, w, dev, stream, steps=10) -> dict:
+    """The same step through the C ABI with host buffers: every step copies its
+    inputs in from pinned host memory and reads every output back. Steps are
+    pipelined the way a caller would run them: two device buffer sets, the
+    host-to-device copies on one stream, the kernels on `stream`, the
+    device-to-host copies on a third, ordered by events (a step's inputs land
+    while the previous step computes and the one before is read back)."""
+    sets = [make_step(mr, w, dev, stream)[:2] for _ in range(2)]
     outs = ("probs", "map", "inter", "idx", "w", "dx", "scores", "amap", "adx")
-    host_out = {n: torch.empty(t[n].shape, dtype=t[n].dtype).pin_memory() for n in outs}
+    t0 = sets[0][1]
+    host_in = {n: t0[n].cpu().pin_memory() for n in ("x", "g")}
+    host_out = {n: torch.empty(t0[n].shape, dtype=t0[n].dtype).pin_memory() for n in outs}
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+    out_done = [None, None]
 
-    def one():
-        for n, h in host_in.items():
-            t[n].copy_(h, non_blocking=True)
-        for _, fn in launches:
-            fn()
-        for n in outs:
-            host_out[n].copy_(t[n], non_blocking=True)
+    def one(i):
+        launches, t = sets[i % 2]
+        with torch.cuda.stream(s_in):
+            if out_done[i % 2] is not None:  # this set's previous step has been read back
+                s_in.wait_event(out_done[i % 2])
+            for n, h in host_in.items():
+                t[n].copy_(h, non_blocking=True)
+            in_done = torch.cuda.Event()
+            in_done.record(s_in)
+        stream.wait_event(in_done)
+        with torch.cuda.stream(stream):
+            for _, fn in launches:
+                fn()
+            comp_done = torch.cuda.Event()
+            comp_done.record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done)
+            for n in outs:
+                host_out[n].copy_(t[n], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(s_out)
+            out_done[i % 2] = ev
 
-    with torch.cuda.stream(stream):
-        one()
-        torch.cuda.synchronize()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(steps):
-            one()
-        b.record(stream)
+    one(0)
+    one(1)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(s_in)
+    for i in range(steps):
+        one(i)
+    b.record(s_out)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
     nb = sum(step_bytes(w).values())
     return {"value": round(nb / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 3),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipeline": "2 buffer sets; h2d / kernels / d2h on 3 streams; timed over %d steps" % steps}
 
 
 # ---------------------------------------------------------------------------------------- CPU oracle
@@ -582,7 +625,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     stream = torch.cuda.Stream(device=dev)
     w = STEP_WORKLOADS[args.workload]()
-    launches, _, _ = make_step(mr, w, dev, stream)
+    launches, _t, _ = make_step(mr, w, dev, stream)
     nbytes = step_bytes(w)
     tm = Timer(stream)
 
