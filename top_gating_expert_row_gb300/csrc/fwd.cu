@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kWideThreads, kWideMinBlocks) k_router_fwd_wid
     }
 }
 
-template <int NV, bool SELECT>
+template <int NV, bool SELECT, bool FULL>
 __global__ void __launch_bounds__(kFusedThreads) k_fused_decode(RouteArgs a, SortArgs s)
 {
     // A decode call is one short launch on one SM whose instruction cache is
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_fused_decode(RouteArgs a, Sor
     if (warp < a.T) {
         unsigned char* wsm = smem + static_cast<size_t>(warp) * L.bytes;
         uint32_t warm = 0u;
-        const float scale = route_row<kScore, InT, NV, SELECT>(a, warp, wsm, L, lane, warm);
+        const float scale = route_row<kScore, InT, NV, SELECT, FULL>(a, warp, wsm, L, lane, warm);
         const size_t o = static_cast<size_t>(warp) * a.topk;
         const uint32_t* win_idx = reinterpret_cast<const uint32_t*>(wsm + L.win_idx);
         const float* win_val = reinterpret_cast<const float*>(wsm + L.win_val);
@@ -246,16 +246,16 @@ FwdFn fwd_kernel(int nv_idx)
     return nullptr;
 }
 
-template <bool SELECT>
+template <bool SELECT, bool FULL>
 FusedFn fused_kernel(int nv_idx)
 {
     switch (kNvBuckets[nv_idx]) {
-        case 1: return k_fused_decode<1, SELECT>;
-        case 2: return k_fused_decode<2, SELECT>;
-        case 3: return k_fused_decode<3, SELECT>;
-        case 4: return k_fused_decode<4, SELECT>;
-        case 6: return k_fused_decode<6, SELECT>;
-        case 8: return k_fused_decode<8, SELECT>;
+        case 1: return k_fused_decode<1, SELECT, FULL>;
+        case 2: return k_fused_decode<2, SELECT, FULL>;
+        case 3: return k_fused_decode<3, SELECT, FULL>;
+        case 4: return k_fused_decode<4, SELECT, FULL>;
+        case 6: return k_fused_decode<6, SELECT, FULL>;
+        case 8: return k_fused_decode<8, SELECT, FULL>;
     }
     return nullptr;
 }
@@ -298,7 +298,11 @@ int MR_CAT(launch_fwd, MR_SUFFIX)(const RouteArgs& a, int nv_idx, bool select, c
 int MR_CAT(launch_fused, MR_SUFFIX)(const RouteArgs& a, const SortArgs& s, int nv_idx, bool select,
                                     cudaStream_t st)
 {
-    const FusedFn f = select ? fused_kernel<true>(nv_idx) : fused_kernel<false>(nv_idx);
+    // every chunk whole and vector-aligned: the specialisation without edge tests
+    // (a shorter instruction stream, which is what a decode call waits on)
+    const bool full = a.vec && a.E == 128 * kNvBuckets[nv_idx];
+    const FusedFn f = select ? (full ? fused_kernel<true, true>(nv_idx) : fused_kernel<true, false>(nv_idx))
+                             : (full ? fused_kernel<false, true>(nv_idx) : fused_kernel<false, false>(nv_idx));
     if (!f) return cudaErrorInvalidValue;
     const int nw = kFusedThreads / 32;
     const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, select, a.n_group > 0);
