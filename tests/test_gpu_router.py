@@ -260,6 +260,9 @@ def test_device_exp_matches_its_specification_bit_for_bit(mr, orc):
     torch.cuda.synchronize()
     ref = orc.expf(x.numpy())
     yc = y.cpu().numpy()
+    # the diagnostic writes a NaN wherever the device's packed and scalar forms
+    # (exp_spec2 / exp_spec, exp_value2 / exp_value) disagree
+    assert int(np.isnan(yc).sum()) == 0, "packed and scalar device exponentials disagree"
     assert np.array_equal(yc.view(np.uint32), ref.view(np.uint32))
     # and within CUDA's own expf error bound (2 ulp) of the device's expf
     cuda_exp = torch.exp(xg).cpu().numpy().astype(np.float64)

@@ -102,9 +102,26 @@ int launch_fused_decode(int score_fn, int in_dtype, const RouteArgs& a, const So
 
 // ---- diagnostics ------------------------------------------------------------------------------
 
+// Evaluates the specification through both device forms the kernels use, the
+// scalar exp_f32 and the packed exp_spec2 (on the pair (x[i], -x[i])), and
+// writes the scalar result; a NaN with payload 0x0badba is written instead
+// wherever the two forms disagree for a non-NaN input, and likewise where the
+// softmax-value exponential's packed form exp_value2 disagrees with its
+// scalar form exp_value on (-|x[i]|, -|x[i]|/2).
 __global__ void k_expf(const float* __restrict__ x, float* __restrict__ y, int n)
 {
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) y[i] = exp_f32(x[i]);
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const float v = x[i];
+        const float s = exp_f32(v);
+        const float2 p = exp_spec2(make_float2(v, -v));
+        const float a = -fabsf(v), b = __fmul_rn(a, 0.5f);
+        const float2 q = exp_value2(make_float2(a, b));
+        const bool same = (v != v) || (__float_as_uint(p.x) == __float_as_uint(s) &&
+                                       __float_as_uint(p.y) == __float_as_uint(exp_f32(-v)) &&
+                                       __float_as_uint(q.x) == __float_as_uint(exp_value(a)) &&
+                                       __float_as_uint(q.y) == __float_as_uint(exp_value(b)));
+        y[i] = same ? s : __uint_as_float(0x7f8badbau);
+    }
 }
 
 __global__ void k_noop() {}

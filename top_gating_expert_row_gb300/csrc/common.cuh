@@ -67,6 +67,35 @@ __device__ __forceinline__ float exp_spec(float x)
 // The specification including NaN (used by the diagnostic entry point).
 __device__ __forceinline__ float exp_f32(float x) { return (x != x) ? x : exp_spec(x); }
 
+// exp_spec on two values, bit-identical to two exp_spec calls: the reduction
+// and the scaling per value as in exp_spec, the degree-7 polynomial (8 of the
+// ~24 operations) on both values at once as packed fp32x2 fused multiply-adds,
+// each lane rounding as __fmaf_rn. (An all-packed form, with the rounding of
+// x*log2 e and the exponent split in packed and integer operations, was
+// computed wrong in one lane by this toolchain; the device exp diagnostic
+// checks this form against exp_spec on every input it evaluates.)
+__device__ __forceinline__ float2 exp_spec2(float2 x)
+{
+    const float ax = fminf(fmaxf(x.x, -104.0f), 89.0f);
+    const float ay = fminf(fmaxf(x.y, -104.0f), 89.0f);
+    const float nfx = rintf(__fmul_rn(ax, kLog2e));
+    const float nfy = rintf(__fmul_rn(ay, kLog2e));
+    const float2 r = make_float2(__fmaf_rn(-nfx, kLn2Lo, __fmaf_rn(-nfx, kLn2Hi, ax)),
+                                 __fmaf_rn(-nfy, kLn2Lo, __fmaf_rn(-nfy, kLn2Hi, ay)));
+    float2 p = make_float2(static_cast<float>(1.0 / 5040.0), static_cast<float>(1.0 / 5040.0));
+    p = __ffma2_rn(p, r, make_float2(static_cast<float>(1.0 / 720.0), static_cast<float>(1.0 / 720.0)));
+    p = __ffma2_rn(p, r, make_float2(static_cast<float>(1.0 / 120.0), static_cast<float>(1.0 / 120.0)));
+    p = __ffma2_rn(p, r, make_float2(static_cast<float>(1.0 / 24.0), static_cast<float>(1.0 / 24.0)));
+    p = __ffma2_rn(p, r, make_float2(static_cast<float>(1.0 / 6.0), static_cast<float>(1.0 / 6.0)));
+    p = __ffma2_rn(p, r, make_float2(0.5f, 0.5f));
+    p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
+    p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
+    const int nx = __float2int_rn(nfx), ny = __float2int_rn(nfy);
+    const int hx = nx / 2, hy = ny / 2;
+    return make_float2(__fmul_rn(__fmul_rn(p.x, pow2_normal(hx)), pow2_normal(nx - hx)),
+                       __fmul_rn(__fmul_rn(p.y, pow2_normal(hy)), pow2_normal(ny - hy)));
+}
+
 // exp for x <= 0 where only the value matters (softmax numerators): the same
 // reduction and polynomial, with x clamped at -87 so that 2^n stays a normal
 // scale applied by one exponent add. Below -87 it returns exp(-87) ~ 1.6e-38
@@ -133,6 +162,13 @@ __device__ __forceinline__ float2 exp_value2(float2 x)
 __device__ __forceinline__ float sigmoid_f32(float x)
 {
     return __frcp_rn(__fadd_rn(1.0f, exp_spec(-x)));
+}
+
+// sigmoid_f32 on two values (bit-identical), through exp_spec2.
+__device__ __forceinline__ float2 sigmoid_f32x2(float2 x)
+{
+    const float2 e = __fadd2_rn(make_float2(1.0f, 1.0f), exp_spec2(make_float2(-x.x, -x.y)));
+    return make_float2(__frcp_rn(e.x), __frcp_rn(e.y));
 }
 
 // ---------------------------------------------------------------------------

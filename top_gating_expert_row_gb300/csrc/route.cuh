@@ -235,10 +235,11 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
                         for (int c = 0; c < 4; ++c) b[c] = inside(v, c) ? __ldg(a.bias + e0 + c) : 0.0f;
                     }
                 }
-                float sv[4];
+                const float2 s01 = sigmoid_f32x2(make_float2(x[v][0], x[v][1]));
+                const float2 s23 = sigmoid_f32x2(make_float2(x[v][2], x[v][3]));
+                float sv[4] = {s01.x, s01.y, s23.x, s23.y};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    sv[c] = sigmoid_f32(x[v][c]);
                     key[v][c] = inside(v, c) ? key_of(a.bias ? __fadd_rn(sv[c], b[c]) : sv[c]) : 0u;
                     lm[c] = max(lm[c], key[v][c]);
                 }

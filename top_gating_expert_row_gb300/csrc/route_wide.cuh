@@ -134,10 +134,12 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
                         for (int c = 0; c < 4; ++c) b[c] = (e0 + c < E) ? __ldg(a.bias + e0 + c) : 0.0f;
                     }
                 }
-                float sv[4];
+                const float2 s01 = sigmoid_f32x2(make_float2(x[u][0], x[u][1]));
+                const float2 s23 = sigmoid_f32x2(make_float2(x[u][2], x[u][3]));
+                float sv[4] = {s01.x, s01.y, s23.x, s23.y};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    sv[c] = (FULL || e0 + c < E) ? sigmoid_f32(x[u][c]) : 0.0f;
+                    sv[c] = (FULL || e0 + c < E) ? sv[c] : 0.0f;
                     kk[c] = (FULL || e0 + c < E) ? key_of(a.bias ? __fadd_rn(sv[c], b[c]) : sv[c]) : 0u;
                 }
                 if (irow0) {
