@@ -585,7 +585,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["all", "step", "decode", "aux_loss"], default="all",
+    ap.add_argument("--only", choices=["all", "step", "decode", "aux_loss", "prefill"], default="all",
                     help="step: the timed step only; decode: the decode latency table only "
                          "(both used for profiling captures)")
     ap.add_argument("--decode-calls", type=int, default=200, help="calls per decode timing loop")
@@ -613,6 +613,11 @@ def main():
             ts = tuple(int(t) for t in args.decode_ts.split(","))
             print(json.dumps({"decode": decode_latency(mr, dev, torch.cuda.Stream(device=dev),
                                                        args.decode_calls, ts)}), flush=True)
+        return 0
+    if args.only == "prefill":
+        if rank == 0:
+            print(json.dumps({"prefill_route_sort": prefill_route_sort(mr, dev, torch.cuda.Stream(device=dev))}),
+                  flush=True)
         return 0
     if args.only == "aux_loss":
         if rank == 0:

@@ -27,10 +27,18 @@ __global__ void __launch_bounds__(kSortThreads) k_sort_hist(const int32_t* __res
     const int f0 = blockIdx.x * kSortChunk;
     const int f1 = min(f0 + kSortChunk, N);
     bool bad = false;
-    for (int i0 = f0 + (tid & ~31); i0 < f1; i0 += blockDim.x) {
-        const int i = i0 + lane;
-        int e = (i < f1) ? __ldg(idx + i) : kInvalidExpert;
-        if (i < f1 && (e < 0 || e >= E_tot)) {
+    // every id of this thread loaded first (one memory latency, not one per step)
+    constexpr int kSteps = kSortChunk / kSortThreads;
+    int ev[kSteps];
+#pragma unroll
+    for (int u = 0; u < kSteps; ++u) {
+        const int i = f0 + u * kSortThreads + tid;
+        ev[u] = (i < f1) ? __ldg(idx + i) : kInvalidExpert;
+    }
+#pragma unroll
+    for (int u = 0; u < kSteps; ++u) {
+        int e = ev[u];
+        if (f0 + u * kSortThreads + tid < f1 && (e < 0 || e >= E_tot)) {
             bad = true;
             e = kInvalidExpert;
         }
@@ -58,6 +66,7 @@ __global__ void __launch_bounds__(kSortThreads) k_sort_scatter(
 
     for (int e = tid; e < E_tot; e += blockDim.x) {
         uint32_t before = 0u, total = 0u;
+#pragma unroll 8
         for (int q = 0; q < nchunk; ++q) {
             const uint32_t v = __ldg(ws + static_cast<size_t>(q) * E_tot + e);
             before += (q < c) ? v : 0u;

@@ -64,9 +64,10 @@ __device__ inline uint32_t cta_exclusive_scan(uint32_t* a, int n, uint32_t* tmp)
     return total;
 }
 
-// Stable scatter of flat ids [f0, f1). base[e] is the absolute position of the
-// first pair of expert e handled by this CTA. wh: nwarps*E_tot 16-bit counters
-// (shared). Pairs with ids outside [0, E_tot) are skipped.
+// Stable scatter of flat ids [f0, f1), f1 - f0 <= kSortChunk, by a CTA of
+// kSortThreads threads. base[e] is the absolute position of the first pair of
+// expert e handled by this CTA. wh: nwarps*E_tot 16-bit counters (shared).
+// Pairs with ids outside [0, E_tot) are skipped.
 __device__ inline void cta_scatter(const int32_t* idx, const float* w, int f0, int f1, int E_tot,
                             const uint32_t* base, uint16_t* wh, int32_t* out_ids, float* out_w)
 {
@@ -77,11 +78,21 @@ __device__ inline void cta_scatter(const int32_t* idx, const float* w, int f0, i
     const int r1 = min(r0 + sub, f1);
     uint16_t* mine = wh + warp * E_tot;
     for (int i = tid; i < nw * E_tot; i += blockDim.x) wh[i] = 0;
-    __syncthreads();
-    for (int i0 = r0; i0 < r1; i0 += 32) {
-        const int i = i0 + lane;
+    // the warp's ids, loaded once (all steps in flight) and kept for both passes;
+    // a warp owns at most kSortChunk / (32 * warps) steps of 32 ids
+    constexpr int kMaxSteps = (kSortChunk + kSortThreads - 1) / kSortThreads;
+    int ev[kMaxSteps];
+#pragma unroll
+    for (int u = 0; u < kMaxSteps; ++u) {
+        const int i = r0 + u * 32 + lane;
         int e = (i < r1) ? idx[i] : kInvalidExpert;
-        if (e >= E_tot) e = kInvalidExpert;
+        ev[u] = (e >= E_tot) ? kInvalidExpert : e;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kMaxSteps; ++u) {
+        if (r0 + u * 32 >= r1) break;
+        const int e = ev[u];
         const unsigned peers = __match_any_sync(kFull, e);
         if (e >= 0 && lane == __ffs(peers) - 1) mine[e] = static_cast<uint16_t>(mine[e] + __popc(peers));
         __syncwarp();
@@ -97,10 +108,11 @@ __device__ inline void cta_scatter(const int32_t* idx, const float* w, int f0, i
     }
     __syncthreads();
     const unsigned lt = lanemask_lt();
-    for (int i0 = r0; i0 < r1; i0 += 32) {
-        const int i = i0 + lane;
-        int e = (i < r1) ? idx[i] : kInvalidExpert;
-        if (e >= E_tot) e = kInvalidExpert;
+#pragma unroll
+    for (int u = 0; u < kMaxSteps; ++u) {
+        if (r0 + u * 32 >= r1) break;
+        const int i = r0 + u * 32 + lane;
+        const int e = ev[u];
         const unsigned peers = __match_any_sync(kFull, e);
         if (e >= 0) {
             const uint32_t pos = base[e] + mine[e] + __popc(peers & lt);
