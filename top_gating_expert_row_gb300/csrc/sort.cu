@@ -7,8 +7,8 @@
 //   k_sort_scatter  every CTA reads the whole (chunks x E_tot) count table,
 //                   derives the padded per-expert offsets (block scan) and its
 //                   own start inside each expert's range (counts of the chunks
-//                   before it), scatters its pairs stably, and fills the
-//                   sentinels / expert ids of its share of the padded positions
+//                   before it), scatters its pairs stably, and writes the
+//                   sentinels / expert ids of its share of the experts
 //
 // The kernel boundary is the only grid-wide ordering, so nothing spins.
 #include "internal.h"
@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(kSortThreads) k_sort_hist(const int32_t* __res
     }
 #pragma unroll
     for (int u = 0; u < kSteps; ++u) {
+        if (f0 + u * kSortThreads + (tid & ~31) >= f1) break;  // the warp's ids all past the chunk
         int e = ev[u];
         if (f0 + u * kSortThreads + tid < f1 && (e < 0 || e >= E_tot)) {
             bad = true;
@@ -85,11 +86,11 @@ __global__ void __launch_bounds__(kSortThreads) k_sort_scatter(
     const int f0 = c * kSortChunk;
     const int f1 = min(f0 + kSortChunk, N);
     cta_scatter(idx, w, f0, f1, E_tot, base, wh, ids, sw);
-    // this CTA's share of the padded positions
-    const int share = static_cast<int>((P + nchunk - 1) / nchunk);
-    const int p0 = min(static_cast<int>(P), c * share);
-    const int p1 = min(static_cast<int>(P), p0 + share);
-    cta_fill_pads(off, cnt, E_tot, bm, p0, p1, N, ids, sw, eids);
+    // this CTA's share of the experts' padding and block ids
+    const int share = (E_tot + nchunk - 1) / nchunk;
+    const int e0 = min(E_tot, c * share);
+    const int e1 = min(E_tot, e0 + share);
+    cta_fill_pads(off, cnt, e0, e1, bm, N, ids, sw, eids);
 }
 
 int launch_sort(const int32_t* idx, const float* w, int N, int E_tot, int block_m, int32_t* ids, float* sw,

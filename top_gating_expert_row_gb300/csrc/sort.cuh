@@ -12,7 +12,7 @@
 //              range, and within a 32-entry step a pair's rank is the number of
 //              lower lanes holding the same expert
 //   pads       every padded position past an expert's pairs gets the sentinel,
-//              every block start gets its expert id (binary search on offsets)
+//              every block of an expert's range its id (a thread per expert)
 #pragma once
 
 #include "common.cuh"
@@ -82,11 +82,13 @@ __device__ inline void cta_scatter(const int32_t* idx, const float* w, int f0, i
     // a warp owns at most kSortChunk / (32 * warps) steps of 32 ids
     constexpr int kMaxSteps = (kSortChunk + kSortThreads - 1) / kSortThreads;
     int ev[kMaxSteps];
+    float wv[kMaxSteps];  // and their weights
 #pragma unroll
     for (int u = 0; u < kMaxSteps; ++u) {
         const int i = r0 + u * 32 + lane;
         int e = (i < r1) ? idx[i] : kInvalidExpert;
         ev[u] = (e >= E_tot) ? kInvalidExpert : e;
+        wv[u] = (w && i < r1) ? w[i] : 0.0f;
     }
     __syncthreads();
 #pragma unroll
@@ -117,7 +119,7 @@ __device__ inline void cta_scatter(const int32_t* idx, const float* w, int f0, i
         if (e >= 0) {
             const uint32_t pos = base[e] + mine[e] + __popc(peers & lt);
             out_ids[pos] = i;
-            if (out_w) out_w[pos] = w ? w[i] : 0.0f;
+            if (out_w) out_w[pos] = wv[u];
         }
         __syncwarp();
         if (e >= 0 && lane == __ffs(peers) - 1) mine[e] = static_cast<uint16_t>(mine[e] + __popc(peers));
@@ -125,24 +127,20 @@ __device__ inline void cta_scatter(const int32_t* idx, const float* w, int f0, i
     }
 }
 
-// Sentinels and expert ids for padded positions [p0, p1). off: E_tot+1
-// exclusive offsets (off[E_tot] = total), cnt: pairs per expert.
-__device__ inline void cta_fill_pads(const uint32_t* off, const uint32_t* cnt, int E_tot, int bm, int p0, int p1,
-                              int32_t sentinel, int32_t* out_ids, float* out_w, int32_t* expert_ids)
+// Sentinels and expert ids of experts [e0, e1), one thread per expert: the
+// padded tail of the expert's range, [off[e] + cnt[e], off[e+1]), gets the
+// sentinel (weight 0) and each block of the range gets the expert's id. off:
+// E_tot+1 exclusive offsets (multiples of bm), cnt: pairs per expert.
+__device__ inline void cta_fill_pads(const uint32_t* off, const uint32_t* cnt, int e0, int e1, int bm,
+                                     int32_t sentinel, int32_t* out_ids, float* out_w, int32_t* expert_ids)
 {
-    for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
-        int lo = 0, hi = E_tot;  // find the last e with off[e] <= p
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (off[mid] <= static_cast<uint32_t>(p)) lo = mid;
-            else hi = mid;
-        }
-        const uint32_t r = static_cast<uint32_t>(p) - off[lo];
-        if (r >= cnt[lo]) {
+    for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += blockDim.x) {
+        const uint32_t a = off[e], b = off[e + 1];
+        for (uint32_t p = a + cnt[e]; p < b; ++p) {
             out_ids[p] = sentinel;
             if (out_w) out_w[p] = 0.0f;
         }
-        if (p % bm == 0) expert_ids[p / bm] = lo;
+        for (uint32_t blk = a / bm; blk < b / bm; ++blk) expert_ids[blk] = e;
     }
 }
 
