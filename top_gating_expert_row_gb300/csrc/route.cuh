@@ -75,8 +75,10 @@ __host__ __device__ inline WarpLayout warp_layout(int k_r, int stop, int E, bool
 // group that is not among the topk_group best. A group's score is the fp32 sum
 // of its m largest keys, largest first. MAXM >= m bounds the per-lane list.
 // ---------------------------------------------------------------------------
+// group_kept: the same selection, returned as a mask of the kept groups (bit g
+// set: group g is kept) without touching the keys.
 template <int MAXM>
-__device__ void group_limit(uint32_t* skeys, int E, int G, int gk, int m, int lane)
+__device__ uint32_t group_kept(const uint32_t* skeys, int E, int G, int gk, int m, int lane)
 {
     const int gs = E / G;
     int lpg = 32 / G;                      // lanes per group, rounded down to a power of 2
@@ -86,6 +88,7 @@ __device__ void group_limit(uint32_t* skeys, int E, int G, int gk, int m, int la
 #pragma unroll
     for (int i = 0; i < MAXM; ++i) top[i] = 0u;
     if (g < G) {
+#pragma unroll 4
         for (int i = j; i < gs; i += lpg) {
             uint32_t k = skeys[g * gs + i];
 #pragma unroll
@@ -123,7 +126,14 @@ __device__ void group_limit(uint32_t* skeys, int E, int G, int gk, int m, int la
         const uint32_t o = __shfl_sync(kFull, sk, q * lpg);
         rank += (o > mine) || (o == mine && q < lane);
     }
-    const uint32_t kept = __ballot_sync(kFull, lane < G && rank < (uint32_t)gk);
+    return __ballot_sync(kFull, lane < G && rank < (uint32_t)gk);
+}
+
+template <int MAXM>
+__device__ void group_limit(uint32_t* skeys, int E, int G, int gk, int m, int lane)
+{
+    const int gs = E / G;
+    const uint32_t kept = group_kept<MAXM>(skeys, E, G, gk, m, lane);
     for (int q = 0; q < G; ++q)
         if (!((kept >> q) & 1u))
             for (int i = lane; i < gs; i += 32) skeys[q * gs + i] = 0u;
@@ -271,28 +281,29 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
         }
         __syncwarp();
         const int m = k_r / a.topk_group;
-        if (m <= 1) group_limit<1>(sk, E, a.n_group, a.topk_group, m, lane);
-        else if (m <= 2) group_limit<2>(sk, E, a.n_group, a.topk_group, m, lane);
-        else if (m <= 4) group_limit<4>(sk, E, a.n_group, a.topk_group, m, lane);
-        else group_limit<8>(sk, E, a.n_group, a.topk_group, m, lane);
-        __syncwarp();
+        uint32_t kept;
+        if (m <= 1) kept = group_kept<1>(sk, E, a.n_group, a.topk_group, m, lane);
+        else if (m <= 2) kept = group_kept<2>(sk, E, a.n_group, a.topk_group, m, lane);
+        else if (m <= 4) kept = group_kept<4>(sk, E, a.n_group, a.topk_group, m, lane);
+        else kept = group_kept<8>(sk, E, a.n_group, a.topk_group, m, lane);
+        // the keys are still in registers: drop those of the groups not kept.
+        // An element's group e / gs is taken as umulhi(e, ceil(2^32 / gs)), exact
+        // for e and gs below 2^12 (gs = 1: the group is e itself).
+        const uint32_t gs = static_cast<uint32_t>(E / a.n_group);
+        const uint32_t inv_gs = gs > 1u ? 0xffffffffu / gs + 1u : 0u;
         uint32_t lmax = 0u;
 #pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            const int e0 = v * 128 + lane4;
-            if (whole(v)) {
-                const uint4 q = *reinterpret_cast<const uint4*>(sk + e0);
-                key[v][0] = q.x; key[v][1] = q.y; key[v][2] = q.z; key[v][3] = q.w;
-            } else {
+        for (int v = 0; v < NV; ++v)
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    if (inside(v, c)) key[v][c] = sk[e0 + c];
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t e = static_cast<uint32_t>(v * 128 + lane4 + c);
+                const uint32_t g = gs > 1u ? __umulhi(e, inv_gs) : e;
+                const bool keep = e < static_cast<uint32_t>(E) && ((kept >> g) & 1u);
+                key[v][c] = keep ? key[v][c] : 0u;
+                lmax = max(lmax, key[v][c]);
             }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) lmax = max(lmax, key[v][c]);
-        }
         kmax = __reduce_max_sync(kFull, lmax);
-        __syncwarp();
+        __syncwarp();  // the staged keys are read no more; the region may be reused
     }
 
     // 3. selection
