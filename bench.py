@@ -267,8 +267,8 @@ def time_kernels(mr, w, dev, stream, calls=20, replays=5) -> dict:
     return out
 
 
-def decode_latency(mr, dev, stream, n_calls=200, Ts=synth.DECODE_TS) -> dict:
-    """Fused vs unfused decode route+sort (E=256, topk=8, bf16), eager and graph."""
+def decode_latency(mr, dev, stream, n_calls=200, Ts=synth.DECODE_TS, shape=synth.decode) -> dict:
+    """Fused vs unfused decode route+sort (default E=256, topk=8, bf16), eager and graph."""
     L = mr._lib
     res = {}
     s = stream.cuda_stream
@@ -321,7 +321,7 @@ def decode_latency(mr, dev, stream, n_calls=200, Ts=synth.DECODE_TS) -> dict:
     floor = {"eager_us": round(eager(noop), 2), "graph_us": round(graph(noop), 2)}
     res["launch_floor"] = floor
     for T in Ts:
-        w = synth.decode(T)
+        w = shape(T)
         x = w.make_logits().to(dev)
         p = mr.RouterParams(T=T, E=w.E, topk=w.topk, in_dtype=w.in_dtype, renorm=w.renorm)
         cp = p.c()
@@ -611,6 +611,9 @@ def main():
     if args.only == "decode":
         if rank == 0:
             ts = tuple(int(t) for t in args.decode_ts.split(","))
+            print(json.dumps({"decode_gpt_oss": decode_latency(mr, dev, torch.cuda.Stream(device=dev),
+                                                               args.decode_calls, (1, 4, 16, 32),
+                                                               synth.decode_gpt_oss)}), flush=True)
             print(json.dumps({"decode": decode_latency(mr, dev, torch.cuda.Stream(device=dev),
                                                        args.decode_calls, ts)}), flush=True)
         return 0
@@ -702,6 +705,8 @@ def main():
         line["e2e"] = e2e_rate(mr, w, dev, stream)
         if rank == 0:
             line["decode"] = decode_latency(mr, dev, stream, args.decode_calls)
+            line["decode_gpt_oss"] = decode_latency(mr, dev, stream, args.decode_calls, (1, 4, 16, 32),
+                                                    synth.decode_gpt_oss)
             line["prefill_route_sort"] = prefill_route_sort(mr, dev, stream)
             line["aux_loss"] = aux_loss_rates(mr, w, dev, stream)
             breakdown = {}

@@ -64,6 +64,8 @@ typedef enum { MR_F32 = 0, MR_BF16 = 1 } mr_dtype;
 #define MR_MAX_SORT_EXPERTS 4096 /* E_tot for moe_sort */
 #define MR_MAX_FUSED_TOKENS 16   /* T at or below which the fused call is one launch ... */
 #define MR_MAX_FUSED_EXPERTS 1024 /* ... when E is at most this */
+#define MR_MAX_FUSED_TOKENS_SMALL_E 32  /* and T at or below which it is one launch ... */
+#define MR_MAX_FUSED_EXPERTS_SMALL 256  /* ... when E is at most this */
 
 /*
  * Router options, one token per row ([TE] fused_topk_with_score_function).
@@ -232,11 +234,12 @@ int moe_sort_noalloc(const int32_t* topk_idx, const float* topk_w, int T, int to
 /*
  * moe_router_fused_fwd_sort -- moe_router_fwd (compact outputs) followed by moe_sort
  * over E_tot = E + n_shared experts ([FLY] fused top-k + sorting). For
- * T <= MR_MAX_FUSED_TOKENS and E <= MR_MAX_FUSED_EXPERTS it is ONE launch of one CTA;
- * above that (the pages report no gain from fusing beyond T = 16) it runs as the
- * separate forward and sort launches.
+ * T <= MR_MAX_FUSED_TOKENS and E <= MR_MAX_FUSED_EXPERTS, and for
+ * T <= MR_MAX_FUSED_TOKENS_SMALL_E and E <= MR_MAX_FUSED_EXPERTS_SMALL, it is ONE
+ * launch of one CTA; above that (the pages report no gain from fusing beyond T = 16
+ * and leave larger T open) it runs as the separate forward and sort launches.
  * topk_idx / topk_w are nullable (compact outputs written only when given). The
- * workspace (moe_router_fused_workspace_bytes, 0 for T <= MR_MAX_FUSED_TOKENS) holds
+ * workspace (moe_router_fused_workspace_bytes, 0 for the one-launch sizes) holds
  * the compact outputs when those are NULL and the sort's scratch (0 bytes for the
  * one-launch case).
  */

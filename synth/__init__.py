@@ -144,7 +144,12 @@ def decode(T: int) -> Workload:
     return Workload(f"decode_T{T}_E256_k8_bf16", T, 256, 8, SOFTMAX, BF16, renorm=1, block_m=32)
 
 
-DECODE_TS = (1, 2, 4, 8, 12, 16)
+def decode_gpt_oss(T: int) -> Workload:
+    """GPT-OSS-shaped decode: E=128, topk=4, bf16 N(0,1), softmax + renorm, block_m=32."""
+    return Workload(f"decode_T{T}_E128_k4_bf16", T, 128, 4, SOFTMAX, BF16, renorm=1, block_m=32)
+
+
+DECODE_TS = (1, 2, 4, 8, 12, 16, 24, 32)
 
 
 def large_softmax(topk: int) -> Workload:

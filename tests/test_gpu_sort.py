@@ -86,7 +86,13 @@ FUSED = [synth.decode(T) for T in synth.DECODE_TS] + [
     synth.Workload("decode_T16_grouped_shared", 16, 384, 9, synth.SIGMOID, synth.BF16, renorm=1, scaling=2.827,
                    n_group=8, topk_group=4, n_shared=1, bias_range=0.05, zipf_s=1.1, block_m=64),
     synth.Workload("decode_T5_e128_k4", 5, 128, 4, synth.SOFTMAX, synth.BF16, renorm=1, block_m=16),
-    synth.Workload("fallback_T17", 17, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
+    synth.Workload("fused32_T17", 17, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
+    synth.Workload("fused32_T32_e256_k8", 32, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
+    synth.Workload("fused32_T24_e128_k4", 24, 128, 4, synth.SOFTMAX, synth.BF16, renorm=1, block_m=16),
+    synth.Workload("fused32_T29_e100_sigmoid", 29, 100, 6, synth.SIGMOID, synth.F32, renorm=1, scaling=1.5,
+                   bias_range=0.1, block_m=8),
+    synth.Workload("fallback_T33", 33, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
+    synth.Workload("fallback_T17_e384", 17, 384, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
     synth.Workload("fallback_T300_grouped", 300, 384, 9, synth.SIGMOID, synth.BF16, renorm=1, scaling=2.827,
                    n_group=8, topk_group=4, n_shared=1, bias_range=0.05, block_m=64),
     synth.Workload("fallback_wide_T4_e2304", 4, 2304, 36, synth.SOFTMAX, synth.F32, block_m=8),

@@ -142,6 +142,9 @@ int launch_noop(cudaStream_t st)
 
 // ---- device status word ------------------------------------------------------------------------
 
+static_assert(MR_MAX_FUSED_TOKENS == 16 && MR_MAX_FUSED_TOKENS_SMALL_E == kFusedWideMaxTokens &&
+                  MR_MAX_FUSED_EXPERTS_SMALL == 128 * kFusedWideMaxNv,
+              "the header's fused-launch limits and the kernels' must agree");
 static_assert(kStatusTimeout == MR_ETIMEOUT, "device timeout bit and the C ABI's code must agree");
 
 // The library's status word on each device: kernels whose waits are bounded
@@ -507,7 +510,7 @@ size_t moe_router_fused_workspace_bytes(const mr_router_params* p, int block_m)
     if (check_router(p) != MR_OK || block_m < 1) return 0;
     const int nv = nv_index(p->E);
     if (nv < 0) return 0;
-    if (p->T <= MR_MAX_FUSED_TOKENS && kNvBuckets[nv] <= kFusedMaxNv) return 0;
+    if (fused_one_launch(p->T, kNvBuckets[nv])) return 0;
     const size_t N = static_cast<size_t>(p->T) * p->topk;
     return align_up(N * 4, 256) * 2 + sort_ws_bytes(static_cast<long long>(N), p->E + p->n_shared);
 }
@@ -526,14 +529,14 @@ int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int
     const int nv = nv_index(p->E);
     if (nv < 0) return MR_EUNSUPPORTED;
     const int k_r = p->topk - p->n_shared;
-    if (p->T <= MR_MAX_FUSED_TOKENS && kNvBuckets[nv] <= kFusedMaxNv) {
+    if (fused_one_launch(p->T, kNvBuckets[nv])) {
         RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, topk_idx, topk_w);
         SortArgs s{sorted_token_ids, sorted_weights, expert_ids, num_tokens_post_pad, E_tot, block_m,
                    log2_if_pow2(block_m)};
         // a one-CTA decode launch is bound by instruction fetch on a cold SM: the
         // arg-max path has the shorter code, so it is the default up to k_r = 32
         const bool sel = g_path.force == 2 || (g_path.force == 0 && k_r > 32);
-        const int nw = kFusedThreads / 32;
+        const int nw = (p->T > 16 ? kFusedWideThreads : kFusedThreads) / 32;
         const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, sel, a.n_group > 0);
         const size_t smem = static_cast<size_t>(L.bytes) * nw + fused_sort_layout(p->T * p->topk, E_tot, block_m).bytes;
         int dev = 0, maxsm = 0;

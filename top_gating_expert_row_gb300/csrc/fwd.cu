@@ -5,7 +5,8 @@
 //   k_router_fwd     persistent grid, 8 warps per CTA, one token row per warp
 //                    at a time (TransformerEngine PR 3012, fused_topk_with_
 //                    score_function; also serves fused_score_for_moe_aux_loss)
-//   k_fused_decode   ONE CTA for T <= 16 tokens: warp t routes token t, then
+//   k_fused_decode   ONE CTA for T <= 16 tokens (T <= 32 for E <= 256, with 32
+//                    warps): warp t routes token t, then
 //                    the whole CTA histograms, scans and scatters the T*topk
 //                    pairs in shared memory (FlyDSL PR 582, fused top-k gating
 //                    + MoE sorting at decode sizes)
@@ -122,8 +123,8 @@ __global__ void __launch_bounds__(kWideThreads, kWideMinBlocks) k_router_fwd_wid
     }
 }
 
-template <int NV, bool SELECT, bool FULL>
-__global__ void __launch_bounds__(kFusedThreads) k_fused_decode(RouteArgs a, SortArgs s)
+template <int NV, bool SELECT, bool FULL, int THREADS>
+__global__ void __launch_bounds__(THREADS) k_fused_decode(RouteArgs a, SortArgs s)
 {
     // A decode call is one short launch on one SM whose instruction cache is
     // usually cold, so this kernel keeps its executed code short: per-expert
@@ -247,15 +248,22 @@ FwdFn fwd_kernel(int nv_idx)
 }
 
 template <bool SELECT, bool FULL>
-FusedFn fused_kernel(int nv_idx)
+FusedFn fused_kernel(int nv_idx, bool wide)
 {
+    if (wide) {
+        switch (kNvBuckets[nv_idx]) {
+            case 1: return k_fused_decode<1, SELECT, FULL, kFusedWideThreads>;
+            case 2: return k_fused_decode<2, SELECT, FULL, kFusedWideThreads>;
+        }
+        return nullptr;
+    }
     switch (kNvBuckets[nv_idx]) {
-        case 1: return k_fused_decode<1, SELECT, FULL>;
-        case 2: return k_fused_decode<2, SELECT, FULL>;
-        case 3: return k_fused_decode<3, SELECT, FULL>;
-        case 4: return k_fused_decode<4, SELECT, FULL>;
-        case 6: return k_fused_decode<6, SELECT, FULL>;
-        case 8: return k_fused_decode<8, SELECT, FULL>;
+        case 1: return k_fused_decode<1, SELECT, FULL, kFusedThreads>;
+        case 2: return k_fused_decode<2, SELECT, FULL, kFusedThreads>;
+        case 3: return k_fused_decode<3, SELECT, FULL, kFusedThreads>;
+        case 4: return k_fused_decode<4, SELECT, FULL, kFusedThreads>;
+        case 6: return k_fused_decode<6, SELECT, FULL, kFusedThreads>;
+        case 8: return k_fused_decode<8, SELECT, FULL, kFusedThreads>;
     }
     return nullptr;
 }
@@ -301,15 +309,18 @@ int MR_CAT(launch_fused, MR_SUFFIX)(const RouteArgs& a, const SortArgs& s, int n
     // every chunk whole and vector-aligned: the specialisation without edge tests
     // (a shorter instruction stream, which is what a decode call waits on)
     const bool full = a.vec && a.E == 128 * kNvBuckets[nv_idx];
-    const FusedFn f = select ? (full ? fused_kernel<true, true>(nv_idx) : fused_kernel<true, false>(nv_idx))
-                             : (full ? fused_kernel<false, true>(nv_idx) : fused_kernel<false, false>(nv_idx));
+    const bool wide = a.T > 16;  // one warp per token: 32 warps
+    const FusedFn f = select ? (full ? fused_kernel<true, true>(nv_idx, wide) : fused_kernel<true, false>(nv_idx, wide))
+                             : (full ? fused_kernel<false, true>(nv_idx, wide)
+                                     : fused_kernel<false, false>(nv_idx, wide));
     if (!f) return cudaErrorInvalidValue;
-    const int nw = kFusedThreads / 32;
+    const int threads = wide ? kFusedWideThreads : kFusedThreads;
+    const int nw = threads / 32;
     const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, select, a.n_group > 0);
     const size_t smem = static_cast<size_t>(L.bytes) * nw + fused_sort_layout(a.T * a.topk, s.E_tot, s.block_m).bytes;
     int err = ensure_smem(reinterpret_cast<const void*>(f), smem);
     if (err != cudaSuccess) return err;
-    f<<<1, kFusedThreads, smem, st>>>(a, s);
+    f<<<1, threads, smem, st>>>(a, s);
     return cudaGetLastError();
 }
 

@@ -31,6 +31,15 @@ inline int nv_index(int E)
 
 // The one-CTA fused decode kernel keeps rows up to this many chunks (E <= 1024).
 constexpr int kFusedMaxNv = 8;
+// 16 < T <= 32 (E <= 256): the same one-CTA kernel with 32 warps
+constexpr int kFusedWideThreads = 1024;
+constexpr int kFusedWideMaxNv = 2;
+constexpr int kFusedWideMaxTokens = 32;
+// whether moe_router_fused_fwd_sort runs as one launch for T tokens of row bucket nv
+inline bool fused_one_launch(int T, int nv_bucket)
+{
+    return (T <= 16 && nv_bucket <= kFusedMaxNv) || (T <= kFusedWideMaxTokens && nv_bucket <= kFusedWideMaxNv);
+}
 // The forward keeps rows of up to this many chunks in registers (E <= 1024);
 // wider rows take the shared-memory routine, two warps per CTA.
 constexpr int kRegisterMaxNv = 8;
