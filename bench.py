@@ -612,7 +612,7 @@ def main():
         if rank == 0:
             ts = tuple(int(t) for t in args.decode_ts.split(","))
             print(json.dumps({"decode_gpt_oss": decode_latency(mr, dev, torch.cuda.Stream(device=dev),
-                                                               args.decode_calls, (1, 4, 16, 32),
+                                                               args.decode_calls, (1, 4, 16, 32, 64),
                                                                synth.decode_gpt_oss)}), flush=True)
             print(json.dumps({"decode": decode_latency(mr, dev, torch.cuda.Stream(device=dev),
                                                        args.decode_calls, ts)}), flush=True)
@@ -705,7 +705,7 @@ def main():
         line["e2e"] = e2e_rate(mr, w, dev, stream)
         if rank == 0:
             line["decode"] = decode_latency(mr, dev, stream, args.decode_calls)
-            line["decode_gpt_oss"] = decode_latency(mr, dev, stream, args.decode_calls, (1, 4, 16, 32),
+            line["decode_gpt_oss"] = decode_latency(mr, dev, stream, args.decode_calls, (1, 4, 16, 32, 64),
                                                     synth.decode_gpt_oss)
             line["prefill_route_sort"] = prefill_route_sort(mr, dev, stream)
             line["aux_loss"] = aux_loss_rates(mr, w, dev, stream)

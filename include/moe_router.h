@@ -64,7 +64,7 @@ typedef enum { MR_F32 = 0, MR_BF16 = 1 } mr_dtype;
 #define MR_MAX_SORT_EXPERTS 4096 /* E_tot for moe_sort */
 #define MR_MAX_FUSED_TOKENS 16   /* T at or below which the fused call is one launch ... */
 #define MR_MAX_FUSED_EXPERTS 1024 /* ... when E is at most this */
-#define MR_MAX_FUSED_TOKENS_SMALL_E 32  /* and T at or below which it is one launch ... */
+#define MR_MAX_FUSED_TOKENS_SMALL_E 64  /* and T at or below which it is one launch ... */
 #define MR_MAX_FUSED_EXPERTS_SMALL 256  /* ... when E is at most this */
 
 /*

@@ -149,7 +149,7 @@ def decode_gpt_oss(T: int) -> Workload:
     return Workload(f"decode_T{T}_E128_k4_bf16", T, 128, 4, SOFTMAX, BF16, renorm=1, block_m=32)
 
 
-DECODE_TS = (1, 2, 4, 8, 12, 16, 24, 32)
+DECODE_TS = (1, 2, 4, 8, 12, 16, 24, 32, 48, 64)
 
 
 def large_softmax(topk: int) -> Workload:

@@ -147,14 +147,18 @@ def test_sort_sizes_and_rejects(lib):
 
 
 def test_fused_rejects(lib):
-    cp = _p(lib, T=64).c()
+    cp = _p(lib, T=65).c()
     f = lib._lib.moe_router_fused_fwd_sort
     assert f(ctypes.byref(cp), FAKE, 0, None, None, FAKE, FAKE, FAKE, FAKE, None, 0, None) == 1
     assert f(ctypes.byref(cp), FAKE, 8, None, None, None, FAKE, FAKE, FAKE, None, 0, None) == 1
-    # above the one-launch size a workspace is needed
-    assert lib.moe_router_fused_workspace_bytes(_p(lib, T=64), 8) > 0
+    # above the one-launch sizes a workspace is needed
+    assert lib.moe_router_fused_workspace_bytes(_p(lib, T=65), 8) > 0
     assert f(ctypes.byref(cp), FAKE, 8, None, None, FAKE, FAKE, FAKE, FAKE, None, 0, None) == 1
-    assert lib.moe_router_fused_workspace_bytes(_p(lib, T=16), 8) == 0
+    assert lib.moe_router_fused_workspace_bytes(_p(lib, T=17, E=512), 8) > 0
+    # one launch: T <= 16 for E <= 1024, T <= 64 for E <= 256
+    assert lib.moe_router_fused_workspace_bytes(_p(lib, T=16, E=1024, topk=8), 8) == 0
+    assert lib.moe_router_fused_workspace_bytes(_p(lib, T=64, E=256, topk=8), 8) == 0
+    assert lib.moe_router_fused_workspace_bytes(_p(lib, T=64), 8) == 0
 
 
 def test_set_topk_path(lib):

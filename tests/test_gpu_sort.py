@@ -91,7 +91,11 @@ FUSED = [synth.decode(T) for T in synth.DECODE_TS] + [
     synth.Workload("fused32_T24_e128_k4", 24, 128, 4, synth.SOFTMAX, synth.BF16, renorm=1, block_m=16),
     synth.Workload("fused32_T29_e100_sigmoid", 29, 100, 6, synth.SIGMOID, synth.F32, renorm=1, scaling=1.5,
                    bias_range=0.1, block_m=8),
-    synth.Workload("fallback_T33", 33, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
+    synth.Workload("fused64_T33", 33, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
+    synth.Workload("fused64_T64_e256_k8", 64, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
+    synth.Workload("fused64_T50_e128_k4_grouped", 50, 128, 4, synth.SIGMOID, synth.BF16, renorm=1, n_group=4,
+                   topk_group=2, bias_range=0.05, block_m=16),
+    synth.Workload("fallback_T65", 65, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
     synth.Workload("fallback_T17_e384", 17, 384, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
     synth.Workload("fallback_T300_grouped", 300, 384, 9, synth.SIGMOID, synth.BF16, renorm=1, scaling=2.827,
                    n_group=8, topk_group=4, n_shared=1, bias_range=0.05, block_m=64),

@@ -27,7 +27,7 @@ MR_SOFTMAX, MR_SIGMOID = 0, 1
 MR_F32, MR_BF16 = 0, 1
 MR_MAX_FUSED_TOKENS = 16
 MR_MAX_FUSED_EXPERTS = 1024
-MR_MAX_FUSED_TOKENS_SMALL_E = 32
+MR_MAX_FUSED_TOKENS_SMALL_E = 64
 MR_MAX_FUSED_EXPERTS_SMALL = 256
 
 

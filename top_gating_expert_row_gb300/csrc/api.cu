@@ -538,7 +538,8 @@ int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int
         const bool sel = g_path.force == 2 || (g_path.force == 0 && k_r > 32);
         const int nw = (p->T > 16 ? kFusedWideThreads : kFusedThreads) / 32;
         const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, sel, a.n_group > 0);
-        const size_t smem = static_cast<size_t>(L.bytes) * nw + fused_sort_layout(p->T * p->topk, E_tot, block_m).bytes;
+        const size_t smem = static_cast<size_t>(L.bytes) * nw +
+                            fused_sort_layout(p->T * p->topk, E_tot, block_m, p->T > 16 ? 8 : 4).bytes;
         int dev = 0, maxsm = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)

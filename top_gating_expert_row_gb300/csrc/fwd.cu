@@ -5,11 +5,13 @@
 //   k_router_fwd     persistent grid, 8 warps per CTA, one token row per warp
 //                    at a time (TransformerEngine PR 3012, fused_topk_with_
 //                    score_function; also serves fused_score_for_moe_aux_loss)
-//   k_fused_decode   ONE CTA for T <= 16 tokens (T <= 32 for E <= 256, with 32
-//                    warps): warp t routes token t, then
+//   k_fused_decode   ONE CTA for T <= 16 tokens (T <= 64 for E <= 256, with 32
+//                    warps): warp t routes token t (and t + 32), then
 //                    the whole CTA histograms, scans and scatters the T*topk
 //                    pairs in shared memory (FlyDSL PR 582, fused top-k gating
 //                    + MoE sorting at decode sizes)
+#include <type_traits>
+
 #include "internal.h"
 #include "route_wide.cuh"
 #include "sort.cuh"
@@ -124,51 +126,56 @@ __global__ void __launch_bounds__(kWideThreads, kWideMinBlocks) k_router_fwd_wid
 }
 
 template <int NV, bool SELECT, bool FULL, int THREADS>
-__global__ void __launch_bounds__(THREADS) k_fused_decode(RouteArgs a, SortArgs s)
+__global__ void __launch_bounds__(THREADS, 1) k_fused_decode(RouteArgs a, SortArgs s)
 {
     // A decode call is one short launch on one SM whose instruction cache is
     // usually cold, so this kernel keeps its executed code short: per-expert
     // token bitmasks give every pair its stable rank directly (a token's topk
     // experts are distinct, so the rank of (t, j) inside expert e is the number
     // of earlier tokens that chose e), one warp scans the padded counts, and
-    // three block barriers separate the phases.
+    // three block barriers separate the phases. The 32-warp form routes up to
+    // 64 tokens (warp w: tokens w and w + 32) with 64-bit masks.
+    using Mask = typename std::conditional<(THREADS > kFusedThreads), unsigned long long, uint32_t>::type;
     extern __shared__ __align__(16) unsigned char smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5, nt = blockDim.x;
     const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, SELECT, a.n_group > 0);
     const int N = a.T * a.topk;
     const int E_tot = s.E_tot, bm = s.block_m;
-    const FusedSortLayout F = fused_sort_layout(N, E_tot, bm);
+    const FusedSortLayout F = fused_sort_layout(N, E_tot, bm, sizeof(Mask));
     unsigned char* base = smem + static_cast<size_t>(nw) * L.bytes;
     int32_t* s_idx = reinterpret_cast<int32_t*>(base + F.idx);
     float* s_w = reinterpret_cast<float*>(base + F.w);
-    uint32_t* mask = reinterpret_cast<uint32_t*>(base + F.mask);
+    Mask* mask = reinterpret_cast<Mask*>(base + F.mask);
     uint32_t* off = reinterpret_cast<uint32_t*>(base + F.off);
     int32_t* blk = reinterpret_cast<int32_t*>(base + F.blk);
+    auto popc = [](Mask m) { return static_cast<uint32_t>(sizeof(Mask) == 8 ? __popcll(m) : __popc(static_cast<uint32_t>(m))); };
 
     for (int e = tid; e < E_tot; e += nt) mask[e] = 0u;
-    if (warp < a.T) {
+    {
         unsigned char* wsm = smem + static_cast<size_t>(warp) * L.bytes;
         uint32_t warm = 0u;
-        const float scale = route_row<kScore, InT, NV, SELECT, FULL>(a, warp, wsm, L, lane, warm);
-        const size_t o = static_cast<size_t>(warp) * a.topk;
-        const uint32_t* win_idx = reinterpret_cast<const uint32_t*>(wsm + L.win_idx);
-        const float* win_val = reinterpret_cast<const float*>(wsm + L.win_val);
-        for (int j = lane; j < a.topk; j += 32) {  // compact outputs, to shared and global
-            const bool routed = j < a.k_r;
-            const int32_t id = routed ? static_cast<int32_t>(win_idx[j]) : a.E + (j - a.k_r);
-            const float wv = routed ? __fmul_rn(win_val[j], scale) : a.shared_weight;
-            s_idx[o + j] = id;
-            s_w[o + j] = wv;
-            if (a.topk_idx) a.topk_idx[o + j] = id;
-            if (a.topk_w) a.topk_w[o + j] = wv;
+        for (int tok = warp; tok < a.T; tok += nw) {
+            const float scale = route_row<kScore, InT, NV, SELECT, FULL>(a, tok, wsm, L, lane, warm);
+            const size_t o = static_cast<size_t>(tok) * a.topk;
+            const uint32_t* win_idx = reinterpret_cast<const uint32_t*>(wsm + L.win_idx);
+            const float* win_val = reinterpret_cast<const float*>(wsm + L.win_val);
+            for (int j = lane; j < a.topk; j += 32) {  // compact outputs, to shared and global
+                const bool routed = j < a.k_r;
+                const int32_t id = routed ? static_cast<int32_t>(win_idx[j]) : a.E + (j - a.k_r);
+                const float wv = routed ? __fmul_rn(win_val[j], scale) : a.shared_weight;
+                s_idx[o + j] = id;
+                s_w[o + j] = wv;
+                if (a.topk_idx) a.topk_idx[o + j] = id;
+                if (a.topk_w) a.topk_w[o + j] = wv;
+            }
+            __syncwarp();  // the winner lists are rewritten by the warp's next token
         }
     }
     __syncthreads();
-    if (warp < a.T) {
-        __syncwarp();
+    for (int tok = warp; tok < a.T; tok += nw) {
         for (int j = lane; j < a.topk; j += 32) {
-            const int e = s_idx[warp * a.topk + j];
-            if (e >= 0 && e < E_tot) atomicOr(mask + e, 1u << warp);  // range check: NaN rows only
+            const int e = s_idx[tok * a.topk + j];
+            if (e >= 0 && e < E_tot) atomicOr(mask + e, Mask(1) << tok);  // range check: NaN rows only
         }
     }
     __syncthreads();
@@ -183,12 +190,12 @@ __global__ void __launch_bounds__(THREADS) k_fused_decode(RouteArgs a, SortArgs 
         const int e0 = lane * per;
         uint32_t local = 0u;
         for (int i = 0; i < per; ++i)
-            if (e0 + i < E_tot) local += nblocks(__popc(mask[e0 + i]));
+            if (e0 + i < E_tot) local += nblocks(popc(mask[e0 + i]));
         uint32_t run = warp_exclusive_scan(local, lane);  // in blocks
         for (int i = 0; i < per; ++i) {
             const int e = e0 + i;
             if (e >= E_tot) break;
-            const uint32_t nb = nblocks(__popc(mask[e]));
+            const uint32_t nb = nblocks(popc(mask[e]));
             off[e] = run * bm;
             for (uint32_t b = 0; b < nb; ++b) blk[run + b] = e;
             run += nb;
@@ -200,14 +207,14 @@ __global__ void __launch_bounds__(THREADS) k_fused_decode(RouteArgs a, SortArgs 
         }
     }
     __syncthreads();
-    // real pairs: warp t writes its token's slots
-    if (warp < a.T) {
-        const uint32_t before = (1u << warp) - 1u;
+    // real pairs: a token's warp writes its slots
+    for (int tok = warp; tok < a.T; tok += nw) {
+        const Mask before = (Mask(1) << tok) - 1u;
         for (int j = lane; j < a.topk; j += 32) {
-            const int f = warp * a.topk + j;
+            const int f = tok * a.topk + j;
             const int e = s_idx[f];
             if (e < 0 || e >= E_tot) continue;
-            const uint32_t pos = off[e] + __popc(mask[e] & before);
+            const uint32_t pos = off[e] + popc(mask[e] & before);
             s.ids[pos] = f;
             if (s.w) s.w[pos] = s_w[f];
         }
@@ -216,7 +223,7 @@ __global__ void __launch_bounds__(THREADS) k_fused_decode(RouteArgs a, SortArgs 
     const int nblk = static_cast<int>(off[E_tot]) / bm;
     for (int b = warp; b < nblk; b += nw) {
         const int e = blk[b];
-        const uint32_t c = __popc(mask[e]);
+        const uint32_t c = popc(mask[e]);
         const uint32_t r_first = static_cast<uint32_t>(b * bm) - off[e];
         for (int r = lane; r < bm; r += 32) {
             if (r_first + r >= c) {
@@ -317,7 +324,8 @@ int MR_CAT(launch_fused, MR_SUFFIX)(const RouteArgs& a, const SortArgs& s, int n
     const int threads = wide ? kFusedWideThreads : kFusedThreads;
     const int nw = threads / 32;
     const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, select, a.n_group > 0);
-    const size_t smem = static_cast<size_t>(L.bytes) * nw + fused_sort_layout(a.T * a.topk, s.E_tot, s.block_m).bytes;
+    const size_t smem = static_cast<size_t>(L.bytes) * nw +
+                        fused_sort_layout(a.T * a.topk, s.E_tot, s.block_m, wide ? 8 : 4).bytes;
     int err = ensure_smem(reinterpret_cast<const void*>(f), smem);
     if (err != cudaSuccess) return err;
     f<<<1, threads, smem, st>>>(a, s);

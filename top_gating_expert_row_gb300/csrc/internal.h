@@ -31,10 +31,11 @@ inline int nv_index(int E)
 
 // The one-CTA fused decode kernel keeps rows up to this many chunks (E <= 1024).
 constexpr int kFusedMaxNv = 8;
-// 16 < T <= 32 (E <= 256): the same one-CTA kernel with 32 warps
+// 16 < T <= 64 (E <= 256): the same one-CTA kernel with 32 warps, each routing
+// up to two tokens, and 64-bit token masks
 constexpr int kFusedWideThreads = 1024;
 constexpr int kFusedWideMaxNv = 2;
-constexpr int kFusedWideMaxTokens = 32;
+constexpr int kFusedWideMaxTokens = 64;
 // whether moe_router_fused_fwd_sort runs as one launch for T tokens of row bucket nv
 inline bool fused_one_launch(int T, int nv_bucket)
 {
@@ -76,7 +77,8 @@ struct FusedSortLayout {
     int idx, w, mask, off, blk, bytes;
 };
 
-__host__ __device__ inline FusedSortLayout fused_sort_layout(int N, int E_tot, int bm)
+// mask_bytes: bytes of one expert's token mask (4 for T <= 32, 8 for T <= 64)
+__host__ __device__ inline FusedSortLayout fused_sort_layout(int N, int E_tot, int bm, int mask_bytes)
 {
     FusedSortLayout F;
     const int nonempty = N < E_tot ? N : E_tot;
@@ -84,7 +86,7 @@ __host__ __device__ inline FusedSortLayout fused_sort_layout(int N, int E_tot, i
     int o = 0;
     F.idx = o; o += align16(N * 4);
     F.w = o; o += align16(N * 4);
-    F.mask = o; o += align16(E_tot * 4);
+    F.mask = o; o += align16(E_tot * mask_bytes);
     F.off = o; o += align16((E_tot + 1) * 4);
     F.blk = o; o += align16((nblk > 0 ? nblk : 1) * 4);
     F.bytes = o;
