@@ -210,16 +210,16 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
             for (int v = 0; v < NV; ++v) {
                 const int e0 = v * 128 + lane4;
                 if (whole(v)) {
-                    float4 q = *reinterpret_cast<const float4*>(vbuf + e0);
-                    q.x = exp_value(__fsub_rn(q.x, m));
-                    q.y = exp_value(__fsub_rn(q.y, m));
-                    q.z = exp_value(__fsub_rn(q.z, m));
-                    q.w = exp_value(__fsub_rn(q.w, m));
-                    sum[0] = __fadd_rn(sum[0], q.x);
-                    sum[1] = __fadd_rn(sum[1], q.y);
-                    sum[2] = __fadd_rn(sum[2], q.z);
-                    sum[3] = __fadd_rn(sum[3], q.w);
-                    *reinterpret_cast<float4*>(vbuf + e0) = q;
+                    // packed fp32x2 (bit-identical to exp_value / __fadd_rn per value);
+                    // x - m as x + (-m), the same IEEE result
+                    const float4 q = *reinterpret_cast<const float4*>(vbuf + e0);
+                    const float2 negm = make_float2(-m, -m);
+                    const float2 e01 = exp_value2(__fadd2_rn(make_float2(q.x, q.y), negm));
+                    const float2 e23 = exp_value2(__fadd2_rn(make_float2(q.z, q.w), negm));
+                    const float2 s01 = __fadd2_rn(make_float2(sum[0], sum[1]), e01);
+                    const float2 s23 = __fadd2_rn(make_float2(sum[2], sum[3]), e23);
+                    sum[0] = s01.x; sum[1] = s01.y; sum[2] = s23.x; sum[3] = s23.y;
+                    *reinterpret_cast<float4*>(vbuf + e0) = make_float4(e01.x, e01.y, e23.x, e23.y);
                 } else {
                     for (int c = 0; c < 4; ++c)
                         if (inside(v, c)) {
@@ -494,8 +494,9 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
             if (vec && whole(v)) {
                 if (irow) {
                     const float4 q = *reinterpret_cast<const float4*>(vbuf + e0);
-                    *reinterpret_cast<float4*>(irow + e0) =
-                        make_float4(__fmul_rn(q.x, vmul), __fmul_rn(q.y, vmul), __fmul_rn(q.z, vmul), __fmul_rn(q.w, vmul));
+                    const float2 xy = __fmul2_rn(make_float2(q.x, q.y), make_float2(vmul, vmul));
+                    const float2 zw = __fmul2_rn(make_float2(q.z, q.w), make_float2(vmul, vmul));
+                    *reinterpret_cast<float4*>(irow + e0) = make_float4(xy.x, xy.y, zw.x, zw.y);
                 }
                 if (prow) {
                     const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
