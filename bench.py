@@ -267,6 +267,42 @@ def time_kernels(mr, w, dev, stream, calls=20, replays=5) -> dict:
     return out
 
 
+def bf16_rates(mr, dev, stream, calls=20, replays=5) -> dict:
+    """SURVEY-f4 shape: T=8192 E=2304 topk=36 softmax with bf16 logits; the forward
+    writes bf16 probs, the backward takes and returns bf16 gradients (the
+    intermediate stays fp32): 9 bytes per element each. Graph replays rotating
+    over buffer sets larger than 3x L2."""
+    w = synth.Workload("softmax_T8192_E2304_k36_bf16", 8192, 2304, 36, synth.SOFTMAX, synth.BF16)
+    sets = []
+    while len(sets) < 3:
+        launches, t, p = make_step(mr, w, dev, stream)
+        g16 = t["g"].to(torch.bfloat16)
+        dx16 = torch.empty_like(g16)
+        cp = p.c()
+        L, s = mr._lib, stream.cuda_stream
+
+        def bwd(cp=cp, g16=g16, dx16=dx16, t=t, owned=(p, launches)):
+            rc = L.moe_router_bwd_dtype(ctypes.byref(cp), mr.MR_BF16, g16.data_ptr(), t["inter"].data_ptr(),
+                                        t["map"].data_ptr(), dx16.data_ptr(), s)
+            if rc != 0:
+                raise RuntimeError(mr.strerror(rc))
+
+        with torch.cuda.stream(stream):
+            dict(launches)["fwd"]()
+        sets.append({"fwd": dict(launches)["fwd"], "bwd_bf16": bwd})
+    torch.cuda.synchronize()
+    n = w.T * w.E
+    nbytes = {"fwd": kernel_bytes("fwd", w.T, w.E, w.topk, 2), "bwd_bf16": n * (2 + 4 + 1 + 2)}
+    pk = peaks()["hbm_gbs"]
+    out = {"workload": w.name, "timing": f"CUDA graph, {calls} calls per replay over {len(sets)} buffer sets"}
+    for name, nb in nbytes.items():
+        it = iter(range(10 ** 9))
+        us = graph_us(lambda: sets[next(it) % len(sets)][name](), stream, calls, replays)
+        gbs = nb / (us * 1e-6) / 1e9
+        out[name] = {"us": round(us, 2), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / pk, 3)}
+    return out
+
+
 def decode_latency(mr, dev, stream, n_calls=200, Ts=synth.DECODE_TS, shape=synth.decode) -> dict:
     """Fused vs unfused decode route+sort (default E=256, topk=8, bf16), eager and graph."""
     L = mr._lib
@@ -585,7 +621,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["all", "step", "decode", "aux_loss", "prefill"], default="all",
+    ap.add_argument("--only", choices=["all", "step", "decode", "aux_loss", "prefill", "bf16"], default="all",
                     help="step: the timed step only; decode: the decode latency table only "
                          "(both used for profiling captures)")
     ap.add_argument("--decode-calls", type=int, default=200, help="calls per decode timing loop")
@@ -616,6 +652,10 @@ def main():
                                                                synth.decode_gpt_oss)}), flush=True)
             print(json.dumps({"decode": decode_latency(mr, dev, torch.cuda.Stream(device=dev),
                                                        args.decode_calls, ts)}), flush=True)
+        return 0
+    if args.only == "bf16":
+        if rank == 0:
+            print(json.dumps({"bf16": bf16_rates(mr, dev, torch.cuda.Stream(device=dev))}), flush=True)
         return 0
     if args.only == "prefill":
         if rank == 0:
@@ -709,6 +749,7 @@ def main():
                                                     synth.decode_gpt_oss)
             line["prefill_route_sort"] = prefill_route_sort(mr, dev, stream)
             line["aux_loss"] = aux_loss_rates(mr, w, dev, stream)
+            line["bf16"] = bf16_rates(mr, dev, stream)
             breakdown = {}
             for wl in [synth.large_softmax(k) for k in synth.LARGE_TOPKS] + [synth.large_e_sigmoid()]:
                 breakdown[wl.name] = time_kernels(mr, wl, dev, stream)

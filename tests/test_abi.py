@@ -169,6 +169,16 @@ def test_set_topk_path(lib):
     assert lib._lib.moe_router_expf(None, None, 0, None) == 0
 
 
+def test_bwd_dtype_rejects(lib):
+    cp = _p(lib).c()
+    f = lib._lib.moe_router_bwd_dtype
+    assert f(ctypes.byref(cp), 5, FAKE, FAKE, FAKE, FAKE, None) == lib.MR_EINVAL
+    assert f(ctypes.byref(cp), lib.MR_BF16, None, FAKE, FAKE, FAKE, None) == lib.MR_EINVAL
+    assert f(ctypes.byref(cp), lib.MR_BF16, FAKE, FAKE, FAKE, None, None) == lib.MR_EINVAL
+    assert f(ctypes.byref(_p(lib, E=3000).c()), lib.MR_BF16, FAKE, FAKE, FAKE, FAKE, None) == lib.MR_EUNSUPPORTED
+    assert f(ctypes.byref(_p(lib, T=0).c()), lib.MR_BF16, FAKE, FAKE, FAKE, FAKE, None) == lib.MR_OK
+
+
 def test_aux_loss_sizes_and_rejects(lib):
     L = lib._lib
     assert L.moe_aux_loss_workspace_bytes(0, 64) == 0

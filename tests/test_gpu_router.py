@@ -191,6 +191,30 @@ def test_bwd_matches_oracle(mr, orc, w):
     assert_close(dx, ref, f"{w.name} grad_logits")
 
 
+BWD_BF16_CASES = [W("e2304_k36_bf16", 150, 2304, 36, SM, BF16), W("e2304_k36_sig_bf16", 150, 2304, 36, SG, BF16,
+                                                                   renorm=1, scaling=2.5, bias_range=0.1),
+                  W("e512_k22_bf16", 300, 512, 22, SM, BF16, sigma=2.0),
+                  W("e100_k5_renorm_bf16", 90, 100, 5, SM, BF16, renorm=1, scaling=0.7),
+                  W("e37_sig_bf16", 40, 37, 4, SG, BF16, renorm=1)]
+
+
+@pytest.mark.parametrize("w", BWD_BF16_CASES, ids=lambda w: w.name)
+def test_bwd_bf16_grads_match_oracle(mr, orc, w):
+    """bf16 logits: grad_probs in and grad_logits out in bf16, the intermediate in
+    fp32; grad_logits must be a correct bf16 rounding of a value within the fp32
+    bound of the oracle's gradient of the same (bf16) inputs."""
+    x, b, xg, bg = gpu_inputs(w)
+    out = gpu_route(mr, w, xg, bg, 0, compact=False)
+    g = (synth.grad(w.T, w.E).cuda() * out["routing_map"]).to(torch.bfloat16).contiguous()
+    p = mr.params_for(xg, w.topk, score_fn=w.score_fn, renorm=w.renorm, scaling=w.scaling, bias=bg)
+    dx = mr.route_bwd(p, g, out["intermediate"], out["routing_map"])
+    torch.cuda.synchronize()
+    assert dx.dtype == torch.bfloat16
+    ref = orc.router_bwd(g.cpu().double().numpy(), out["intermediate"].cpu().double().numpy(),
+                         out["routing_map"].cpu().numpy(), w.score_fn, w.renorm, w.scaling)
+    assert_bf16_close(dx, ref, f"{w.name} grad_logits (bf16)")
+
+
 @pytest.mark.parametrize("w", [synth.large_softmax(22), synth.large_e_softmax(), synth.large_e_sigmoid()],
                          ids=lambda w: w.name)
 def test_bwd_full_size_sampled_rows(mr, orc, w):

@@ -60,6 +60,7 @@ _SIGS = {
     "moe_router_expf": ([_P, _P, _I, _P], _I),
     "moe_router_noop": ([_P], _I),
     "moe_router_device_status": ([_P, _I, _P], _I),
+    "moe_router_bwd_dtype": ([_PP, _I, _P, _P, _P, _P, _P], _I),
     "moe_tokens_per_expert": ([_I, _I, _P, _P, _P], _I),
     "moe_aux_loss_workspace_bytes": ([_I, _I], _SZ),
     "moe_aux_loss_fwd": ([_I, _I, _I, ctypes.c_float, ctypes.c_longlong, _P, _P, _P, _P, _SZ, _P], _I),
@@ -164,6 +165,13 @@ def moe_router_fwd(p, logits, probs=None, routing_map=None, intermediate=None, t
     return _ok(_lib.moe_router_fwd(ctypes.byref(cp), _ptr(logits), _ptr(probs), _ptr(routing_map),
                                    _ptr(intermediate), _ptr(topk_idx), _ptr(topk_w), _stream(stream)),
                "moe_router_fwd")
+
+
+def moe_router_bwd_dtype(p, grad_dtype, grad_probs, intermediate, routing_map, grad_logits, stream=None) -> int:
+    cp = _params(p)
+    return _ok(_lib.moe_router_bwd_dtype(ctypes.byref(cp), grad_dtype, _ptr(grad_probs), _ptr(intermediate),
+                                         _ptr(routing_map), _ptr(grad_logits), _stream(stream)),
+               "moe_router_bwd_dtype")
 
 
 def moe_router_bwd(p, grad_probs, intermediate, routing_map, grad_logits, stream=None) -> int:
@@ -316,6 +324,11 @@ def route(logits: torch.Tensor, topk: int, dense: bool = True, compact: bool = T
 
 
 def route_bwd(p: RouterParams, grad_probs, intermediate, routing_map, stream=None) -> torch.Tensor:
+    """grad_logits in grad_probs' dtype (fp32, or bf16 for bf16 logits)."""
+    if grad_probs.dtype == torch.bfloat16:
+        dx = torch.empty(intermediate.shape, dtype=torch.bfloat16, device=intermediate.device)
+        moe_router_bwd_dtype(p, MR_BF16, grad_probs, intermediate, routing_map, dx, stream)
+        return dx
     dx = torch.empty_like(intermediate)
     moe_router_bwd(p, grad_probs, intermediate, routing_map, dx, stream)
     return dx

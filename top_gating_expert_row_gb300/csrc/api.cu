@@ -388,6 +388,27 @@ int moe_router_bwd(const mr_router_params* p, const float* grad_probs, const flo
                                 p->renorm ? 1 : 0, p->scaling, vec, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int moe_router_bwd_dtype(const mr_router_params* p, int grad_dtype, const void* grad_probs,
+                         const float* intermediate, const uint8_t* routing_map, void* grad_logits, mr_stream_t stream)
+{
+    if (grad_dtype == MR_F32)
+        return moe_router_bwd(p, static_cast<const float*>(grad_probs), intermediate, routing_map,
+                              static_cast<float*>(grad_logits), stream);
+    if (grad_dtype != MR_BF16) return MR_EINVAL;
+    if (!p || !grad_probs || !intermediate || !routing_map || !grad_logits) return MR_EINVAL;
+    if (p->T < 0 || p->E < 1) return MR_EINVAL;
+    if (p->score_fn != MR_SOFTMAX && p->score_fn != MR_SIGMOID) return MR_EINVAL;
+    if (static_cast<long long>(p->T) * p->E > INT_MAX) return MR_EINVAL;
+    if (p->E > MR_MAX_EXPERTS) return MR_EUNSUPPORTED;
+    if (p->T == 0) return MR_OK;
+    const int nv = nv_index(p->E);
+    const bool vec = p->E % 4 == 0 && aligned(grad_probs, 8) && aligned(intermediate, 16) &&
+                     aligned(grad_logits, 8) && aligned(routing_map, 4);
+    return from_cuda(launch_bwd_bf16(p->score_fn, nv, static_cast<const __nv_bfloat16*>(grad_probs), intermediate,
+                                     routing_map, static_cast<__nv_bfloat16*>(grad_logits), p->T, p->E,
+                                     p->renorm ? 1 : 0, p->scaling, vec, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int moe_aux_scores_bwd(int T, int E, int score_fn, const float* grad_scores, const float* scores,
                        float* grad_logits, mr_stream_t stream)
 {

@@ -7,43 +7,69 @@
 //   ds_i = (c * m_i / A) * (g_i - B / A)          (renorm; A = sum m s, B = sum m s g)
 //   softmax: dx_i = s_i * (ds_i - sum_j s_j ds_j);  sigmoid: dx_i = ds_i * s_i * (1 - s_i)
 // The aux-score backward is the same with m = 1, c = 1 and no renorm.
+#include <type_traits>
+
 #include "internal.h"
 
 namespace mr {
 
-template <int SCORE, int NV, bool HAS_MAP>
-__global__ void __launch_bounds__(kBwdThreads) k_router_bwd(const float* __restrict__ grad,
+// GradT: the dtype of grad and dx (fp32, or bf16 for bf16 logits: the
+// gradient is computed in fp32 and rounded once when stored).
+template <int SCORE, int NV, bool HAS_MAP, typename GradT>
+__global__ void __launch_bounds__(kBwdThreads) k_router_bwd(const GradT* __restrict__ grad,
                                                             const float* __restrict__ inter,
                                                             const uint8_t* __restrict__ map,
-                                                            float* __restrict__ dx, int T, int E,
+                                                            GradT* __restrict__ dx, int T, int E,
                                                             int renorm, float c, int vec)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    constexpr bool kPacked = !std::is_same<GradT, float>::value;
     for (int t = blockIdx.x * nw + warp; t < T; t += gridDim.x * nw) {
         const size_t ro = static_cast<size_t>(t) * E;
-        float g[NV][4], s[NV][4];
+        // fp32 grads go straight into d; bf16 grads stay packed (two per word)
+        // until used, so every row load can be in flight at once within the
+        // register budget. d then holds ds.
+        float d[NV][4], s[NV][4];
+        uint2 gp[NV];
         uint32_t m[NV];
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             const int e0 = (v * 32 + lane) * 4;
             if (vec && e0 + 4 <= E) {
-                const float4 a = __ldcs(reinterpret_cast<const float4*>(grad + ro + e0));
+                if (kPacked) {
+                    gp[v] = __ldcs(reinterpret_cast<const uint2*>(grad + ro + e0));
+                } else {
+                    const float4 a = __ldcs(reinterpret_cast<const float4*>(grad + ro + e0));
+                    d[v][0] = a.x; d[v][1] = a.y; d[v][2] = a.z; d[v][3] = a.w;
+                }
                 const float4 b = __ldcs(reinterpret_cast<const float4*>(inter + ro + e0));
-                g[v][0] = a.x; g[v][1] = a.y; g[v][2] = a.z; g[v][3] = a.w;
                 s[v][0] = b.x; s[v][1] = b.y; s[v][2] = b.z; s[v][3] = b.w;
                 m[v] = HAS_MAP ? __ldcs(reinterpret_cast<const unsigned int*>(map + ro + e0)) : 0x01010101u;
             } else {
                 m[v] = 0u;
+                gp[v] = make_uint2(0u, 0u);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const bool in = e0 + q < E;
-                    g[v][q] = in ? __ldcs(grad + ro + e0 + q) : 0.0f;
+                    if (kPacked) {
+                        const uint32_t bits = in ? __ldcs(reinterpret_cast<const unsigned short*>(grad + ro + e0 + q)) : 0u;
+                        if (q < 2) gp[v].x |= bits << (16 * q);
+                        else gp[v].y |= bits << (16 * (q - 2));
+                    } else {
+                        d[v][q] = in ? load_scalar<GradT>(grad + ro + e0 + q) : 0.0f;
+                    }
                     s[v][q] = in ? __ldcs(inter + ro + e0 + q) : 0.0f;
                     const uint32_t mb = in ? (HAS_MAP ? static_cast<uint32_t>(map[ro + e0 + q] != 0) : 1u) : 0u;
                     m[v] |= mb << (8 * q);
                 }
             }
         }
+        // element q of chunk v of the grad row, as fp32
+        auto gval = [&](int v, int q) -> float {
+            if (!kPacked) return d[v][q];
+            const uint32_t w = q < 2 ? gp[v].x : gp[v].y;
+            return bf16_bits_to_f32((q & 1) ? (w >> 16) : (w & 0xffffu));
+        };
         // pass 1: row sums
         float A = 0.0f, B = 0.0f;
         if (HAS_MAP && renorm) {
@@ -53,7 +79,7 @@ __global__ void __launch_bounds__(kBwdThreads) k_router_bwd(const float* __restr
                 for (int q = 0; q < 4; ++q)
                     if ((m[v] >> (8 * q)) & 0xffu) {
                         A += s[v][q];
-                        B += s[v][q] * g[v][q];
+                        B += s[v][q] * gval(v, q);
                     }
             A = warp_sum(A);
             B = warp_sum(B);
@@ -68,12 +94,13 @@ __global__ void __launch_bounds__(kBwdThreads) k_router_bwd(const float* __restr
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const bool mk = (m[v] >> (8 * q)) & 0xffu;
-                const float ds = mk ? (rn ? cA * (g[v][q] - BA) : c * g[v][q]) : 0.0f;
-                g[v][q] = ds;
+                const float gq = gval(v, q);
+                const float ds = mk ? (rn ? cA * (gq - BA) : c * gq) : 0.0f;
+                d[v][q] = ds;
                 if (SCORE == kSoftmax) D += s[v][q] * ds;
             }
         if (SCORE == kSoftmax) D = warp_sum(D);
-        float* out = dx + ro;
+        GradT* out = dx + ro;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             const int e0 = (v * 32 + lane) * 4;
@@ -81,50 +108,66 @@ __global__ void __launch_bounds__(kBwdThreads) k_router_bwd(const float* __restr
             float r[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                r[q] = (SCORE == kSoftmax) ? s[v][q] * (g[v][q] - D) : g[v][q] * s[v][q] * (1.0f - s[v][q]);
+                r[q] = (SCORE == kSoftmax) ? s[v][q] * (d[v][q] - D) : d[v][q] * s[v][q] * (1.0f - s[v][q]);
             if (vec && e0 + 4 <= E) {
-                __stcs(reinterpret_cast<float4*>(out + e0), make_float4(r[0], r[1], r[2], r[3]));
+                store4_stream<GradT>(out + e0, r);
             } else {
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    if (e0 + q < E) out[e0 + q] = r[q];
+                    if (e0 + q < E) store_scalar<GradT>(out + e0 + q, r[q]);
             }
         }
     }
 }
 
 namespace {
-using BwdFn = void (*)(const float*, const float*, const uint8_t*, float*, int, int, int, float, int);
+template <typename GradT>
+using BwdFn = void (*)(const GradT*, const float*, const uint8_t*, GradT*, int, int, int, float, int);
 
-template <int SCORE, bool HAS_MAP>
-BwdFn bwd_kernel(int nv_idx)
+template <int SCORE, bool HAS_MAP, typename GradT>
+BwdFn<GradT> bwd_kernel(int nv_idx)
 {
     switch (kNvBuckets[nv_idx]) {
-        case 1: return k_router_bwd<SCORE, 1, HAS_MAP>;
-        case 2: return k_router_bwd<SCORE, 2, HAS_MAP>;
-        case 3: return k_router_bwd<SCORE, 3, HAS_MAP>;
-        case 4: return k_router_bwd<SCORE, 4, HAS_MAP>;
-        case 6: return k_router_bwd<SCORE, 6, HAS_MAP>;
-        case 8: return k_router_bwd<SCORE, 8, HAS_MAP>;
-        case 12: return k_router_bwd<SCORE, 12, HAS_MAP>;
-        case 18: return k_router_bwd<SCORE, 18, HAS_MAP>;
+        case 1: return k_router_bwd<SCORE, 1, HAS_MAP, GradT>;
+        case 2: return k_router_bwd<SCORE, 2, HAS_MAP, GradT>;
+        case 3: return k_router_bwd<SCORE, 3, HAS_MAP, GradT>;
+        case 4: return k_router_bwd<SCORE, 4, HAS_MAP, GradT>;
+        case 6: return k_router_bwd<SCORE, 6, HAS_MAP, GradT>;
+        case 8: return k_router_bwd<SCORE, 8, HAS_MAP, GradT>;
+        case 12: return k_router_bwd<SCORE, 12, HAS_MAP, GradT>;
+        case 18: return k_router_bwd<SCORE, 18, HAS_MAP, GradT>;
     }
     return nullptr;
 }
-}  // namespace
 
-int launch_bwd(int score_fn, int nv_idx, const float* g, const float* s, const uint8_t* m, float* dx, int T,
-               int E, int renorm, float scaling, bool vec, cudaStream_t st)
+template <typename GradT>
+int launch(BwdFn<GradT> f, const GradT* g, const float* s, const uint8_t* m, GradT* dx, int T, int E, int renorm,
+           float scaling, bool vec, cudaStream_t st)
 {
-    BwdFn f;
-    if (score_fn == kSoftmax) f = m ? bwd_kernel<kSoftmax, true>(nv_idx) : bwd_kernel<kSoftmax, false>(nv_idx);
-    else f = m ? bwd_kernel<kSigmoid, true>(nv_idx) : bwd_kernel<kSigmoid, false>(nv_idx);
     if (!f) return cudaErrorInvalidValue;
     const long long ctas_needed = (static_cast<long long>(T) + kBwdThreads / 32 - 1) / (kBwdThreads / 32);
     const int grid = persistent_grid(reinterpret_cast<const void*>(f), kBwdThreads, 0, ctas_needed);
     if (grid <= 0) return cudaErrorInvalidConfiguration;
     f<<<grid, kBwdThreads, 0, st>>>(g, s, m, dx, T, E, renorm, scaling, vec ? 1 : 0);
     return cudaGetLastError();
+}
+}  // namespace
+
+int launch_bwd(int score_fn, int nv_idx, const float* g, const float* s, const uint8_t* m, float* dx, int T,
+               int E, int renorm, float scaling, bool vec, cudaStream_t st)
+{
+    BwdFn<float> f;
+    if (score_fn == kSoftmax) f = m ? bwd_kernel<kSoftmax, true, float>(nv_idx) : bwd_kernel<kSoftmax, false, float>(nv_idx);
+    else f = m ? bwd_kernel<kSigmoid, true, float>(nv_idx) : bwd_kernel<kSigmoid, false, float>(nv_idx);
+    return launch<float>(f, g, s, m, dx, T, E, renorm, scaling, vec, st);
+}
+
+int launch_bwd_bf16(int score_fn, int nv_idx, const __nv_bfloat16* g, const float* s, const uint8_t* m,
+                    __nv_bfloat16* dx, int T, int E, int renorm, float scaling, bool vec, cudaStream_t st)
+{
+    const BwdFn<__nv_bfloat16> f = score_fn == kSoftmax ? bwd_kernel<kSoftmax, true, __nv_bfloat16>(nv_idx)
+                                                         : bwd_kernel<kSigmoid, true, __nv_bfloat16>(nv_idx);
+    return launch<__nv_bfloat16>(f, g, s, m, dx, T, E, renorm, scaling, vec, st);
 }
 
 }  // namespace mr

@@ -100,6 +100,8 @@ int launch_fused_decode(int score_fn, int in_dtype, const RouteArgs& a, const So
                         int nv_idx, bool select, cudaStream_t st);
 int launch_bwd(int score_fn, int nv_idx, const float* g, const float* s, const uint8_t* m,
                float* dx, int T, int E, int renorm, float scaling, bool vec, cudaStream_t st);
+int launch_bwd_bf16(int score_fn, int nv_idx, const __nv_bfloat16* g, const float* s, const uint8_t* m,
+                    __nv_bfloat16* dx, int T, int E, int renorm, float scaling, bool vec, cudaStream_t st);
 int launch_sort(const int32_t* idx, const float* w, int N, int E_tot, int block_m, int32_t* ids,
                 float* sw, int32_t* eids, int32_t* npp, uint32_t* ws, int32_t* status,
                 cudaStream_t st);
