@@ -308,29 +308,57 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
 
     // 3. selection
     if (!SELECT) {
-        // k_r rounds of arg-max; a winner's key becomes 1 (below every real key,
-        // above the 0 of padding / dropped groups), which also marks it chosen.
-        for (int j = 0; j < k_r; ++j) {
-            uint32_t best = 0u, bidx = 0xffffffffu;
+        // k_r rounds of arg-max over the lanes' best keys. Each lane keeps its two
+        // best (key, index) pairs in selection order (larger key, then lower
+        // index; the lane's elements are scanned in index order with strict
+        // compares); a round takes the warp's best and only the winning lane
+        // moves on. A lane gives its elements away in selection order, so what it
+        // has left is exactly what comes after its last winner (lk, li); it
+        // rescans for its next two only when both have been taken.
+        uint32_t b1 = 0u, i1 = 0xffffffffu, b2 = 0u, i2 = 0xffffffffu;
+        uint32_t lk = 0xffffffffu, li = 0xffffffffu;  // nothing taken yet: every key is after it
+        auto rescan = [&]() {
+            b1 = 0u; i1 = 0xffffffffu; b2 = 0u; i2 = 0xffffffffu;
 #pragma unroll
             for (int v = 0; v < NV; ++v)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const bool gt = key[v][c] > best;
-                    best = gt ? key[v][c] : best;
-                    bidx = gt ? static_cast<uint32_t>(v * 128 + lane4 + c) : bidx;
+                    const uint32_t k = key[v][c];
+                    const uint32_t idx = static_cast<uint32_t>(v * 128 + lane4 + c);
+                    const bool after = k < lk || (k == lk && idx > li);
+                    const bool gt1 = after && k > b1;
+                    const bool gt2 = after && !gt1 && k > b2;
+                    b2 = gt1 ? b1 : (gt2 ? k : b2);
+                    i2 = gt1 ? i1 : (gt2 ? idx : i2);
+                    b1 = gt1 ? k : b1;
+                    i1 = gt1 ? idx : i1;
                 }
-            const uint32_t wmax = __reduce_max_sync(kFull, best);
-            const uint32_t widx = __reduce_min_sync(kFull, best == wmax ? bidx : 0xffffffffu);
+        };
+        rescan();
+        bool has2 = true;  // (b2, i2) is the lane's next after (b1, i1)
+        for (int j = 0; j < k_r; ++j) {
+            const uint32_t wmax = __reduce_max_sync(kFull, b1);
+            const uint32_t widx = __reduce_min_sync(kFull, b1 == wmax ? i1 : 0xffffffffu);
             if (lane == 0) {
                 win_idx[j] = widx;
                 win_val[j] = __fmul_rn(vbuf[min(widx, static_cast<uint32_t>(E - 1))], vmul);
             }
-#pragma unroll
-            for (int v = 0; v < NV; ++v)
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    key[v][c] = (static_cast<uint32_t>(v * 128 + lane4 + c) == widx) ? 1u : key[v][c];
+            bool more = false;
+            if (i1 == widx && b1 == wmax) {  // this lane supplied the winner
+                lk = b1;
+                li = i1;
+                if (has2) {
+                    b1 = b2;
+                    i1 = i2;
+                    has2 = false;
+                } else {
+                    more = true;
+                }
+            }
+            if (j + 1 < k_r && __any_sync(kFull, more) && more) {
+                rescan();
+                has2 = true;
+            }
         }
     } else {
         unsigned long long* cand = reinterpret_cast<unsigned long long*>(wsm + L.cand);
