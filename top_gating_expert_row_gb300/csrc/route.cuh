@@ -466,7 +466,7 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
             n = min(base, lim);
         }
         n = min(n, cap);
-        const uint32_t warm_rank = min(n - 1u, static_cast<uint32_t>(k_r + k_r / 2));
+        const uint32_t warm_rank = min(n - 1u, static_cast<uint32_t>(k_r + k_r / 4));
         if (lane == 0) scal[3] = lo;
         __syncwarp();
         // exact rank of each candidate in selection order
