@@ -13,6 +13,12 @@
 
 namespace mr {
 
+// 4 warps, one token row per warp at a time. Rows live in registers, so
+// registers bound the warps per SM; small CTAs let the occupancy reach that
+// bound (bf16 grads at 166 registers: 3 CTAs = 12 warps, where one 8-warp CTA
+// would leave the rest of the register file idle).
+constexpr int kBwdThreads = 128;
+
 // GradT: the dtype of grad and dx (fp32, or bf16 for bf16 logits: the
 // gradient is computed in fp32 and rounded once when stored).
 template <int SCORE, int NV, bool HAS_MAP, typename GradT>
@@ -36,7 +42,7 @@ __global__ void __launch_bounds__(kBwdThreads) k_router_bwd(const GradT* __restr
         for (int v = 0; v < NV; ++v) {
             const int e0 = (v * 32 + lane) * 4;
             if (vec && e0 + 4 <= E) {
-                if (kPacked) {
+                if constexpr (kPacked) {
                     gp[v] = __ldcs(reinterpret_cast<const uint2*>(grad + ro + e0));
                 } else {
                     const float4 a = __ldcs(reinterpret_cast<const float4*>(grad + ro + e0));
@@ -47,11 +53,11 @@ __global__ void __launch_bounds__(kBwdThreads) k_router_bwd(const GradT* __restr
                 m[v] = HAS_MAP ? __ldcs(reinterpret_cast<const unsigned int*>(map + ro + e0)) : 0x01010101u;
             } else {
                 m[v] = 0u;
-                gp[v] = make_uint2(0u, 0u);
+                if constexpr (kPacked) gp[v] = make_uint2(0u, 0u);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const bool in = e0 + q < E;
-                    if (kPacked) {
+                    if constexpr (kPacked) {
                         const uint32_t bits = in ? __ldcs(reinterpret_cast<const unsigned short*>(grad + ro + e0 + q)) : 0u;
                         if (q < 2) gp[v].x |= bits << (16 * q);
                         else gp[v].y |= bits << (16 * (q - 2));
@@ -66,9 +72,12 @@ __global__ void __launch_bounds__(kBwdThreads) k_router_bwd(const GradT* __restr
         }
         // element q of chunk v of the grad row, as fp32
         auto gval = [&](int v, int q) -> float {
-            if (!kPacked) return d[v][q];
-            const uint32_t w = q < 2 ? gp[v].x : gp[v].y;
-            return bf16_bits_to_f32((q & 1) ? (w >> 16) : (w & 0xffffu));
+            if constexpr (!kPacked) {
+                return d[v][q];
+            } else {
+                const uint32_t w = q < 2 ? gp[v].x : gp[v].y;
+                return bf16_bits_to_f32((q & 1) ? (w >> 16) : (w & 0xffffu));
+            }
         };
         // pass 1: row sums
         float A = 0.0f, B = 0.0f;

@@ -14,7 +14,6 @@ constexpr int kFwdThreads = 256;     // 8 warps, one token row per warp at a tim
 constexpr int kFusedThreads = 512;   // 16 warps: one per decode token, then the whole CTA sorts
 constexpr int kSortThreads = 512;
 constexpr int kSortChunk = 4096;     // flat (token, slot) pairs per sort CTA
-constexpr int kBwdThreads = 256;
 
 // Register-resident row widths: NV chunks of 128 elements per row (E <= 2304).
 constexpr int kNvBuckets[] = {1, 2, 3, 4, 6, 8, 12, 18};
