@@ -44,3 +44,24 @@ def test_device_status_is_clear_after_staged_rows(mr):
     torch.cuda.synchronize()
     assert out["scores"].shape == (w.T, w.E)
     assert mr.device_status() == 0
+
+
+@pytest.mark.parametrize("path", [ARGMAX, SELECT], ids=["argmax", "select"])
+@pytest.mark.parametrize("in_dtype", [F32, BF16], ids=["f32", "bf16"])
+def test_staged_softmax_rows_far_from_the_previous_max(mr, orc, path, in_dtype):
+    """Staged softmax rows shifted by offsets from -500 to +1000 in a random
+    order (bf16: coarse values, many ties at the threshold), so the threshold
+    and the row max a warp meets change by large steps from row to row; every
+    row is checked."""
+    T, E, k = 6500, 2304, 36
+    g = torch.Generator().manual_seed(21)
+    x = torch.randn(T, E, generator=g)
+    offs = torch.tensor([0.0, 20.0, 63.0, 66.0, -70.0, 200.0, -500.0, 1000.0])
+    x = x + offs[torch.randint(0, len(offs), (T, 1), generator=g)]
+    if in_dtype == BF16:
+        x = x.to(torch.bfloat16)
+    x = x.contiguous()
+    w = W("far_max", T, E, k, SM, in_dtype)
+    out = gpu_route(mr, w, x.cuda(), None, path)
+    torch.cuda.synchronize()
+    check_fwd(out, oracle_route(orc, w, x, None), w, what="far from the previous max")

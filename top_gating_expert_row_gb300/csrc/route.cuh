@@ -23,6 +23,8 @@
 // Both selection paths produce the identical winner list.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace mr {
@@ -147,6 +149,53 @@ __device__ void group_limit(uint32_t* skeys, int E, int G, int gk, int m, int la
 // ---------------------------------------------------------------------------
 // FULL: E == 128 * NV and a.vec, so every chunk is whole and vector-aligned and
 // the per-element edge tests compile away.
+// Exact rank of the n candidates in selection order. Each candidate is a
+// 64-bit word (key << 32 | ~index), so all are distinct and a larger word
+// comes first; a candidate's rank is the number of larger words, counted
+// over all pairs. W candidates per lane per pass over the list: three when
+// more than 64 remain, so up to 96 take one pass. Ranks below k_r go to
+// win_idx / win_val (score(idx, key) gives the value); the key at rank
+// warm_rank goes to *warm_key.
+template <typename ScoreFn>
+__device__ __forceinline__ void rank_candidates(const unsigned long long* cand, uint32_t n, int k_r,
+                                                uint32_t warm_rank, int lane, uint32_t* win_idx, float* win_val,
+                                                uint32_t* warm_key, ScoreFn score)
+{
+    auto pass = [&](uint32_t b, auto wc) {
+        constexpr int W = decltype(wc)::value;
+        unsigned long long c[W];
+        uint32_t r[W];
+#pragma unroll
+        for (int h = 0; h < W; ++h) {
+            const uint32_t i = b + 32u * h + lane;
+            c[h] = (i < n) ? cand[i] : 0ull;
+            r[h] = 0u;
+        }
+#pragma unroll 8
+        for (uint32_t q = 0; q < n; ++q) {
+            const unsigned long long cq = cand[q];
+#pragma unroll
+            for (int h = 0; h < W; ++h) r[h] += (cq > c[h]);
+        }
+#pragma unroll
+        for (int h = 0; h < W; ++h) {
+            const uint32_t i = b + 32u * h + lane;
+            if (i < n) {
+                const uint32_t idx = ~static_cast<uint32_t>(c[h]);
+                const uint32_t kk = static_cast<uint32_t>(c[h] >> 32);
+                if (r[h] < static_cast<uint32_t>(k_r)) {
+                    win_idx[r[h]] = idx;
+                    win_val[r[h]] = score(idx, kk);
+                }
+                if (r[h] == warm_rank) *warm_key = kk;
+            }
+        }
+    };
+    uint32_t b = 0;
+    for (; b < n && n - b > 64u; b += 96u) pass(b, std::integral_constant<int, 3>{});
+    if (b < n) pass(b, std::integral_constant<int, 2>{});
+}
+
 template <int SCORE, typename InT, int NV, bool SELECT, bool FULL = false>
 __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned char* wsm,
                                            const WarpLayout& L, int lane, uint32_t& warm)
@@ -469,34 +518,9 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
         const uint32_t warm_rank = min(n - 1u, static_cast<uint32_t>(k_r + k_r / 4));
         if (lane == 0) scal[3] = lo;
         __syncwarp();
-        // exact rank of each candidate in selection order
-        for (uint32_t b = 0; b < n; b += 64) {
-            const uint32_t i0 = b + lane, i1 = b + 32 + lane;
-            const unsigned long long c0 = (i0 < n) ? cand[i0] : 0ull;
-            const unsigned long long c1 = (i1 < n) ? cand[i1] : 0ull;
-            uint32_t r0 = 0u, r1 = 0u;
-#pragma unroll 8
-            for (uint32_t q = 0; q < n; ++q) {
-                const unsigned long long cq = cand[q];
-                r0 += (cq > c0);
-                r1 += (cq > c1);
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t i = h ? i1 : i0;
-                const uint32_t r = h ? r1 : r0;
-                const unsigned long long cc = h ? c1 : c0;
-                if (i < n) {
-                    const uint32_t idx = ~static_cast<uint32_t>(cc);
-                    const uint32_t kk = static_cast<uint32_t>(cc >> 32);
-                    if (r < static_cast<uint32_t>(k_r)) {
-                        win_idx[r] = idx;
-                        win_val[r] = __fmul_rn(vbuf[min(idx, static_cast<uint32_t>(E - 1))], vmul);
-                    }
-                    if (r == warm_rank) scal[3] = kk;
-                }
-            }
-        }
+        rank_candidates(cand, n, k_r, warm_rank, lane, win_idx, win_val, scal + 3, [&](uint32_t idx, uint32_t) {
+            return __fmul_rn(vbuf[min(idx, static_cast<uint32_t>(E - 1))], vmul);
+        });
         __syncwarp();
         warm = scal[3];
     }

@@ -35,9 +35,10 @@ struct WideLayout {
     int kbuf, vbuf, win_idx, win_val, cand, scal, bar, bytes;
 };
 
-// Staging of the next row: while a warp finishes row t (weights and dense
-// outputs, which no longer read kbuf) the bulk-copy engine brings row `next`
-// into kbuf, so the next row's load pass reads shared memory.
+// Staging of the next row: while a warp finishes row t (the threshold select's
+// ranking of its candidates, the weights and the dense outputs, none of which
+// read kbuf) the bulk-copy engine brings row `next` into kbuf, so the next
+// row's load pass reads shared memory.
 struct Stage {
     uint64_t* bar;
     const void* next;  // nullptr: no next row for this warp
@@ -394,42 +395,22 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
         n = min(n, cap);
         const uint32_t warm_rank = min(n - 1u, static_cast<uint32_t>(k_r + k_r / 4));
         if (lane == 0) scal[3] = lo;
+        // the ranking reads only cand: kbuf is free from here on, so the next
+        // row's copy starts now and lands while this row is ranked and written.
+        // The proxy fence orders this lane's generic accesses to kbuf before
+        // the copy's writes.
+        if (FULL && st.next) fence_proxy_async_smem();
         __syncwarp();
-        for (uint32_t b = 0; b < n; b += 64) {
-            const uint32_t i0 = b + lane, i1 = b + 32 + lane;
-            const unsigned long long c0 = (i0 < n) ? cand[i0] : 0ull;
-            const unsigned long long c1 = (i1 < n) ? cand[i1] : 0ull;
-            uint32_t r0 = 0u, r1 = 0u;
-#pragma unroll 8
-            for (uint32_t q = 0; q < n; ++q) {
-                const unsigned long long cq = cand[q];
-                r0 += (cq > c0);
-                r1 += (cq > c1);
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t i = h ? i1 : i0;
-                const uint32_t r = h ? r1 : r0;
-                const unsigned long long cc = h ? c1 : c0;
-                if (i < n) {
-                    const uint32_t idx = ~static_cast<uint32_t>(cc);
-                    const uint32_t kk = static_cast<uint32_t>(cc >> 32);
-                    if (r < static_cast<uint32_t>(k_r)) {
-                        win_idx[r] = idx;
-                        win_val[r] = score_of(idx, kk);
-                    }
-                    if (r == warm_rank) scal[3] = kk;
-                }
-            }
-        }
+        if (FULL && st.next && lane == 0) bulk_load_row(wsm + L.kbuf + st.off, st.next, st.bytes, st.bar);
+        rank_candidates(cand, n, k_r, warm_rank, lane, win_idx, win_val, scal + 3, score_of);
         __syncwarp();
         warm = scal[3];
     }
-    // kbuf is free from here on: stage the next row into it. The proxy fence
-    // orders this lane's generic accesses to kbuf before the copy's writes.
-    if (FULL && st.next) fence_proxy_async_smem();
+    // arg-max rounds read kbuf to the end: stage the next row only now (the
+    // threshold select staged it before its ranking)
+    if (!SELECT && FULL && st.next) fence_proxy_async_smem();
     __syncwarp();
-    if (FULL && st.next && lane == 0) bulk_load_row(wsm + L.kbuf + st.off, st.next, st.bytes, st.bar);
+    if (!SELECT && FULL && st.next && lane == 0) bulk_load_row(wsm + L.kbuf + st.off, st.next, st.bytes, st.bar);
 
     // 4. weights
     float wsum = 0.0f;
