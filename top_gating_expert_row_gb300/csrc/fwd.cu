@@ -40,7 +40,9 @@ constexpr int kScore = MR_SCORE_FN;
 // 4*NV registers per lane.
 constexpr int fwd_min_blocks(int nv) { return nv >= 12 ? 2 : (nv >= 6 ? 3 : 4); }
 
-template <int NV, bool SELECT, bool FULL>
+// RANKW: candidates per lane in a pass of the candidate rank (3 only where the
+// candidate cap exceeds 64, see rank_candidates)
+template <int NV, bool SELECT, bool FULL, int RANKW = 2>
 __global__ void __launch_bounds__(kFwdThreads, fwd_min_blocks(NV)) k_router_fwd(RouteArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -55,7 +57,7 @@ __global__ void __launch_bounds__(kFwdThreads, fwd_min_blocks(NV)) k_router_fwd(
         // the warp's next row streams into L2 while this one is computed
         if (a.prefetch && lane == 0 && t + stride < a.T)
             prefetch_l2(static_cast<const InT*>(a.logits) + static_cast<size_t>(t + stride) * a.E, row_bytes);
-        const float scale = route_row<kScore, InT, NV, SELECT, FULL>(a, t, wsm, L, lane, warm);
+        const float scale = route_row<kScore, InT, NV, SELECT, FULL, RANKW>(a, t, wsm, L, lane, warm);
         if (a.topk_idx || a.topk_w) {
             const size_t o = static_cast<size_t>(t) * a.topk;
             emit_compact(a, wsm, L, scale, lane, a.topk_idx ? a.topk_idx + o : nullptr,
@@ -240,16 +242,16 @@ namespace {
 using FwdFn = void (*)(RouteArgs);
 using FusedFn = void (*)(RouteArgs, SortArgs);
 
-template <bool SELECT, bool FULL>
+template <bool SELECT, bool FULL, int RANKW = 2>
 FwdFn fwd_kernel(int nv_idx)
 {
     switch (kNvBuckets[nv_idx]) {
-        case 1: return k_router_fwd<1, SELECT, FULL>;
-        case 2: return k_router_fwd<2, SELECT, FULL>;
-        case 3: return k_router_fwd<3, SELECT, FULL>;
-        case 4: return k_router_fwd<4, SELECT, FULL>;
-        case 6: return k_router_fwd<6, SELECT, FULL>;
-        case 8: return k_router_fwd<8, SELECT, FULL>;
+        case 1: return k_router_fwd<1, SELECT, FULL, RANKW>;
+        case 2: return k_router_fwd<2, SELECT, FULL, RANKW>;
+        case 3: return k_router_fwd<3, SELECT, FULL, RANKW>;
+        case 4: return k_router_fwd<4, SELECT, FULL, RANKW>;
+        case 6: return k_router_fwd<6, SELECT, FULL, RANKW>;
+        case 8: return k_router_fwd<8, SELECT, FULL, RANKW>;
     }
     return nullptr;
 }
@@ -296,7 +298,10 @@ int MR_CAT(launch_fwd, MR_SUFFIX)(const RouteArgs& a, int nv_idx, bool select, c
     }
     // every chunk whole and vector-aligned: the specialisation without edge tests
     const bool full = a.vec && a.E == 128 * kNvBuckets[nv_idx];
-    const FwdFn f = select ? (full ? fwd_kernel<true, true>(nv_idx) : fwd_kernel<true, false>(nv_idx))
+    // more than 64 candidates possible (k_r > 32): rank three per lane per pass
+    const bool rank3 = full && a.stop > 64;
+    const FwdFn f = select ? (rank3 ? fwd_kernel<true, true, 3>(nv_idx)
+                                    : (full ? fwd_kernel<true, true>(nv_idx) : fwd_kernel<true, false>(nv_idx)))
                            : (full ? fwd_kernel<false, true>(nv_idx) : fwd_kernel<false, false>(nv_idx));
     if (!f) return cudaErrorInvalidValue;
     const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, select, a.n_group > 0);

@@ -152,11 +152,13 @@ __device__ void group_limit(uint32_t* skeys, int E, int G, int gk, int m, int la
 // Exact rank of the n candidates in selection order. Each candidate is a
 // 64-bit word (key << 32 | ~index), so all are distinct and a larger word
 // comes first; a candidate's rank is the number of larger words, counted
-// over all pairs. W candidates per lane per pass over the list: three when
-// more than 64 remain, so up to 96 take one pass. Ranks below k_r go to
-// win_idx / win_val (score(idx, key) gives the value); the key at rank
-// warm_rank goes to *warm_key.
-template <typename ScoreFn>
+// over all pairs. Two candidates per lane per pass over the list; with
+// MAXW = 3, three when more than 64 remain, so up to 96 take one pass (worth
+// it only where n can exceed 64: in a fully unrolled kernel the extra code
+// costs more than it saves at smaller n). Ranks below k_r go to win_idx /
+// win_val (score(idx, key) gives the value); the key at rank warm_rank goes
+// to *warm_key.
+template <int MAXW, typename ScoreFn>
 __device__ __forceinline__ void rank_candidates(const unsigned long long* cand, uint32_t n, int k_r,
                                                 uint32_t warm_rank, int lane, uint32_t* win_idx, float* win_val,
                                                 uint32_t* warm_key, ScoreFn score)
@@ -191,12 +193,17 @@ __device__ __forceinline__ void rank_candidates(const unsigned long long* cand, 
             }
         }
     };
-    uint32_t b = 0;
-    for (; b < n && n - b > 64u; b += 96u) pass(b, std::integral_constant<int, 3>{});
-    if (b < n) pass(b, std::integral_constant<int, 2>{});
+    static_assert(MAXW == 2 || MAXW == 3, "two or three candidates per lane");
+    if constexpr (MAXW == 3) {
+        uint32_t b = 0;
+        for (; b < n && n - b > 64u; b += 96u) pass(b, std::integral_constant<int, 3>{});
+        if (b < n) pass(b, std::integral_constant<int, 2>{});
+    } else {
+        for (uint32_t b = 0; b < n; b += 64u) pass(b, std::integral_constant<int, 2>{});
+    }
 }
 
-template <int SCORE, typename InT, int NV, bool SELECT, bool FULL = false>
+template <int SCORE, typename InT, int NV, bool SELECT, bool FULL = false, int RANKW = 2>
 __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned char* wsm,
                                            const WarpLayout& L, int lane, uint32_t& warm)
 {
@@ -518,7 +525,7 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
         const uint32_t warm_rank = min(n - 1u, static_cast<uint32_t>(k_r + k_r / 4));
         if (lane == 0) scal[3] = lo;
         __syncwarp();
-        rank_candidates(cand, n, k_r, warm_rank, lane, win_idx, win_val, scal + 3, [&](uint32_t idx, uint32_t) {
+        rank_candidates<RANKW>(cand, n, k_r, warm_rank, lane, win_idx, win_val, scal + 3, [&](uint32_t idx, uint32_t) {
             return __fmul_rn(vbuf[min(idx, static_cast<uint32_t>(E - 1))], vmul);
         });
         __syncwarp();

@@ -402,7 +402,7 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
         if (FULL && st.next) fence_proxy_async_smem();
         __syncwarp();
         if (FULL && st.next && lane == 0) bulk_load_row(wsm + L.kbuf + st.off, st.next, st.bytes, st.bar);
-        rank_candidates(cand, n, k_r, warm_rank, lane, win_idx, win_val, scal + 3, score_of);
+        rank_candidates<3>(cand, n, k_r, warm_rank, lane, win_idx, win_val, scal + 3, score_of);
         __syncwarp();
         warm = scal[3];
     }
