@@ -70,6 +70,8 @@ def _load():
         lib.orc_aux_loss_fwd.restype = i32
         lib.orc_aux_loss_bwd.argtypes = [i32, i32, i32, f64, i64, P, f64, P]
         lib.orc_aux_loss_bwd.restype = i32
+        lib.orc_near_tie_gaps.argtypes = [i32] * 4 + [P, P, P]
+        lib.orc_near_tie_gaps.restype = i32
         _lib = lib
     return _lib
 
@@ -217,3 +219,16 @@ def aux_loss_bwd(T: int, tokens_per_expert, topk: int, coeff: float, total_num_t
     _check(lib.orc_aux_loss_bwd(T, E, topk, coeff, total_num_tokens, _p(c), grad_loss, _p(g)),
            "orc_aux_loss_bwd")
     return g
+
+
+def near_tie_gaps(logits, k_r: int, score_fn: int = SOFTMAX, bias=None) -> np.ndarray:
+    """Per token, the gap between the k_r-th and (k_r+1)-th largest selection
+    key (computed in double) in fp32 ulps; -1 where k_r >= E. Informational:
+    small gaps mark the tokens whose selection another rounding could flip."""
+    lib = _load()
+    x = _c(logits, np.float32)
+    T, E = x.shape
+    b = None if bias is None else _c(bias, np.float32)
+    gap = np.empty(T, np.float64)
+    _check(lib.orc_near_tie_gaps(T, E, k_r, score_fn, _p(x), _p(b), _p(gap)), "orc_near_tie_gaps")
+    return gap

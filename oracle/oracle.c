@@ -519,3 +519,51 @@ int orc_aux_loss_bwd(int T, int E, int topk, double coeff, int64_t total_num_tok
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Near ties at the selection boundary (informational; not a step of the     */
+/* method). Per token, the selection keys in double (softmax: the logit;     */
+/* sigmoid: 1/(1 + e^-x) plus the bias) sorted descending, and              */
+/*   gap[t] = (key_(k_r) - key_(k_r+1)) / ulp_fp32(key_(k_r+1)),             */
+/* the distance between the last key taken and the first left out, in fp32   */
+/* ulps at the latter's magnitude. A token with a gap of a few ulps is one   */
+/* whose selected set another fp32 rounding of its keys could change: the    */
+/* rows where bit-exact agreement of the selections says the most.           */
+/* k_r >= E: gap = -1 (no key is left out).                                  */
+/* ------------------------------------------------------------------------- */
+static int orc_desc_double(const void* a, const void* b)
+{
+    const double x = *(const double*)a, y = *(const double*)b;
+    return (x < y) - (x > y);
+}
+
+/* spacing of fp32 values around |v| (the subnormal spacing below FLT_MIN) */
+static double orc_ulp_f32(double v)
+{
+    v = fabs(v);
+    if (v < ldexp(1.0, -126)) return ldexp(1.0, -149);
+    int ex;
+    frexp(v, &ex); /* v = f * 2^ex, 0.5 <= f < 1: fp32 spacing 2^(ex - 24) */
+    return ldexp(1.0, ex - 24);
+}
+
+int orc_near_tie_gaps(int T, int E, int k_r, int score_fn, const float* logits, const float* bias, double* gap)
+{
+    if (T < 0 || E < 1 || k_r < 1 || (T > 0 && (!logits || !gap))) return -1;
+    double* key = (double*)malloc(sizeof(double) * (size_t)E);
+    if (!key) return -1;
+    for (int t = 0; t < T; ++t) {
+        const float* x = logits + (size_t)t * E;
+        if (k_r >= E) {
+            gap[t] = -1.0;
+            continue;
+        }
+        for (int e = 0; e < E; ++e)
+            key[e] = score_fn == ORC_SOFTMAX ? (double)x[e]
+                                              : 1.0 / (1.0 + exp(-(double)x[e])) + (bias ? (double)bias[e] : 0.0);
+        qsort(key, (size_t)E, sizeof(double), orc_desc_double);
+        gap[t] = (key[k_r - 1] - key[k_r]) / orc_ulp_f32(key[k_r]);
+    }
+    free(key);
+    return 0;
+}

@@ -30,3 +30,13 @@ def mr():
     import top_gating_expert_row_gb300 as m
 
     return m
+
+
+def pytest_terminal_summary(terminalreporter):
+    parity = sys.modules.get("parity")
+    rows = getattr(parity, "NEAR_TIES", None)
+    if not rows:
+        return
+    terminalreporter.section("near ties at the selection boundary (< 4 fp32 ulp; informational)")
+    for what, n, total in rows:
+        terminalreporter.write_line(f"{what}: {n} of {total} token rows")

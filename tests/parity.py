@@ -67,3 +67,21 @@ def sample_rows(T: int, n: int, seed: int = 5) -> np.ndarray:
     rows = set(rng.choice(T, size=min(n, T), replace=False).tolist())
     rows.update({0, T - 1})
     return np.array(sorted(rows))
+
+
+# (label, rows with a near tie, rows) of every parity case that noted them;
+# conftest prints them at the end of the run
+NEAR_TIES: list = []
+
+
+def note_near_ties(orc, what: str, x, k_r: int, score_fn: int, bias=None, ulps: float = 4.0) -> int:
+    """Records how many of these token rows have the last key taken and the
+    first key left out within `ulps` fp32 ulps (keys in double, by the oracle).
+    Informational: those are the rows where another rounding of the keys could
+    change the selection, so they are where bit-exact agreement says the most."""
+    xf = x.float().numpy() if isinstance(x, torch.Tensor) else np.asarray(x, np.float32)
+    b = None if bias is None else (bias.float().numpy() if isinstance(bias, torch.Tensor) else bias)
+    gaps = orc.near_tie_gaps(xf, k_r, score_fn, b)
+    n = int(((gaps >= 0) & (gaps < ulps)).sum())
+    NEAR_TIES.append((what, n, len(gaps)))
+    return n

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import synth
-from parity import assert_bf16_close, assert_close, assert_equal, sample_rows
+from parity import assert_bf16_close, assert_close, assert_equal, note_near_ties, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -95,6 +95,8 @@ def test_fwd_matches_oracle(mr, orc, w, path):
     out = gpu_route(mr, w, xg, bg, path)
     torch.cuda.synchronize()
     check_fwd(out, oracle_route(orc, w, x, b), w, what=w.name)
+    if w.n_group == 0 and path == ARGMAX:
+        note_near_ties(orc, w.name, x, w.topk - w.n_shared, w.score_fn, b)
 
 
 def _tie_logits(kind, T, E):
@@ -143,6 +145,8 @@ def test_full_size_sampled_rows(mr, orc, w):
     torch.cuda.synchronize()
     rows = sample_rows(w.T, 2048)
     check_fwd(out, oracle_route(orc, w, x, b, rows), w, rows=rows, what=w.name)
+    if w.n_group == 0:
+        note_near_ties(orc, f"{w.name} (sampled rows)", x[rows], w.topk - w.n_shared, w.score_fn, b)
     # properties over every row: topk distinct, routing_map consistent with topk_idx
     idx = out["topk_idx"][:, : w.topk - w.n_shared].long()
     srt = torch.sort(idx, dim=1).values
@@ -170,6 +174,8 @@ def test_rows_of_varying_scale_every_row(mr, orc, E, k, fn, path):
     out = gpu_route(mr, w, x.cuda(), None, path)
     torch.cuda.synchronize()
     check_fwd(out, oracle_route(orc, w, x, None), w, what=f"varying E={E} k={k}")
+    if path == ARGMAX:
+        note_near_ties(orc, f"varying scale E={E} k={k} fn={fn}", x, k, fn)
 
 
 BWD_CASES = [synth.tiny(), W("e512_k22", 300, 512, 22, sigma=2.0), W("e512_k22_sig", 300, 512, 22, SG),

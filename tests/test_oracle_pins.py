@@ -477,3 +477,21 @@ def test_tokens_per_expert_counts_columns(orc):
     x = synth.logits(200, 33).float().numpy()
     rm = orc.aux_scores_fwd(x, 5, SM)["routing_map"]
     assert orc.tokens_per_expert(rm).sum() == 200 * 5
+
+
+# --------------------------------------------------------------------------- near ties (informational)
+def test_near_tie_gaps_in_fp32_ulps(orc):
+    """The gap between the last key taken and the first left out, in fp32 ulps
+    at the latter: an exact tie is 0; 1.0 against the next fp32 value below it
+    (1 - 2^-24) is one ulp; k_r >= E leaves nothing out (-1); sigmoid keys
+    0.5 + 2^-20 and 0.5 differ by 2^-20 = 16 ulps of 0.5 (2^-24 each)."""
+    f = np.float32
+    assert orc.near_tie_gaps(np.array([[3, 1, 1, 0.5]], f), 2)[0] == 0.0
+    assert orc.near_tie_gaps(np.array([[1.0, f(1) - f(2 ** -24), -5]], f), 1)[0] == 1.0
+    assert orc.near_tie_gaps(np.array([[1.0, 2.0]], f), 2)[0] == -1.0
+    g = orc.near_tie_gaps(np.zeros((1, 2), f), 1, SG, np.array([0, 2 ** -20], f))
+    assert g[0] == 16.0
+    # order-free: a permutation of a row's logits leaves its gap unchanged
+    x = np.random.default_rng(5).standard_normal((4, 64)).astype(f)
+    perm = np.random.default_rng(6).permutation(64)
+    assert np.array_equal(orc.near_tie_gaps(x, 9), orc.near_tie_gaps(x[:, perm], 9))
