@@ -16,7 +16,7 @@ workloads, fused decode route+sort in us/call (eager and CUDA-graph replayed,
 against the launch floor), the prefill route+sort, the end-to-end rate through
 host buffers, the roofline of the dominant kernel and the CPU oracle baseline.
 
---impl reference times the CPU oracle (the reference for this build) on a
+--impl reference times the CPU oracle (the reference implementation here) on a
 bounded sample of the same workload and prints the same line shape.
 
 Multi-GPU: one process per GPU (torchrun); every rank routes its own T=8192
@@ -269,7 +269,7 @@ def time_kernels(mr, w, dev, stream, calls=20, replays=5) -> dict:
 
 
 def bf16_rates(mr, dev, stream, calls=20, replays=5) -> dict:
-    """SURVEY-f4 shape: T=8192 E=2304 topk=36 softmax with bf16 logits; the forward
+    """The headline shape with bf16 logits: T=8192 E=2304 topk=36 softmax; the forward
     writes bf16 probs, the backward takes and returns bf16 gradients (the
     intermediate stays fp32): 9 bytes per element each. Graph replays rotating
     over buffer sets larger than 3x L2."""
