@@ -607,6 +607,21 @@ STEP_WORKLOADS = {
 }
 
 
+def aggregate_over_ranks(elapsed_ms: float, bytes_per_step: int, steps: int, ws: int, device) -> tuple:
+    """Whole-job figures of a timed region that every rank ran on its own batch:
+    the elapsed time is the maximum over ranks (all_reduce MAX on the process
+    group, which must be initialised when ws > 1), and the rate counts the
+    bytes of all ranks. Returns (elapsed_ms, ms_per_step, GB/s)."""
+    if ws > 1:
+        import torch.distributed as dist
+
+        tt = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    value = bytes_per_step * steps * ws / (elapsed_ms * 1e-3) / 1e9
+    return elapsed_ms, elapsed_ms / steps, value
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -730,14 +745,8 @@ def main():
         dist.barrier()
     t_wall1 = time.time()
     clocks = sampler.stop(t_wall0, t_wall1)
-    elapsed_ms = start.elapsed_time(end)
-    if ws > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
-    ms_per_step = elapsed_ms / args.steps
-    total_bytes = sum(nbytes.values()) * args.steps * ws
-    value = total_bytes / (elapsed_ms * 1e-3) / 1e9
+    elapsed_ms, ms_per_step, value = aggregate_over_ranks(start.elapsed_time(end), sum(nbytes.values()), args.steps,
+                                                          ws, dev)
 
     pk = peaks()
     per_kernel = {}
