@@ -2,6 +2,7 @@
 // enqueued), path and grid selection, and the launches. Host checks follow
 // TransformerEngine PR 3012 "Hardening" (T*E <= INT_MAX, topk in [1, E],
 // topk % group_topk == 0) plus this library's own limits.
+#include <atomic>
 #include <climits>
 #include <cstdlib>
 #include <cstring>
@@ -180,24 +181,31 @@ uint32_t* device_status_address()
 // ---- top-k path configuration -----------------------------------------------------------------
 
 namespace {
+// Read by every launch and set by moe_router_set_topk_path, possibly from
+// other host threads: atomics (relaxed: each value stands alone).
 struct PathConfig {
-    int threshold = 8;
-    int force = 0;  // 0 by threshold, 1 arg-max, 2 threshold-select
+    std::atomic<int> threshold{8};
+    std::atomic<int> force{0};  // 0 by threshold, 1 arg-max, 2 threshold-select
     PathConfig()
     {
         if (const char* t = std::getenv("MR_TOPK_SELECT_THRESHOLD")) {
             const int v = std::atoi(t);
-            if (v >= 0) threshold = v;
+            if (v >= 0) threshold.store(v, std::memory_order_relaxed);
         }
         if (const char* f = std::getenv("MR_FORCE_PATH")) {
-            if (!std::strcmp(f, "argmax")) force = 1;
-            else if (!std::strcmp(f, "select")) force = 2;
+            if (!std::strcmp(f, "argmax")) force.store(1, std::memory_order_relaxed);
+            else if (!std::strcmp(f, "select")) force.store(2, std::memory_order_relaxed);
         }
     }
+    int forced() const { return force.load(std::memory_order_relaxed); }
 };
 PathConfig g_path;
 
-bool use_select(int k_r) { return g_path.force == 2 || (g_path.force == 0 && k_r >= g_path.threshold); }
+bool use_select(int k_r)
+{
+    const int f = g_path.forced();
+    return f == 2 || (f == 0 && k_r >= g_path.threshold.load(std::memory_order_relaxed));
+}
 
 int select_stop(int k_r)
 {
@@ -331,8 +339,8 @@ const char* moe_router_strerror(int code)
 int moe_router_set_topk_path(int select_threshold, int force_path)
 {
     if (select_threshold < 0 || force_path < 0 || force_path > 2) return MR_EINVAL;
-    g_path.threshold = select_threshold;
-    g_path.force = force_path;
+    g_path.threshold.store(select_threshold, std::memory_order_relaxed);
+    g_path.force.store(force_path, std::memory_order_relaxed);
     return MR_OK;
 }
 
@@ -556,7 +564,8 @@ int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int
                    log2_if_pow2(block_m)};
         // a one-CTA decode launch is bound by instruction fetch on a cold SM: the
         // arg-max path has the shorter code, so it is the default up to k_r = 32
-        const bool sel = g_path.force == 2 || (g_path.force == 0 && k_r > 32);
+        const int f = g_path.forced();
+        const bool sel = f == 2 || (f == 0 && k_r > 32);
         const int nw = (p->T > 16 ? kFusedWideThreads : kFusedThreads) / 32;
         const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, sel, a.n_group > 0);
         const size_t smem = static_cast<size_t>(L.bytes) * nw +
