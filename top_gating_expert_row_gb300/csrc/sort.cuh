@@ -64,10 +64,12 @@ __device__ inline uint32_t cta_exclusive_scan(uint32_t* a, int n, uint32_t* tmp)
     return total;
 }
 
-// Stable scatter of flat ids [f0, f1), f1 - f0 <= kSortChunk, by a CTA of
-// kSortThreads threads. base[e] is the absolute position of the first pair of
-// expert e handled by this CTA. wh: nwarps*E_tot 16-bit counters (shared).
-// Pairs with ids outside [0, E_tot) are skipped.
+// Stable scatter of flat ids [f0, f1), f1 - f0 <= kSortChunk, by a CTA of at
+// least kSortThreads threads (the sort's CTAs have 512, the fused decode's 512
+// or 1024): then no warp owns more than kMaxSteps steps of 32 ids, the number
+// each warp keeps in registers. base[e] is the absolute position of the first
+// pair of expert e handled by this CTA. wh: nwarps*E_tot 16-bit counters
+// (shared). Pairs with ids outside [0, E_tot) are skipped.
 __device__ inline void cta_scatter(const int32_t* idx, const float* w, int f0, int f1, int E_tot,
                             const uint32_t* base, uint16_t* wh, int32_t* out_ids, float* out_w)
 {
@@ -79,7 +81,8 @@ __device__ inline void cta_scatter(const int32_t* idx, const float* w, int f0, i
     uint16_t* mine = wh + warp * E_tot;
     for (int i = tid; i < nw * E_tot; i += blockDim.x) wh[i] = 0;
     // the warp's ids, loaded once (all steps in flight) and kept for both passes;
-    // a warp owns at most kSortChunk / (32 * warps) steps of 32 ids
+    // a warp owns ceil(n / warps) ids rounded up to 32, at most kMaxSteps steps
+    // of 32 for n <= kSortChunk and at least kSortThreads / 32 warps
     constexpr int kMaxSteps = (kSortChunk + kSortThreads - 1) / kSortThreads;
     int ev[kMaxSteps];
     float wv[kMaxSteps];  // and their weights
