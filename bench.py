@@ -222,7 +222,7 @@ def make_step(mr, w, dev, stream):
 
     launches = [
         ("fwd", lambda: chk(L.moe_router_fwd(P, ptr["x"], ptr["probs"], ptr["map"], ptr["inter"], ptr["idx"],
-                                             ptr["w"], s), "fwd")),
+                                             ptr["w"], None, s), "fwd")),
         ("bwd", lambda: chk(L.moe_router_bwd(P, ptr["g"], ptr["inter"], ptr["map"], ptr["dx"], s), "bwd")),
         ("aux_fwd", lambda: chk(L.moe_aux_scores_fwd(T, E, k, w.score_fn, w.in_dtype, ptr["x"], ptr["scores"],
                                                      ptr["amap"], s), "aux_fwd")),
@@ -371,10 +371,10 @@ def decode_latency(mr, dev, stream, n_calls=200, Ts=synth.DECODE_TS, shape=synth
         xp, ip, wp, wsp, wsn = x.data_ptr(), idx.data_ptr(), wt.data_ptr(), ws.data_ptr(), ws.numel()
 
         def fused(st):
-            return L.moe_router_fused_fwd_sort(P, xp, w.block_m, ip, wp, a[0], a[1], a[2], a[3], None, 0, st)
+            return L.moe_router_fused_fwd_sort(P, xp, w.block_m, ip, wp, a[0], a[1], a[2], a[3], None, 0, None, st)
 
         def unfused(st):
-            L.moe_router_fwd(P, xp, None, None, None, ip, wp, st)
+            L.moe_router_fwd(P, xp, None, None, None, ip, wp, None, st)
             return L.moe_sort(ip, wp, T, w.topk, w.E, w.block_m, a[0], a[1], a[2], a[3], wsp, wsn, None, st)
 
         fe, fg = eager(fused), graph(fused)
@@ -423,7 +423,7 @@ def prefill_route_sort(mr, dev, stream, reps=20) -> dict:
     ws = torch.empty(mr.moe_sort_workspace_bytes(w.T, w.topk, w.E_tot, w.block_m), dtype=torch.uint8, device=dev)
     a = [bufs[n].data_ptr() for n in ("sorted_token_ids", "sorted_weights", "expert_ids", "num_tokens_post_pad")]
     s = stream.cuda_stream
-    route = lambda: L.moe_router_fwd(P, x.data_ptr(), None, None, None, idx.data_ptr(), wt.data_ptr(), s)  # noqa
+    route = lambda: L.moe_router_fwd(P, x.data_ptr(), None, None, None, idx.data_ptr(), wt.data_ptr(), None, s)  # noqa
     srt = lambda: L.moe_sort(idx.data_ptr(), wt.data_ptr(), w.T, w.topk, w.E_tot, w.block_m, a[0], a[1], a[2],  # noqa
                              a[3], ws.data_ptr(), ws.numel(), None, s)
     with torch.cuda.stream(stream):

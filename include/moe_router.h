@@ -48,10 +48,20 @@ typedef enum {
     MR_EINVAL = 1,       /* bad argument: null required pointer, size or option out of range */
     MR_EUNSUPPORTED = 2, /* valid on the pages but outside this library's limits (below) */
     MR_ECUDA = 3,        /* a CUDA launch or query failed */
-    MR_ERANGE = 4,       /* (device status word only) an expert id outside [0, E_tot) was dropped */
-    MR_ETIMEOUT = 8      /* (device status word only) a bounded in-kernel wait gave up; the
+    MR_ERANGE = 4,       /* (device status only) an expert id outside [0, E_tot) was dropped */
+    MR_ETIMEOUT = 5      /* (device status only) a bounded in-kernel wait gave up; the
                             outputs of the call that reported it are not valid */
 } mr_status;
+
+/*
+ * Device status words. A kernel reports a condition by raising a device int32
+ * status word to the condition's code with an atomic maximum, so a word holds
+ * the most severe code reported since it was last zeroed (MR_ETIMEOUT >
+ * MR_ERANGE > MR_OK). Calls that take a nullable `int32_t* status` report into
+ * that word (the caller zeroes it before the call); a call given NULL, and
+ * moe_aux_scores_fwd, report timeouts into the library's per-device word
+ * instead (moe_router_device_status reads and clears it), so none is lost.
+ */
 
 typedef enum { MR_SOFTMAX = 0, MR_SIGMOID = 1 } mr_score_fn;
 typedef enum { MR_F32 = 0, MR_BF16 = 1 } mr_dtype;
@@ -108,12 +118,16 @@ typedef struct {
  *   intermediate[T x E] (fp32)      s, the input of moe_router_bwd
  *   topk_idx[T x topk]  (int32)     winners by descending key (ties: ascending index), then shared ids
  *   topk_w[T x topk]    (fp32)      their weights, then shared_weight
+ * status: nullable device int32 (see "Device status words"). Rows wider than 1024
+ * experts are staged in shared memory by bulk copies whose waits are bounded; a wait
+ * that gives up raises *status to MR_ETIMEOUT (the library's per-device word when
+ * status is NULL) and the call's outputs are not valid.
  * Errors: MR_EINVAL (null logits, no output, sizes out of range, T*E > INT_MAX,
  * n_group/topk_group inconsistent), MR_EUNSUPPORTED (limits above), MR_ECUDA.
  */
 int moe_router_fwd(const mr_router_params* p, const void* logits, void* probs,
                    uint8_t* routing_map, float* intermediate, int32_t* topk_idx, float* topk_w,
-                   mr_stream_t stream);
+                   int32_t* status, mr_stream_t stream);
 
 /*
  * moe_router_bwd -- gradient of probs w.r.t. logits ([TE] top-k backward, "Two-pass
@@ -204,8 +218,8 @@ int moe_aux_loss_bwd(int T, int E, int topk, float coeff, long long total_num_to
  *   are written.
  * workspace: device scratch of at least moe_sort_workspace_bytes(), contents
  *   ignored on entry (any state), owned by the caller; the call only writes into it.
- * status: nullable device int32; an id outside [0, E_tot) is dropped and MR_ERANGE is
- *   OR-ed into *status (the caller zeroes it first).
+ * status: nullable device int32; an id outside [0, E_tot) is dropped and *status is
+ *   raised to MR_ERANGE (see "Device status words"; the caller zeroes it first).
  * Limits: T*topk < INT_MAX, E_tot <= MR_MAX_SORT_EXPERTS, block_m >= 1.
  */
 size_t moe_sort_capacity(int T, int topk, int E_tot, int block_m);
@@ -237,6 +251,10 @@ int moe_sort(const int32_t* topk_idx, const float* topk_w, int T, int topk, int 
  * and give wrong results: order them, or use moe_sort with separate workspaces.
  */
 #define MR_SORT_NOALLOC_SCRATCH_BYTES (1u << 20)
+/* The size of that array in bytes, as this build of the library has it (the value of
+ * MR_SORT_NOALLOC_SCRATCH_BYTES it was compiled with), for callers that load the
+ * library at run time. */
+size_t moe_sort_noalloc_scratch_bytes(void);
 int moe_sort_noalloc(const int32_t* topk_idx, const float* topk_w, int T, int topk, int E_tot,
                      int block_m, int32_t* sorted_token_ids, float* sorted_weights,
                      int32_t* expert_ids, int32_t* num_tokens_post_pad, int32_t* status,
@@ -253,13 +271,15 @@ int moe_sort_noalloc(const int32_t* topk_idx, const float* topk_w, int T, int to
  * workspace (moe_router_fused_workspace_bytes, 0 for the one-launch sizes) holds
  * the compact outputs when those are NULL and the sort's scratch (0 bytes for the
  * one-launch case).
+ * status: nullable device int32, as for moe_router_fwd (MR_ETIMEOUT from the staged
+ * wide-row forward when the call runs as separate launches).
  */
 size_t moe_router_fused_workspace_bytes(const mr_router_params* p, int block_m);
 int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int block_m,
                               int32_t* topk_idx, float* topk_w, int32_t* sorted_token_ids,
                               float* sorted_weights, int32_t* expert_ids,
                               int32_t* num_tokens_post_pad, void* workspace, size_t ws_bytes,
-                              mr_stream_t stream);
+                              int32_t* status, mr_stream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char* moe_router_strerror(int code);
@@ -276,14 +296,27 @@ int moe_router_set_topk_path(int select_threshold, int force_path);
 
 /*
  * The library's per-device status word. Kernels that wait on an asynchronous copy
- * (the forward on rows staged in shared memory) bound every wait; if one gives up,
- * the kernel OR-s MR_ETIMEOUT into this word and stops. This call enqueues, on
- * `stream`, a copy of the current device's word into *out (a device int32) and, if
- * clear != 0, resets the word to 0 after copying it. Asynchronous like every other
- * call: *out is valid once the stream reaches this point.
+ * (the forward on rows staged in shared memory) bound every wait; if one gives up
+ * and the call had no status argument (or was moe_aux_scores_fwd), the kernel
+ * raises this word to MR_ETIMEOUT and stops. This call enqueues, on `stream`, a copy
+ * of the current device's word into *out (a device int32) and, if clear != 0, resets
+ * the word to 0 after copying it. Asynchronous like every other call: *out is valid
+ * once the stream reaches this point.
  * Returns MR_EINVAL for a NULL out, MR_ECUDA on a failed launch.
  */
 int moe_router_device_status(int32_t* out, int clear, mr_stream_t stream);
+
+/*
+ * Test hook for the bounded waits ([TE] "Hardening": device-side guards report
+ * instead of trapping). tries: attempts of about a microsecond each before a wait of
+ * the staged wide-row forward gives up (0 restores the default of 2^20, about a
+ * second). drop_copies != 0: the kernel arms each row's barrier for the bytes of
+ * the row but issues no copy, so every wait runs out while no copy is in flight;
+ * the kernel then reports MR_ETIMEOUT and returns, and the outputs are not valid.
+ * Process-wide, read by every later launch; not thread-safe against concurrent
+ * calls. Returns MR_EINVAL for drop_copies outside {0, 1}.
+ */
+int moe_router_set_wait_test(unsigned int tries, int drop_copies);
 
 /* Diagnostics (not part of the routing path):
  * moe_router_expf evaluates the library's device fp32 exponential on n values

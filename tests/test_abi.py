@@ -52,8 +52,9 @@ def test_binding_wraps_every_symbol(lib):
 
 
 def test_strerror(lib):
-    for code in (0, 1, 2, 3, 4, 8):
+    for code in (0, 1, 2, 3, 4, 5):
         assert lib.strerror(code).startswith("MR_")
+    assert (lib.MR_ERANGE, lib.MR_ETIMEOUT) == (4, 5)
     assert "unknown" in lib.strerror(99)
 
 
@@ -72,7 +73,7 @@ FAKE = 0x10000  # never dereferenced: every call below fails validation first
 
 def _fwd(lib, p, logits=FAKE, probs=FAKE):
     cp = p.c()
-    return lib._lib.moe_router_fwd(ctypes.byref(cp), logits, probs, None, None, None, None, None)
+    return lib._lib.moe_router_fwd(ctypes.byref(cp), logits, probs, None, None, None, None, None, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -97,10 +98,10 @@ def test_fwd_rejects_bias_with_softmax_and_missing_pointers(lib):
     p = _p(lib)
     cp = p.c()
     cp.bias = FAKE
-    assert lib._lib.moe_router_fwd(ctypes.byref(cp), FAKE, FAKE, None, None, None, None, None) == 2
+    assert lib._lib.moe_router_fwd(ctypes.byref(cp), FAKE, FAKE, None, None, None, None, None, None) == 2
     assert _fwd(lib, _p(lib), logits=None) == 1
     assert _fwd(lib, _p(lib), probs=None) == 1  # no output at all
-    assert lib._lib.moe_router_fwd(None, FAKE, FAKE, None, None, None, None, None) == 1
+    assert lib._lib.moe_router_fwd(None, FAKE, FAKE, None, None, None, None, None, None) == 1
 
 
 def test_zero_tokens_is_a_no_op(lib):
@@ -149,16 +150,29 @@ def test_sort_sizes_and_rejects(lib):
 def test_fused_rejects(lib):
     cp = _p(lib, T=65).c()
     f = lib._lib.moe_router_fused_fwd_sort
-    assert f(ctypes.byref(cp), FAKE, 0, None, None, FAKE, FAKE, FAKE, FAKE, None, 0, None) == 1
-    assert f(ctypes.byref(cp), FAKE, 8, None, None, None, FAKE, FAKE, FAKE, None, 0, None) == 1
+    assert f(ctypes.byref(cp), FAKE, 0, None, None, FAKE, FAKE, FAKE, FAKE, None, 0, None, None) == 1
+    assert f(ctypes.byref(cp), FAKE, 8, None, None, None, FAKE, FAKE, FAKE, None, 0, None, None) == 1
     # above the one-launch sizes a workspace is needed
     assert lib.moe_router_fused_workspace_bytes(_p(lib, T=65), 8) > 0
-    assert f(ctypes.byref(cp), FAKE, 8, None, None, FAKE, FAKE, FAKE, FAKE, None, 0, None) == 1
+    assert f(ctypes.byref(cp), FAKE, 8, None, None, FAKE, FAKE, FAKE, FAKE, None, 0, None, None) == 1
     assert lib.moe_router_fused_workspace_bytes(_p(lib, T=17, E=512), 8) > 0
     # one launch: T <= 16 for E <= 1024, T <= 64 for E <= 256
     assert lib.moe_router_fused_workspace_bytes(_p(lib, T=16, E=1024, topk=8), 8) == 0
     assert lib.moe_router_fused_workspace_bytes(_p(lib, T=64, E=256, topk=8), 8) == 0
     assert lib.moe_router_fused_workspace_bytes(_p(lib, T=64), 8) == 0
+
+
+def test_noalloc_scratch_size_matches_the_header(lib):
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+MR_SORT_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "MR_SORT_NOALLOC_SCRATCH_BYTES not found in the header"
+    assert lib.moe_sort_noalloc_scratch_bytes() == int(m.group(1)) << int(m.group(2))
+
+
+def test_set_wait_test(lib):
+    assert lib._lib.moe_router_set_wait_test(4, 2) == lib.MR_EINVAL
+    assert lib._lib.moe_router_set_wait_test(4, -1) == lib.MR_EINVAL
+    assert lib._lib.moe_router_set_wait_test(0, 0) == lib.MR_OK
 
 
 def test_set_topk_path(lib):

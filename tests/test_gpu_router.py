@@ -54,12 +54,12 @@ def gpu_inputs(w, logits=None):
     return x, b, x.cuda(), (b.cuda() if b is not None else None)
 
 
-def gpu_route(mr, w, xg, bg, path, dense=True, compact=True):
+def gpu_route(mr, w, xg, bg, path, dense=True, compact=True, status=None):
     mr.moe_router_set_topk_path(8, path)
     try:
         return mr.route(xg, w.topk, dense=dense, compact=compact, score_fn=w.score_fn, renorm=w.renorm,
                         n_group=w.n_group, topk_group=w.topk_group, n_shared=w.n_shared,
-                        scaling=w.scaling, shared_weight=w.shared_weight, bias=bg)
+                        scaling=w.scaling, shared_weight=w.shared_weight, bias=bg, status=status)
     finally:
         mr.moe_router_set_topk_path(8, 0)
 

@@ -82,7 +82,9 @@ def _oracle_fused(orc, w, x, b):
     return r, s
 
 
-FUSED = [synth.decode(T) for T in synth.DECODE_TS] + [
+# the decode shapes exactly as benchmarked: DeepSeek-R1 (E=256, topk=8) and GPT-OSS
+# (E=128, topk=4), both with block_m=32
+FUSED = [synth.decode(T) for T in synth.DECODE_TS] + [synth.decode_gpt_oss(T) for T in (1, 4, 16, 32, 64)] + [
     synth.Workload("decode_T16_grouped_shared", 16, 384, 9, synth.SIGMOID, synth.BF16, renorm=1, scaling=2.827,
                    n_group=8, topk_group=4, n_shared=1, bias_range=0.05, zipf_s=1.1, block_m=64),
     synth.Workload("decode_T5_e128_k4", 5, 128, 4, synth.SOFTMAX, synth.BF16, renorm=1, block_m=16),

@@ -7,6 +7,13 @@ warp several rows (T larger than the persistent grid's warps), in fp32 and bf16
 (whose raw row sits in the buffer's upper half and is turned into keys in
 place), with and without the intermediate output, and check every row against
 the oracle. Afterwards the library's device status word must still be clear.
+
+The bounded wait itself is exercised without any GPU fault: a host-side test
+hook makes the kernel arm each row's barrier for the row's bytes but issue no
+copy, with a wait limit of a few microseconds, so every wait runs out while no
+copy is in flight. The call must report MR_ETIMEOUT in its status word (or in
+the library's device word when it has none) and return, and the next normal
+call must be correct.
 """
 import pytest
 import torch
@@ -65,3 +72,32 @@ def test_staged_softmax_rows_far_from_the_previous_max(mr, orc, path, in_dtype):
     out = gpu_route(mr, w, x.cuda(), None, path)
     torch.cuda.synchronize()
     check_fwd(out, oracle_route(orc, w, x, None), w, what="far from the previous max")
+
+
+@pytest.mark.parametrize("path", [ARGMAX, SELECT], ids=["argmax", "select"])
+@pytest.mark.parametrize("in_dtype", [F32, BF16], ids=["f32", "bf16"])
+def test_bounded_wait_gives_up_and_reports_it(mr, orc, path, in_dtype):
+    w = W("timeout", 3000, 2304, 36, SM, in_dtype)
+    x, b, xg, bg = gpu_inputs(w)
+    assert mr.device_status(clear=True) == 0
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mr.moe_router_set_wait_test(8, 1)
+    try:
+        gpu_route(mr, w, xg, bg, path, status=status)
+        torch.cuda.synchronize()
+        got_call = int(status.item())
+        # no status word of its own: the timeout goes to the library's device word
+        mr.aux_scores(xg, w.topk, w.score_fn)
+        torch.cuda.synchronize()
+    finally:
+        mr.moe_router_set_wait_test(0, 0)
+    assert got_call == mr.MR_ETIMEOUT
+    assert mr.device_status(clear=True) == mr.MR_ETIMEOUT
+    assert mr.device_status() == 0
+    # the context is still usable and the next normal call is correct
+    status.zero_()
+    out = gpu_route(mr, w, xg, bg, path, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    check_fwd(out, oracle_route(orc, w, x, b), w, what="after a timeout")
+    assert mr.device_status() == 0

@@ -55,16 +55,21 @@ def test_two_calls_in_a_row_match_moe_sort(mr):
 
 
 def test_scratch_limit_is_enforced(mr):
-    # 65 chunks of 4096 pairs x 4096 experts x 4 bytes is just over the 1 MiB array
-    T, k, E_tot, bm = 65 * 4096, 1, 4096, 16
-    assert mr.moe_sort_workspace_bytes(T, k, E_tot, bm) > mr.MR_SORT_NOALLOC_SCRATCH_BYTES
+    # the scratch the sort needs grows with the number of 4096-pair chunks; find the
+    # largest T (in whole chunks) whose scratch fits the array, with 4096 experts
+    k, E_tot, bm = 1, 4096, 16
+    limit = mr.moe_sort_noalloc_scratch_bytes()
+    T2 = 4096
+    while mr.moe_sort_workspace_bytes(T2 + 4096, k, E_tot, bm) <= limit:
+        T2 += 4096
+    T = T2 + 4096  # one chunk more: just over the array
+    assert mr.moe_sort_workspace_bytes(T, k, E_tot, bm) > limit
     dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
     with pytest.raises(mr.MoERouterError) as e:
         mr.moe_sort_noalloc(dummy, None, T, k, E_tot, bm, dummy, None, dummy, dummy)
     assert e.value.code == mr.MR_EUNSUPPORTED
     # the largest table that fits is accepted
-    T2 = 64 * 4096
-    assert mr.moe_sort_workspace_bytes(T2, k, E_tot, bm) == mr.MR_SORT_NOALLOC_SCRATCH_BYTES
+    assert mr.moe_sort_workspace_bytes(T2, k, E_tot, bm) <= limit
     idx = torch.randint(0, E_tot, (T2, k), dtype=torch.int32, device="cuda")
     out, status = _noalloc(mr, idx, None, E_tot, bm)
     ref = mr.sort(idx, None, E_tot, bm)

@@ -22,7 +22,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoerouter.so")
 
-MR_OK, MR_EINVAL, MR_EUNSUPPORTED, MR_ECUDA, MR_ERANGE, MR_ETIMEOUT = 0, 1, 2, 3, 4, 8
+MR_OK, MR_EINVAL, MR_EUNSUPPORTED, MR_ECUDA, MR_ERANGE, MR_ETIMEOUT = 0, 1, 2, 3, 4, 5
 MR_SOFTMAX, MR_SIGMOID = 0, 1
 MR_F32, MR_BF16 = 0, 1
 MR_MAX_FUSED_TOKENS = 16
@@ -45,7 +45,7 @@ _I = ctypes.c_int
 _SZ = ctypes.c_size_t
 _PP = ctypes.POINTER(mr_router_params)
 _SIGS = {
-    "moe_router_fwd": ([_PP, _P, _P, _P, _P, _P, _P, _P], _I),
+    "moe_router_fwd": ([_PP, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_router_bwd": ([_PP, _P, _P, _P, _P, _P], _I),
     "moe_aux_scores_fwd": ([_I, _I, _I, _I, _I, _P, _P, _P, _P], _I),
     "moe_aux_scores_bwd": ([_I, _I, _I, _P, _P, _P, _P], _I),
@@ -53,8 +53,10 @@ _SIGS = {
     "moe_sort_workspace_bytes": ([_I, _I, _I, _I], _SZ),
     "moe_sort": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
     "moe_sort_noalloc": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
+    "moe_sort_noalloc_scratch_bytes": ([], _SZ),
+    "moe_router_set_wait_test": ([ctypes.c_uint, _I], _I),
     "moe_router_fused_workspace_bytes": ([_PP, _I], _SZ),
-    "moe_router_fused_fwd_sort": ([_PP, _P, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], _I),
+    "moe_router_fused_fwd_sort": ([_PP, _P, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
     "moe_router_strerror": ([_I], ctypes.c_char_p),
     "moe_router_set_topk_path": ([_I, _I], _I),
     "moe_router_expf": ([_P, _P, _I, _P], _I),
@@ -160,10 +162,11 @@ def _params(p) -> mr_router_params:
 
 
 def moe_router_fwd(p, logits, probs=None, routing_map=None, intermediate=None, topk_idx=None,
-                   topk_w=None, stream=None) -> int:
+                   topk_w=None, status=None, stream=None) -> int:
     cp = _params(p)
     return _ok(_lib.moe_router_fwd(ctypes.byref(cp), _ptr(logits), _ptr(probs), _ptr(routing_map),
-                                   _ptr(intermediate), _ptr(topk_idx), _ptr(topk_w), _stream(stream)),
+                                   _ptr(intermediate), _ptr(topk_idx), _ptr(topk_w), _ptr(status),
+                                   _stream(stream)),
                "moe_router_fwd")
 
 
@@ -219,7 +222,9 @@ def moe_sort_noalloc(topk_idx, topk_w, T, topk, E_tot, block_m, sorted_token_ids
                "moe_sort_noalloc")
 
 
-MR_SORT_NOALLOC_SCRATCH_BYTES = 1 << 20
+def moe_sort_noalloc_scratch_bytes() -> int:
+    """Bytes of moe_sort_noalloc's fixed scratch array, as the loaded library has it."""
+    return int(_lib.moe_sort_noalloc_scratch_bytes())
 
 
 def moe_router_fused_workspace_bytes(p, block_m) -> int:
@@ -228,7 +233,7 @@ def moe_router_fused_workspace_bytes(p, block_m) -> int:
 
 
 def moe_router_fused_fwd_sort(p, logits, block_m, topk_idx, topk_w, sorted_token_ids, sorted_weights,
-                              expert_ids, num_tokens_post_pad, workspace=None, ws_bytes=None,
+                              expert_ids, num_tokens_post_pad, workspace=None, ws_bytes=None, status=None,
                               stream=None) -> int:
     cp = _params(p)
     if ws_bytes is None:
@@ -236,11 +241,16 @@ def moe_router_fused_fwd_sort(p, logits, block_m, topk_idx, topk_w, sorted_token
     return _ok(_lib.moe_router_fused_fwd_sort(ctypes.byref(cp), _ptr(logits), block_m, _ptr(topk_idx),
                                               _ptr(topk_w), _ptr(sorted_token_ids), _ptr(sorted_weights),
                                               _ptr(expert_ids), _ptr(num_tokens_post_pad), _ptr(workspace),
-                                              ws_bytes, _stream(stream)), "moe_router_fused_fwd_sort")
+                                              ws_bytes, _ptr(status), _stream(stream)), "moe_router_fused_fwd_sort")
 
 
 def moe_router_set_topk_path(select_threshold: int = 8, force_path: int = 0) -> int:
     return _ok(_lib.moe_router_set_topk_path(select_threshold, force_path), "moe_router_set_topk_path")
+
+
+def moe_router_set_wait_test(tries: int = 0, drop_copies: int = 0) -> int:
+    """Test hook of the bounded waits (0, 0 restores the defaults)."""
+    return _ok(_lib.moe_router_set_wait_test(tries, drop_copies), "moe_router_set_wait_test")
 
 
 def moe_router_expf(x, y, stream=None) -> int:
@@ -257,7 +267,7 @@ def moe_router_device_status(out, clear: bool = False, stream=None) -> int:
 
 
 def device_status(clear: bool = False) -> int:
-    """The library's device status word on the current device (0, or MR_ETIMEOUT bits)."""
+    """The library's device status word on the current device (0 or MR_ETIMEOUT)."""
     out = torch.zeros(1, dtype=torch.int32, device="cuda")
     moe_router_device_status(out, clear)
     return int(out.item())
@@ -305,7 +315,7 @@ def params_for(logits: torch.Tensor, topk: int, **kw) -> RouterParams:
 
 
 def route(logits: torch.Tensor, topk: int, dense: bool = True, compact: bool = True, stream=None,
-          **kw) -> dict:
+          status: Optional[torch.Tensor] = None, **kw) -> dict:
     """moe_router_fwd with freshly allocated outputs (probs in the logits dtype)."""
     p = params_for(logits, topk, **kw)
     T, E = logits.shape
@@ -319,7 +329,7 @@ def route(logits: torch.Tensor, topk: int, dense: bool = True, compact: bool = T
         out["topk_idx"] = torch.empty(T, topk, dtype=torch.int32, device=dev)
         out["topk_w"] = torch.empty(T, topk, dtype=torch.float32, device=dev)
     moe_router_fwd(p, logits, out.get("probs"), out.get("routing_map"), out.get("intermediate"),
-                   out.get("topk_idx"), out.get("topk_w"), stream)
+                   out.get("topk_idx"), out.get("topk_w"), status, stream)
     return out
 
 
@@ -369,7 +379,7 @@ def sort(topk_idx: torch.Tensor, topk_w: Optional[torch.Tensor], E_tot: int, blo
 
 
 def fused_route_sort(logits: torch.Tensor, topk: int, block_m: int, compact: bool = True, stream=None,
-                     **kw) -> dict:
+                     status: Optional[torch.Tensor] = None, **kw) -> dict:
     p = params_for(logits, topk, **kw)
     T, E = logits.shape
     E_tot = E + p.n_shared
@@ -381,7 +391,7 @@ def fused_route_sort(logits: torch.Tensor, topk: int, block_m: int, compact: boo
     ws = torch.empty(max(1, nb), dtype=torch.uint8, device=logits.device) if nb else None
     moe_router_fused_fwd_sort(p, logits, block_m, out.get("topk_idx"), out.get("topk_w"),
                               out["sorted_token_ids"], out["sorted_weights"], out["expert_ids"],
-                              out["num_tokens_post_pad"], ws, nb, stream)
+                              out["num_tokens_post_pad"], ws, nb, status, stream)
     return out
 
 

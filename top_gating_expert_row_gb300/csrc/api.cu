@@ -146,16 +146,17 @@ int launch_noop(cudaStream_t st)
 static_assert(MR_MAX_FUSED_TOKENS == 16 && MR_MAX_FUSED_TOKENS_SMALL_E == kFusedWideMaxTokens &&
                   MR_MAX_FUSED_EXPERTS_SMALL == 128 * kFusedWideMaxNv,
               "the header's fused-launch limits and the kernels' must agree");
-static_assert(kStatusTimeout == MR_ETIMEOUT, "device timeout bit and the C ABI's code must agree");
+static_assert(kStatusTimeout == MR_ETIMEOUT && kStatusRange == MR_ERANGE,
+              "the device status codes and the C ABI's must agree");
 
 // The library's status word on each device: kernels whose waits are bounded
-// OR MR_ETIMEOUT into it when one gives up.
-static __device__ uint32_t g_device_status;
+// raise it to MR_ETIMEOUT when one gives up and the call had no status word.
+static __device__ int32_t g_device_status;
 
-__global__ void k_take_status(uint32_t* word, int32_t* out, int clear)
+__global__ void k_take_status(int32_t* word, int32_t* out, int clear)
 {
-    out[0] = static_cast<int32_t>(*word);
-    if (clear) *word = 0u;
+    out[0] = *word;
+    if (clear) *word = 0;
 }
 
 namespace {
@@ -164,7 +165,7 @@ void* g_status_ptr[64] = {nullptr};
 
 // Device address of g_device_status on the current device, looked up once per
 // device and cached (nullptr on failure).
-uint32_t* device_status_address()
+int32_t* device_status_address()
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
@@ -174,7 +175,7 @@ uint32_t* device_status_address()
         if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return nullptr;
         g_status_ptr[dev] = ptr;
     }
-    return static_cast<uint32_t*>(g_status_ptr[dev]);
+    return static_cast<int32_t*>(g_status_ptr[dev]);
 }
 }  // namespace
 
@@ -200,6 +201,13 @@ struct PathConfig {
     int forced() const { return force.load(std::memory_order_relaxed); }
 };
 PathConfig g_path;
+
+// Test hook for the bounded waits (moe_router_set_wait_test).
+struct WaitTest {
+    std::atomic<unsigned> tries{0};  // 0: kWaitLimit
+    std::atomic<int> drop{0};
+};
+WaitTest g_wait_test;
 
 bool use_select(int k_r)
 {
@@ -243,7 +251,7 @@ int check_router(const mr_router_params* p)
 }
 
 RouteArgs route_args(const mr_router_params* p, const void* logits, void* probs, uint8_t* map, float* inter,
-                     int32_t* idx, float* w)
+                     int32_t* idx, float* w, int32_t* status)
 {
     RouteArgs a;
     a.logits = logits;
@@ -264,7 +272,10 @@ RouteArgs route_args(const mr_router_params* p, const void* logits, void* probs,
     a.scaling = p->scaling;
     a.shared_weight = p->shared_weight;
     a.stop = select_stop(a.k_r);
-    a.status = device_status_address();
+    a.status = status ? status : device_status_address();
+    const unsigned tries = g_wait_test.tries.load(std::memory_order_relaxed);
+    a.wait_tries = tries ? tries : kWaitLimit;
+    a.drop_copies = g_wait_test.drop.load(std::memory_order_relaxed);
     const uintptr_t in_al = p->in_dtype == MR_BF16 ? 8 : 16;
     a.vec = (p->E % 4 == 0) && aligned(logits, in_al) && aligned(probs, in_al) && aligned(inter, 16) &&
             aligned(map, 4) && aligned(p->bias, 16);
@@ -336,6 +347,14 @@ const char* moe_router_strerror(int code)
     return "unknown moe_router status";
 }
 
+int moe_router_set_wait_test(unsigned int tries, int drop_copies)
+{
+    if (drop_copies != 0 && drop_copies != 1) return MR_EINVAL;
+    g_wait_test.tries.store(tries, std::memory_order_relaxed);
+    g_wait_test.drop.store(drop_copies, std::memory_order_relaxed);
+    return MR_OK;
+}
+
 int moe_router_set_topk_path(int select_threshold, int force_path)
 {
     if (select_threshold < 0 || force_path < 0 || force_path > 2) return MR_EINVAL;
@@ -345,14 +364,14 @@ int moe_router_set_topk_path(int select_threshold, int force_path)
 }
 
 int moe_router_fwd(const mr_router_params* p, const void* logits, void* probs, uint8_t* routing_map,
-                   float* intermediate, int32_t* topk_idx, float* topk_w, mr_stream_t stream)
+                   float* intermediate, int32_t* topk_idx, float* topk_w, int32_t* status, mr_stream_t stream)
 {
     int rc = check_router(p);
     if (rc != MR_OK) return rc;
     if (!logits) return MR_EINVAL;
     if (!probs && !routing_map && !intermediate && !topk_idx && !topk_w) return MR_EINVAL;
     if (p->T == 0) return MR_OK;
-    const RouteArgs a = route_args(p, logits, probs, routing_map, intermediate, topk_idx, topk_w);
+    const RouteArgs a = route_args(p, logits, probs, routing_map, intermediate, topk_idx, topk_w, status);
     const int nv = nv_index(p->E);
     if (nv < 0) return MR_EUNSUPPORTED;
     return from_cuda(launch_fwd(p->score_fn, p->in_dtype, a, nv, use_select(a.k_r),
@@ -374,7 +393,7 @@ int moe_aux_scores_fwd(int T, int E, int topk, int score_fn, int in_dtype, const
     if (rc != MR_OK) return rc;
     if (!logits || (!scores && !routing_map)) return MR_EINVAL;
     if (T == 0) return MR_OK;
-    const RouteArgs a = route_args(&p, logits, nullptr, routing_map, scores, nullptr, nullptr);
+    const RouteArgs a = route_args(&p, logits, nullptr, routing_map, scores, nullptr, nullptr, nullptr);
     const int nv = nv_index(E);
     if (nv < 0) return MR_EUNSUPPORTED;
     return from_cuda(launch_fwd(score_fn, in_dtype, a, nv, use_select(a.k_r), reinterpret_cast<cudaStream_t>(stream)));
@@ -515,6 +534,8 @@ int moe_sort(const int32_t* topk_idx, const float* topk_w, int T, int topk, int 
                                  status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t moe_sort_noalloc_scratch_bytes(void) { return sizeof(g_sort_scratch); }
+
 int moe_sort_noalloc(const int32_t* topk_idx, const float* topk_w, int T, int topk, int E_tot, int block_m,
                      int32_t* sorted_token_ids, float* sorted_weights, int32_t* expert_ids,
                      int32_t* num_tokens_post_pad, int32_t* status, mr_stream_t stream)
@@ -546,7 +567,8 @@ size_t moe_router_fused_workspace_bytes(const mr_router_params* p, int block_m)
 
 int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int block_m, int32_t* topk_idx,
                               float* topk_w, int32_t* sorted_token_ids, float* sorted_weights, int32_t* expert_ids,
-                              int32_t* num_tokens_post_pad, void* workspace, size_t ws_bytes, mr_stream_t stream)
+                              int32_t* num_tokens_post_pad, void* workspace, size_t ws_bytes, int32_t* status,
+                              mr_stream_t stream)
 {
     int rc = check_router(p);
     if (rc != MR_OK) return rc;
@@ -559,7 +581,7 @@ int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int
     if (nv < 0) return MR_EUNSUPPORTED;
     const int k_r = p->topk - p->n_shared;
     if (fused_one_launch(p->T, kNvBuckets[nv])) {
-        RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, topk_idx, topk_w);
+        RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, topk_idx, topk_w, status);
         SortArgs s{sorted_token_ids, sorted_weights, expert_ids, num_tokens_post_pad, E_tot, block_m,
                    log2_if_pow2(block_m)};
         // a one-CTA decode launch is bound by instruction fetch on a cold SM: the
@@ -584,11 +606,11 @@ int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int
     int32_t* idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(w);
     float* wt = topk_w ? topk_w : reinterpret_cast<float*>(w + align_up(N * 4, 256));
     uint32_t* sws = reinterpret_cast<uint32_t*>(w + align_up(N * 4, 256) * 2);
-    const RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, idx, wt);
+    const RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, idx, wt, status);
     int e = launch_fwd(p->score_fn, p->in_dtype, a, nv, use_select(k_r), st);
     if (e != cudaSuccess) return MR_ECUDA;
     return from_cuda(launch_sort(idx, wt, static_cast<int>(N), E_tot, block_m, sorted_token_ids, sorted_weights,
-                                 expert_ids, num_tokens_post_pad, sws, nullptr, st));
+                                 expert_ids, num_tokens_post_pad, sws, status, st));
 }
 
 int moe_router_expf(const float* x, float* y, int n, mr_stream_t stream)
@@ -603,7 +625,7 @@ int moe_router_noop(mr_stream_t stream) { return from_cuda(launch_noop(reinterpr
 int moe_router_device_status(int32_t* out, int clear, mr_stream_t stream)
 {
     if (!out) return MR_EINVAL;
-    uint32_t* word = device_status_address();
+    int32_t* word = device_status_address();
     if (!word) return MR_ECUDA;
     k_take_status<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(word, out, clear);
     return from_cuda(cudaGetLastError());

@@ -256,10 +256,15 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void bulk_load_row(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+// Arms the barrier for `bytes` and issues the copy. drop != 0 (a test mode)
+// arms the barrier without issuing the copy, so its wait runs out while no
+// copy is in flight.
+__device__ __forceinline__ void bulk_load_row(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              int drop = 0)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                  : "memory");
+    if (drop) return;
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_addr(dst)),
                  "l"(src), "r"(bytes), "r"(smem_addr(bar))
@@ -280,16 +285,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
-// Status bit a kernel OR-s into the library's device status word when a bounded
-// wait gives up (the C ABI's MR_ETIMEOUT).
-constexpr uint32_t kStatusTimeout = 8u;
+// Codes a kernel reports in a device status word (the C ABI's MR_ERANGE and
+// MR_ETIMEOUT). A word is raised to a code with an atomic maximum, so it holds
+// the most severe code reported since it was zeroed.
+constexpr int32_t kStatusRange = 4;
+constexpr int32_t kStatusTimeout = 5;
 
-// Bounded wait (about a second at most) for phase `parity` of the barrier:
-// false if it gave up.
-constexpr uint32_t kWaitLimit = 1u << 20;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
+__device__ __forceinline__ void report_status(int32_t* word, int32_t code)
 {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (word) atomicMax(word, code);
+}
+
+// Bounded wait for phase `parity` of the barrier: at most `tries` attempts of
+// about a microsecond each (the default, 2^20, is about a second); false if it
+// gave up.
+constexpr uint32_t kWaitLimit = 1u << 20;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t tries = kWaitLimit)
+{
+    for (uint32_t i = 0; i < tries; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }

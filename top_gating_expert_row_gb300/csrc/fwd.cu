@@ -87,13 +87,14 @@ __global__ void __launch_bounds__(kWideThreads, kWideMinBlocks) k_router_fwd_wid
     st.bytes = row_bytes;
     st.off = sizeof(InT) == 4 ? 0u : static_cast<uint32_t>(a.E) * 2u;
     st.next = nullptr;
+    st.drop = a.drop_copies;
     uint32_t phase = 0u;
     int t = blockIdx.x * nw + warp;
     if (FULL) {
         if (lane == 0) mbar_init(st.bar, 1);
         __syncwarp();
         if (lane == 0 && t < a.T) bulk_load_row(wsm + L.kbuf + st.off, rows + static_cast<size_t>(t) * a.E, row_bytes,
-                                                st.bar);
+                                                st.bar, st.drop);
     }
     for (; t < a.T; t += stride) {
         // rows that are not staged stream into L2 one row ahead (staged rows do
@@ -101,12 +102,14 @@ __global__ void __launch_bounds__(kWideThreads, kWideMinBlocks) k_router_fwd_wid
         if (!FULL && a.prefetch && lane == 0 && t + stride < a.T)
             prefetch_l2(rows + static_cast<size_t>(t + stride) * a.E, row_bytes);
         if (FULL) {
-            const bool ok = __all_sync(kFull, mbar_wait(st.bar, phase));
+            const bool ok = __all_sync(kFull, mbar_wait(st.bar, phase, a.wait_tries));
             if (!ok) {
                 // the copy did not land within the wait limit: report it, give
-                // the copy one more bounded wait, and stop (no further rows)
-                if (lane == 0 && a.status) atomicOr(a.status, kStatusTimeout);
-                mbar_wait(st.bar, phase);
+                // the copy one more bounded wait (so that, short of a failed
+                // memory system, it has landed before the warp leaves), and stop
+                // (no further rows)
+                if (lane == 0) report_status(a.status, kStatusTimeout);
+                mbar_wait(st.bar, phase, a.wait_tries);
                 return;
             }
             phase ^= 1u;

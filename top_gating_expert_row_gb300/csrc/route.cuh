@@ -43,7 +43,9 @@ struct RouteArgs {
     int vec;       // rows and all arrays allow 16-byte (fp32) / 8-byte (bf16) vector access
     int prefetch;  // rows are 16-byte aligned and a multiple of 16 bytes: L2 bulk prefetch allowed
     int stop;      // SELECT: candidate capacity (>= k_r); bisection stops at or below it
-    uint32_t* status;  // device status word (kStatusTimeout is OR-ed in when a bounded wait gives up)
+    int32_t* status;      // device status word, raised to kStatusTimeout when a bounded wait gives up
+    uint32_t wait_tries;  // attempts (about 1 us each) before a bounded wait gives up
+    int drop_copies;      // test mode: arm the staging barriers but issue no copies
 };
 
 // Byte offsets of one warp's shared-memory region (same formula on host and device).

@@ -44,6 +44,7 @@ struct Stage {
     const void* next;  // nullptr: no next row for this warp
     uint32_t bytes;    // row bytes (E * element size)
     uint32_t off;      // byte offset of the raw row inside kbuf
+    int drop;          // test mode: arm the barrier, issue no copy
 };
 
 __host__ __device__ inline WideLayout wide_layout(int k_r, int stop, int E, bool select, bool keep_scores)
@@ -401,7 +402,7 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
         // the copy's writes.
         if (FULL && st.next) fence_proxy_async_smem();
         __syncwarp();
-        if (FULL && st.next && lane == 0) bulk_load_row(wsm + L.kbuf + st.off, st.next, st.bytes, st.bar);
+        if (FULL && st.next && lane == 0) bulk_load_row(wsm + L.kbuf + st.off, st.next, st.bytes, st.bar, st.drop);
         rank_candidates<3>(cand, n, k_r, warm_rank, lane, win_idx, win_val, scal + 3, score_of);
         __syncwarp();
         warm = scal[3];
@@ -410,7 +411,7 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
     // threshold select staged it before its ranking)
     if (!SELECT && FULL && st.next) fence_proxy_async_smem();
     __syncwarp();
-    if (!SELECT && FULL && st.next && lane == 0) bulk_load_row(wsm + L.kbuf + st.off, st.next, st.bytes, st.bar);
+    if (!SELECT && FULL && st.next && lane == 0) bulk_load_row(wsm + L.kbuf + st.off, st.next, st.bytes, st.bar, st.drop);
 
     // 4. weights
     float wsum = 0.0f;

@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(kSortThreads) k_sort_hist(const int32_t* __res
         }
         warp_hist_add(hist, e, lane);
     }
-    if (status && __any_sync(kFull, bad) && lane == 0) atomicOr(status, 4 /* MR_ERANGE */);
+    if (__any_sync(kFull, bad) && lane == 0) report_status(status, kStatusRange);
     __syncthreads();
     uint32_t* out = ws + static_cast<size_t>(blockIdx.x) * E_tot;
     for (int e = tid; e < E_tot; e += blockDim.x) out[e] = hist[e];
