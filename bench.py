@@ -431,16 +431,87 @@ def prefill_route_sort(mr, dev, stream, reps=20) -> dict:
             route()
             srt()
     torch.cuda.synchronize()
+    fws = torch.empty(max(1, mr.moe_router_fused_workspace_bytes(cp, w.block_m)), dtype=torch.uint8, device=dev)
+    fused = lambda: L.moe_router_fused_fwd_sort(P, x.data_ptr(), w.block_m, idx.data_ptr(), wt.data_ptr(), a[0],  # noqa
+                                                a[1], a[2], a[3], fws.data_ptr(), fws.numel(), None, s)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            if fused() != 0:
+                raise RuntimeError("fused prefill call failed")
+    torch.cuda.synchronize()
     # tens of µs per call, close to the cost of a Python launch: timed as CUDA-graph replays
     r_us = graph_us(route, stream, reps)
     s_us = graph_us(srt, stream, reps)
+    f_us = graph_us(fused, stream, reps)
     rb = w.T * w.E * 2 + w.T * w.topk * 8 + w.E * 4
     npp = int(bufs["num_tokens_post_pad"].item())
     sb = w.T * w.topk * 8 + npp * 8 + (npp // w.block_m) * 4 + 4
     return {"workload": w.name, "route_us": round(r_us, 2), "sort_us": round(s_us, 2),
             "route_GB/s": round(rb / (r_us * 1e-6) / 1e9, 1), "sort_GB/s": round(sb / (s_us * 1e-6) / 1e9, 1),
-            "route_plus_sort_us": round(r_us + s_us, 2), "num_tokens_post_pad": npp,
+            "route_plus_sort_us": round(r_us + s_us, 2), "fused_us": round(f_us, 2),
+            "fused_launches": "route counting the sort's chunks + scatter", "num_tokens_post_pad": npp,
             "timing": "CUDA graph, 20 calls per replay"}
+
+
+# sort-only workloads (T, topk, E_tot, block_m, Zipf skew of the expert load):
+# the prefill shape, the large-E shape and about a million pairs
+SORT_SCALING = ((16384, 9, 385, 64, 1.1), (8192, 36, 2304, 64, 0.8), (131072, 8, 256, 32, 1.1))
+
+
+def sort_scaling(mr, dev, stream, reps=20, shapes=SORT_SCALING) -> dict:
+    """moe_sort alone on seeded (token, slot) -> expert assignments of growing
+    size, to show how its cost grows with T*topk. CUDA-graph replays."""
+    L = mr._lib
+    s = stream.cuda_stream
+    out = {"timing": f"CUDA graph, {reps} calls per replay"}
+    for T, k, E_tot, bm, skew in shapes:
+        idx, wt = synth.random_topk_idx(T, k, E_tot, skew)
+        idx, wt = idx.to(dev), wt.to(dev)
+        bufs = mr.sort_buffers(T, k, E_tot, bm, dev)
+        ws = torch.empty(max(1, mr.moe_sort_workspace_bytes(T, k, E_tot, bm)), dtype=torch.uint8, device=dev)
+        a = [bufs[n].data_ptr() for n in ("sorted_token_ids", "sorted_weights", "expert_ids", "num_tokens_post_pad")]
+
+        def call(idx=idx, wt=wt, a=a, ws=ws, bufs=bufs, T=T, k=k, E_tot=E_tot, bm=bm):
+            rc = L.moe_sort(idx.data_ptr(), wt.data_ptr(), T, k, E_tot, bm, a[0], a[1], a[2], a[3], ws.data_ptr(),
+                            ws.numel(), None, s)
+            if rc != 0:
+                raise RuntimeError(mr.strerror(rc))
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                call()
+        torch.cuda.synchronize()
+        us = graph_us(call, stream, reps)
+        out[f"T={T} k={k} E_tot={E_tot} bm={bm}"] = {"pairs": T * k, "us": round(us, 2),
+                                                      "ns_per_kpair": round(us * 1e6 / (T * k), 1)}
+    return out
+
+
+def summary(line) -> dict:
+    """The key figures of the line, short enough to survive a truncated log:
+    fractions of the measured HBM peak per kernel (in the step, and isolated
+    with rotated buffers), decode µs (fused/unfused x graph/eager, the launch
+    floor), the prefill route + sort and the sort's growth."""
+    pk = line["roofline"]["peak"]
+    out = {"peak_GB/s": pk, "step_frac": {n: v["frac_of_peak"] for n, v in line["per_kernel"].items()}}
+    for name, d in line.get("breakdown", {}).items():
+        short = name.replace("softmax_T8192_", "").replace("sigmoid_bias_T8192_", "sig_")
+        short = short.replace("_isolated", "_iso")
+        out[short] = [round(d[kd]["GB/s"] / pk, 2) for kd in ("fwd", "bwd", "aux_fwd", "aux_bwd") if kd in d]
+    dec = line.get("decode")
+    if dec:
+        out["decode_floor_us"] = [dec["launch_floor"]["graph_us"], dec["launch_floor"]["eager_us"]]
+        out["decode_us[fg,fe,ug,ue]"] = {
+            t.split("=")[1]: [dec[t]["fused_graph_us"], dec[t]["fused_eager_us"], dec[t]["unfused_graph_us"],
+                              dec[t]["unfused_eager_us"]]
+            for t in dec if t.startswith("T=") and int(t.split("=")[1]) <= 16}
+    pf = line.get("prefill_route_sort")
+    if pf:
+        out["prefill_us[route,sort,fused]"] = [pf["route_us"], pf["sort_us"], pf["fused_us"]]
+    ss = line.get("sort_scaling")
+    if ss:
+        out["sort_us_by_pairs"] = {v["pairs"]: v["us"] for k, v in ss.items() if isinstance(v, dict)}
+    return out
 
 
 def aux_loss_rates(mr, w, dev, stream, reps=50) -> dict:
@@ -664,7 +735,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["all", "step", "decode", "aux_loss", "prefill", "bf16"], default="all",
+    ap.add_argument("--only", choices=["all", "step", "decode", "aux_loss", "prefill", "bf16", "sort"], default="all",
                     help="step: the timed step only; decode: the decode latency table only "
                          "(both used for profiling captures)")
     ap.add_argument("--decode-calls", type=int, default=200, help="calls per decode timing loop")
@@ -699,6 +770,10 @@ def main():
     if args.only == "bf16":
         if rank == 0:
             print(json.dumps({"bf16": bf16_rates(mr, dev, torch.cuda.Stream(device=dev))}), flush=True)
+        return 0
+    if args.only == "sort":
+        if rank == 0:
+            print(json.dumps({"sort_scaling": sort_scaling(mr, dev, torch.cuda.Stream(device=dev))}), flush=True)
         return 0
     if args.only == "prefill":
         if rank == 0:
@@ -785,14 +860,19 @@ def main():
             line["decode_gpt_oss"] = decode_latency(mr, dev, stream, args.decode_calls, (1, 4, 16, 32, 64),
                                                     synth.decode_gpt_oss)
             line["prefill_route_sort"] = prefill_route_sort(mr, dev, stream)
+            line["sort_scaling"] = sort_scaling(mr, dev, stream)
             line["aux_loss"] = aux_loss_rates(mr, w, dev, stream)
             line["bf16"] = bf16_rates(mr, dev, stream)
             breakdown = {}
             for wl in [synth.large_softmax(k) for k in synth.LARGE_TOPKS] + [synth.large_e_sigmoid()]:
                 breakdown[wl.name] = time_kernels(mr, wl, dev, stream)
+            # the step's own kernels isolated: rotated buffer sets beyond L2, so the
+            # backward kernels read inputs the forward did not just leave in L2
+            breakdown[w.name + "_isolated"] = time_kernels(mr, w, dev, stream)
             line["breakdown"] = breakdown
             if not args.no_cpu_baseline:
                 line["cpu_baseline"] = cpu_baseline(w, args.cpu_rows)
+            line["summary"] = summary(line)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -140,9 +140,15 @@ def test_sort_sizes_and_rejects(lib):
         return s(*a)
 
     assert call(T=-1) == 1 and call(topk=0) == 1 and call(E_tot=0) == 1 and call(bm=0) == 1
-    assert call(ids=None) == 1 and call(eids=None) == 1 and call(npp=None) == 1 and call(ws=None) == 1
+    assert call(ids=None) == 1 and call(eids=None) == 1 and call(npp=None) == 1
     assert call(idx=None) == 1
-    assert call(wsb=0) == 1                       # workspace too small
+    # up to 4096 pairs one CTA sorts without a workspace; above that the
+    # workspace holds per-chunk prefixes and cluster totals
+    assert lib.moe_sort_workspace_bytes(4, 2, 8, 4) == 0
+    assert lib.moe_sort_workspace_bytes(2048, 2, 8, 4) == 0
+    assert lib.moe_sort_workspace_bytes(2049, 2, 8, 4) > 0
+    assert call(T=4096, ws=None) == 1             # workspace needed, none given
+    assert call(T=4096, wsb=0) == 1               # workspace too small
     assert call(E_tot=5000) == 2                  # beyond MR_MAX_SORT_EXPERTS
     assert call(T=1 << 28, topk=16) == 1          # T*topk >= INT_MAX
 

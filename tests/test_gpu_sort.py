@@ -10,9 +10,14 @@ from parity import assert_close, assert_equal
 pytestmark = pytest.mark.gpu
 
 
+# One CTA up to 4096 pairs; above that chunks of 1024..4096 pairs in clusters of
+# 8 (a partial last cluster, fewer experts than a cluster has CTAs, 4096
+# experts over many chunks, about a million pairs).
 SORT_CASES = [(16, 2, 8, 4, None), (16384, 9, 385, 64, 1.1), (16, 8, 256, 32, None), (1000, 4, 37, 1, None),
               (50, 3, 5, 7, 2.0), (4097, 6, 128, 16, None), (3, 1, 4096, 8, None), (8192, 36, 2304, 64, 0.8),
-              (1, 1, 1, 1, None), (5000, 2, 3, 128, None)]
+              (1, 1, 1, 1, None), (5000, 2, 3, 128, None), (1025, 4, 100, 16, None), (4096, 1, 64, 8, None),
+              (20000, 3, 5, 3, None), (50000, 8, 4096, 32, 1.1), (131072, 8, 256, 32, 1.1),
+              (70001, 9, 385, 64, 1.1)]
 
 
 @pytest.mark.parametrize("T,k,E_tot,bm,skew", SORT_CASES)
@@ -102,6 +107,17 @@ FUSED = [synth.decode(T) for T in synth.DECODE_TS] + [synth.decode_gpt_oss(T) fo
     synth.Workload("fallback_T300_grouped", 300, 384, 9, synth.SIGMOID, synth.BF16, renorm=1, scaling=2.827,
                    n_group=8, topk_group=4, n_shared=1, bias_range=0.05, block_m=64),
     synth.Workload("fallback_wide_T4_e2304", 4, 2304, 36, synth.SOFTMAX, synth.F32, block_m=8),
+    # above 4096 pairs (E <= 1024) the route kernel counts the sort's chunks itself
+    synth.Workload("prefill_T600_e256_k8", 600, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
+    synth.Workload("prefill_T5000_e100_k5_sigmoid", 5000, 100, 5, synth.SIGMOID, synth.F32, renorm=1, scaling=1.5,
+                   bias_range=0.1, block_m=8),
+    synth.Workload("prefill_T3000_grouped_shared", 3000, 384, 9, synth.SIGMOID, synth.BF16, renorm=1, scaling=2.827,
+                   n_group=8, topk_group=4, n_shared=1, bias_range=0.05, zipf_s=1.1, block_m=64),
+    synth.Workload("prefill_T2500_e1024_k36", 2500, 1024, 36, synth.SOFTMAX, synth.F32, block_m=16),
+    synth.Workload("prefill_T9000_e64_k2", 9000, 64, 2, synth.SOFTMAX, synth.F32, renorm=1, block_m=128),
+    # wide rows: the forward, then moe_sort
+    synth.Workload("prefill_wide_T300_e2304", 300, 2304, 36, synth.SIGMOID, synth.F32, renorm=1, scaling=2.5,
+                   bias_range=0.1, block_m=32),
 ]
 
 
@@ -141,3 +157,38 @@ def test_fused_route_sort_matches_oracle(mr, orc, w, path):
     refw = np.zeros(len(ids))
     refw[real] = r["topk_w"].reshape(-1)[ids[real]]
     assert_close(out["sorted_weights"][:n], refw, "sorted_weights")
+
+
+@pytest.mark.parametrize("path", [0, 1, 2], ids=["auto", "argmax", "select"])
+def test_fused_prefill_full_size_every_row(mr, orc, path):
+    """The prefill workload (T=16384, E=384 + 1 shared, topk=9, grouped sigmoid,
+    block_m=64) through moe_router_fused_fwd_sort, whose route kernel also counts
+    the sort's chunks: every row's top-k and the whole sorted layout against the
+    oracle."""
+    w = synth.prefill_grouped()
+    x = w.make_logits()
+    b = w.make_bias()
+    xg, bg = x.cuda(), b.cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mr.moe_router_set_topk_path(8, path)
+    try:
+        out = mr.fused_route_sort(xg, w.topk, w.block_m, score_fn=w.score_fn, renorm=w.renorm, n_group=w.n_group,
+                                  topk_group=w.topk_group, n_shared=w.n_shared, scaling=w.scaling,
+                                  shared_weight=w.shared_weight, bias=bg, status=status)
+    finally:
+        mr.moe_router_set_topk_path(8, 0)
+    torch.cuda.synchronize()
+    r, srt = _oracle_fused(orc, w, x, b)
+    assert int(status.item()) == 0
+    assert_equal(out["topk_idx"], r["topk_idx"], "topk_idx")
+    assert_close(out["topk_w"], r["topk_w"], "topk_w")
+    n = int(out["num_tokens_post_pad"].item())
+    assert n == srt["num_tokens_post_pad"]
+    assert_equal(out["sorted_token_ids"][:n], srt["sorted_token_ids"], "sorted_token_ids")
+    assert_equal(out["expert_ids"][: n // w.block_m], srt["expert_ids"], "expert_ids")
+    # the sorted weights are the GPU's own topk_w gathered by sorted id (bit for bit)
+    ids = out["sorted_token_ids"][:n].long()
+    real = ids < w.T * w.topk
+    want = torch.zeros(n, dtype=torch.float32, device="cuda")
+    want[real] = out["topk_w"].reshape(-1)[ids[real]]
+    assert torch.equal(out["sorted_weights"][:n], want)

@@ -85,12 +85,25 @@ int launch_fused_s0_d0(const RouteArgs&, const SortArgs&, int, bool, cudaStream_
 int launch_fused_s0_d1(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
 int launch_fused_s1_d0(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
 int launch_fused_s1_d1(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
+int launch_fwd_hist_s0_d0(const RouteArgs&, int, bool, int, int, int, uint32_t*, uint32_t*, int*, int*, cudaStream_t);
+int launch_fwd_hist_s0_d1(const RouteArgs&, int, bool, int, int, int, uint32_t*, uint32_t*, int*, int*, cudaStream_t);
+int launch_fwd_hist_s1_d0(const RouteArgs&, int, bool, int, int, int, uint32_t*, uint32_t*, int*, int*, cudaStream_t);
+int launch_fwd_hist_s1_d1(const RouteArgs&, int, bool, int, int, int, uint32_t*, uint32_t*, int*, int*, cudaStream_t);
 
 int launch_fwd(int score_fn, int in_dtype, const RouteArgs& a, int nv_idx, bool select, cudaStream_t st)
 {
     if (score_fn == kSoftmax)
         return in_dtype ? launch_fwd_s0_d1(a, nv_idx, select, st) : launch_fwd_s0_d0(a, nv_idx, select, st);
     return in_dtype ? launch_fwd_s1_d1(a, nv_idx, select, st) : launch_fwd_s1_d0(a, nv_idx, select, st);
+}
+
+int launch_fwd_hist(int score_fn, int in_dtype, const RouteArgs& a, int nv_idx, bool select, int R_min,
+                    int nchunk_max_pad, int E_tot, uint32_t* pre, uint32_t* ctot, int* R_out, int* nchunk_pad_out,
+                    cudaStream_t st)
+{
+    auto f = score_fn == kSoftmax ? (in_dtype ? launch_fwd_hist_s0_d1 : launch_fwd_hist_s0_d0)
+                                  : (in_dtype ? launch_fwd_hist_s1_d1 : launch_fwd_hist_s1_d0);
+    return f(a, nv_idx, select, R_min, nchunk_max_pad, E_tot, pre, ctot, R_out, nchunk_pad_out, st);
 }
 
 int launch_fused_decode(int score_fn, int in_dtype, const RouteArgs& a, const SortArgs& s, int nv_idx,
@@ -283,8 +296,6 @@ RouteArgs route_args(const mr_router_params* p, const void* logits, void* probs,
     a.prefetch = a.vec && row_bytes % 16 == 0 && aligned(logits, 16);
     return a;
 }
-
-size_t sort_ws_bytes(long long N, int E_tot) { return static_cast<size_t>(sort_chunks(N)) * E_tot * 4; }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -525,10 +536,11 @@ int moe_sort(const int32_t* topk_idx, const float* topk_w, int T, int topk, int 
 {
     int rc = check_sort(T, topk, E_tot, block_m);
     if (rc != MR_OK) return rc;
-    if (!sorted_token_ids || !expert_ids || !num_tokens_post_pad || !workspace) return MR_EINVAL;
+    if (!sorted_token_ids || !expert_ids || !num_tokens_post_pad) return MR_EINVAL;
     if (T > 0 && !topk_idx) return MR_EINVAL;
     const long long N = static_cast<long long>(T) * topk;
-    if (ws_bytes < sort_ws_bytes(N, E_tot) || !aligned(workspace, 4)) return MR_EINVAL;
+    const size_t need = sort_ws_bytes(N, E_tot);
+    if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 4))) return MR_EINVAL;
     return from_cuda(launch_sort(topk_idx, topk_w, static_cast<int>(N), E_tot, block_m, sorted_token_ids,
                                  sorted_weights, expert_ids, num_tokens_post_pad, static_cast<uint32_t*>(workspace),
                                  status, reinterpret_cast<cudaStream_t>(stream)));
@@ -562,7 +574,14 @@ size_t moe_router_fused_workspace_bytes(const mr_router_params* p, int block_m)
     if (nv < 0) return 0;
     if (fused_one_launch(p->T, kNvBuckets[nv])) return 0;
     const size_t N = static_cast<size_t>(p->T) * p->topk;
-    return align_up(N * 4, 256) * 2 + sort_ws_bytes(static_cast<long long>(N), p->E + p->n_shared);
+    const int E_tot = p->E + p->n_shared;
+    size_t table;
+    if (fused_counts_in_route(static_cast<long long>(N), kNvBuckets[nv])) {  // route + counts, then the scatter
+        table = sort_table_bytes(fused_plan(p->T, p->topk, kNvBuckets[nv]).nchunk_max_pad, E_tot);
+    } else {
+        table = sort_ws_bytes(static_cast<long long>(N), E_tot);
+    }
+    return align_up(N * 4, 256) * 2 + table;
 }
 
 int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int block_m, int32_t* topk_idx,
@@ -607,6 +626,20 @@ int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int
     float* wt = topk_w ? topk_w : reinterpret_cast<float*>(w + align_up(N * 4, 256));
     uint32_t* sws = reinterpret_cast<uint32_t*>(w + align_up(N * 4, 256) * 2);
     const RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, idx, wt, status);
+    if (fused_counts_in_route(static_cast<long long>(N), kNvBuckets[nv])) {
+        // the route kernel counts its chunks' pairs for the sort, whose
+        // histogram launch is then not needed
+        const FusedPlan fp = fused_plan(p->T, p->topk, kNvBuckets[nv]);
+        uint32_t* pre = sws;
+        uint32_t* ctot = sws + static_cast<size_t>(fp.nchunk_max_pad) * E_tot;
+        int R = 0, nchunk_pad = 0;
+        int e = launch_fwd_hist(p->score_fn, p->in_dtype, a, nv, use_select(k_r), fp.R_min, fp.nchunk_max_pad, E_tot,
+                                pre, ctot, &R, &nchunk_pad, st);
+        if (e != cudaSuccess) return MR_ECUDA;
+        return from_cuda(launch_sort_scatter(idx, wt, static_cast<int>(N), R * p->topk, nchunk_pad, E_tot, block_m,
+                                             pre, ctot, sorted_token_ids, sorted_weights, expert_ids,
+                                             num_tokens_post_pad, st));
+    }
     int e = launch_fwd(p->score_fn, p->in_dtype, a, nv, use_select(k_r), st);
     if (e != cudaSuccess) return MR_ECUDA;
     return from_cuda(launch_sort(idx, wt, static_cast<int>(N), E_tot, block_m, sorted_token_ids, sorted_weights,

@@ -5,11 +5,17 @@
 //   k_router_fwd     persistent grid, 8 warps per CTA, one token row per warp
 //                    at a time (TransformerEngine PR 3012, fused_topk_with_
 //                    score_function; also serves fused_score_for_moe_aux_loss)
+//   k_router_fwd_hist  the prefill route + sort's first launch: CTA c routes a
+//                    contiguous run of rows (its chunk of pairs), counts the
+//                    chunk's experts in shared memory, and its cluster of 8
+//                    turns the counts into the sort's prefixes (FlyDSL PR 582,
+//                    fusing the top-k gating with the sorting step)
 //   k_fused_decode   ONE CTA for T <= 16 tokens (T <= 64 for E <= 256, with 32
 //                    warps): warp t routes token t (and t + 32), then
 //                    the whole CTA histograms, scans and scatters the T*topk
 //                    pairs in shared memory (FlyDSL PR 582, fused top-k gating
 //                    + MoE sorting at decode sizes)
+#include <mutex>
 #include <type_traits>
 
 #include "internal.h"
@@ -36,10 +42,6 @@ using InT = float;
 #endif
 constexpr int kScore = MR_SCORE_FN;
 
-// Resident CTAs per SM the register budget is sized for: the row's keys take
-// 4*NV registers per lane.
-constexpr int fwd_min_blocks(int nv) { return nv >= 12 ? 2 : (nv >= 6 ? 3 : 4); }
-
 // RANKW: candidates per lane in a pass of the candidate rank (3 only where the
 // candidate cap exceeds 64, see rank_candidates)
 template <int NV, bool SELECT, bool FULL, int RANKW = 2>
@@ -65,6 +67,51 @@ __global__ void __launch_bounds__(kFwdThreads, fwd_min_blocks(NV)) k_router_fwd(
         }
         __syncwarp();
     }
+}
+
+// Route + the sort's counts: CTA c routes rows [c*R, min(T, (c+1)*R)) (pairs
+// [c*R*topk, ...), its sort chunk), writes the compact outputs, counts the
+// chunk's experts (routed winners and shared experts) in shared memory and
+// hands the counts to cluster_prefix_counts, whose pre / ctot feed
+// k_sort_scatter. Counted are exactly the ids written to topk_idx that lie in
+// [0, E_tot), the ids the scatter places.
+template <int NV, bool SELECT, bool FULL, int RANKW = 2>
+__global__ void __cluster_dims__(kClusterChunks, 1, 1) __launch_bounds__(kFwdThreads, fwd_min_blocks(NV))
+    k_router_fwd_hist(RouteArgs a, int R, int E_tot, uint32_t* pre, uint32_t* ctot)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nw = blockDim.x >> 5;
+    const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, SELECT, a.n_group > 0);
+    unsigned char* wsm = smem + static_cast<size_t>(warp) * L.bytes;
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + static_cast<size_t>(nw) * L.bytes);
+    for (int e = threadIdx.x; e < E_tot; e += blockDim.x) hist[e] = 0u;
+    __syncthreads();
+    const long long r0l = static_cast<long long>(blockIdx.x) * R;
+    const int r0 = static_cast<int>(r0l < a.T ? r0l : a.T);
+    const int r1 = min(a.T, r0 + R);
+    const uint32_t row_bytes = static_cast<uint32_t>(a.E) * sizeof(InT);
+    uint32_t warm = 0u;
+    for (int t = r0 + warp; t < r1; t += nw) {
+        if (a.prefetch && lane == 0 && t + nw < r1)
+            prefetch_l2(static_cast<const InT*>(a.logits) + static_cast<size_t>(t + nw) * a.E, row_bytes);
+        const float scale = route_row<kScore, InT, NV, SELECT, FULL, RANKW>(a, t, wsm, L, lane, warm);
+        const size_t o = static_cast<size_t>(t) * a.topk;
+        emit_compact(a, wsm, L, scale, lane, a.topk_idx + o, a.topk_w ? a.topk_w + o : nullptr);
+        const uint32_t* win_idx = reinterpret_cast<const uint32_t*>(wsm + L.win_idx);
+        for (int j0 = 0; j0 < a.topk; j0 += 32) {
+            const int j = j0 + lane;
+            int e = kInvalidExpert;
+            if (j < a.topk) {
+                e = j < a.k_r ? static_cast<int>(win_idx[j]) : a.E + (j - a.k_r);  // as emit_compact writes it
+                if (e < 0 || e >= E_tot) e = kInvalidExpert;
+            }
+            warp_hist_add(hist, e, lane);
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+    cluster_prefix_counts(hist, E_tot, pre, ctot);
 }
 
 // Wide rows (E > 1024): the row lives in shared memory, one warp per row.
@@ -259,6 +306,52 @@ FwdFn fwd_kernel(int nv_idx)
     return nullptr;
 }
 
+using FwdHistFn = void (*)(RouteArgs, int, int, uint32_t*, uint32_t*);
+
+template <bool SELECT, bool FULL, int RANKW = 2>
+FwdHistFn fwd_hist_kernel(int nv_idx)
+{
+    switch (kNvBuckets[nv_idx]) {
+        case 1: return k_router_fwd_hist<1, SELECT, FULL, RANKW>;
+        case 2: return k_router_fwd_hist<2, SELECT, FULL, RANKW>;
+        case 3: return k_router_fwd_hist<3, SELECT, FULL, RANKW>;
+        case 4: return k_router_fwd_hist<4, SELECT, FULL, RANKW>;
+        case 6: return k_router_fwd_hist<6, SELECT, FULL, RANKW>;
+        case 8: return k_router_fwd_hist<8, SELECT, FULL, RANKW>;
+    }
+    return nullptr;
+}
+
+// Clusters of this kernel that fit on the device at once (cached per kernel,
+// shared-memory size and device; 0 if the query fails).
+int resident_clusters(const void* func, int threads, size_t smem)
+{
+    static std::mutex mu;
+    struct Entry {
+        const void* func;
+        size_t smem;
+        int dev, clusters;
+    };
+    static Entry cache[64];
+    static int n = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < n; ++i)
+        if (cache[i].func == func && cache[i].smem == smem && cache[i].dev == dev) return cache[i].clusters;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kClusterChunks, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, func, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        clusters = 0;
+    }
+    if (n < 64) cache[n++] = Entry{func, smem, dev, clusters};
+    return clusters;
+}
+
 template <bool SELECT, bool FULL>
 FusedFn fused_kernel(int nv_idx, bool wide)
 {
@@ -315,6 +408,37 @@ int MR_CAT(launch_fwd, MR_SUFFIX)(const RouteArgs& a, int nv_idx, bool select, c
     const int grid = persistent_grid(reinterpret_cast<const void*>(f), kFwdThreads, smem, ctas_needed);
     if (grid <= 0) return cudaErrorInvalidConfiguration;
     f<<<grid, kFwdThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+int MR_CAT(launch_fwd_hist, MR_SUFFIX)(const RouteArgs& a, int nv_idx, bool select, int R_min, int nchunk_max_pad,
+                                      int E_tot, uint32_t* pre, uint32_t* ctot, int* R_out, int* nchunk_pad_out,
+                                      cudaStream_t st)
+{
+    const bool full = a.vec && a.E == 128 * kNvBuckets[nv_idx];
+    const bool rank3 = full && a.stop > 64;
+    const FwdHistFn f = select ? (rank3 ? fwd_hist_kernel<true, true, 3>(nv_idx)
+                                        : (full ? fwd_hist_kernel<true, true>(nv_idx) : fwd_hist_kernel<true, false>(nv_idx)))
+                               : (full ? fwd_hist_kernel<false, true>(nv_idx) : fwd_hist_kernel<false, false>(nv_idx));
+    if (!f) return cudaErrorInvalidValue;
+    const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, select, a.n_group > 0);
+    const size_t smem = static_cast<size_t>(L.bytes) * (kFwdThreads / 32) + static_cast<size_t>(align16(E_tot * 4));
+    int err = ensure_smem(reinterpret_cast<const void*>(f), smem);
+    if (err != cudaSuccess) return err;
+    // at least R_min rows per CTA, more if the grid would not fit on the GPU at once
+    int R = R_min;
+    const int fit = resident_clusters(reinterpret_cast<const void*>(f), kFwdThreads, smem);
+    if (fit > 0) {
+        const long long ctas = static_cast<long long>(fit) * kClusterChunks;
+        const int r_fit = static_cast<int>((a.T + ctas - 1) / ctas);
+        if (r_fit > R) R = min(r_fit, kSortChunk / a.topk);
+    }
+    const int nchunk = (a.T + R - 1) / R;
+    const int nchunk_pad = (nchunk + kClusterChunks - 1) / kClusterChunks * kClusterChunks;
+    if (nchunk_pad > nchunk_max_pad) return cudaErrorInvalidConfiguration;  // R >= R_min: never
+    f<<<nchunk_pad, kFwdThreads, smem, st>>>(a, R, E_tot, pre, ctot);
+    *R_out = R;
+    *nchunk_pad_out = nchunk_pad;
     return cudaGetLastError();
 }
 

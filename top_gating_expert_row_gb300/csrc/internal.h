@@ -7,13 +7,12 @@
 #include <cuda_runtime.h>
 
 #include "route.cuh"
+#include "sort.cuh"
 
 namespace mr {
 
 constexpr int kFwdThreads = 256;     // 8 warps, one token row per warp at a time
 constexpr int kFusedThreads = 512;   // 16 warps: one per decode token, then the whole CTA sorts
-constexpr int kSortThreads = 512;
-constexpr int kSortChunk = 4096;     // flat (token, slot) pairs per sort CTA
 
 // Register-resident row widths: NV chunks of 128 elements per row (E <= 2304).
 constexpr int kNvBuckets[] = {1, 2, 3, 4, 6, 8, 12, 18};
@@ -104,6 +103,19 @@ int launch_bwd_bf16(int score_fn, int nv_idx, const __nv_bfloat16* g, const floa
 int launch_sort(const int32_t* idx, const float* w, int N, int E_tot, int block_m, int32_t* ids,
                 float* sw, int32_t* eids, int32_t* npp, uint32_t* ws, int32_t* status,
                 cudaStream_t st);
+// The multi-CTA sort's second launch on chunks of PC pairs (nchunk_pad CTAs, a
+// multiple of kClusterChunks) whose within-cluster prefixes and cluster totals
+// are in pre / ctot.
+int launch_sort_scatter(const int32_t* idx, const float* w, int N, int PC, int nchunk_pad, int E_tot, int block_m,
+                        const uint32_t* pre, const uint32_t* ctot, int32_t* ids, float* sw, int32_t* eids,
+                        int32_t* npp, cudaStream_t st);
+// Route + first sort stage in one launch (prefill sizes, E <= 1024): CTA c routes
+// rows [c*R, (c+1)*R) and counts their pairs; the clusters write pre / ctot.
+// R is at least R_min and chosen so that the grid fits on the GPU at once; the
+// rows per CTA and the padded CTA count used are returned.
+int launch_fwd_hist(int score_fn, int in_dtype, const RouteArgs& a, int nv_idx, bool select, int R_min,
+                    int nchunk_max_pad, int E_tot, uint32_t* pre, uint32_t* ctot, int* R_out, int* nchunk_pad_out,
+                    cudaStream_t st);
 int launch_expf(const float* x, float* y, int n, cudaStream_t st);
 int aux_chunks(long long T);
 size_t aux_workspace_bytes(long long T, int E);
@@ -114,7 +126,72 @@ int launch_aux_loss_bwd(const int32_t* tokens_per_expert, const float* grad_loss
 int launch_tokens_per_expert(const uint8_t* map, int T, int E, int32_t* out, cudaStream_t st);
 int launch_noop(cudaStream_t st);
 
-inline int sort_chunks(long long N) { return N <= 0 ? 1 : static_cast<int>((N + kSortChunk - 1) / kSortChunk); }
+// Chunking of the multi-CTA sort: PC pairs per CTA, nchunk CTAs padded to whole
+// clusters. At most kSortChunk pairs take the one-CTA sort. Larger sorts use
+// chunks of about N/256 pairs (1024..4096, multiples of 512) so that the grid
+// spreads over the GPU; with more than 1024 experts the per-CTA cost of the
+// expert-wide steps dominates, so chunks stay at 4096.
+struct SortPlan {
+    int pc, nchunk, nchunk_pad;
+};
+
+inline SortPlan sort_plan(long long N, int E_tot)
+{
+    long long pc = kSortChunk;
+    if (N > kSortChunk && E_tot <= 1024) {
+        pc = ((N + 255) / 256 + 511) / 512 * 512;
+        pc = pc < 1024 ? 1024 : (pc > kSortChunk ? kSortChunk : pc);
+    }
+    SortPlan p;
+    p.pc = static_cast<int>(pc);
+    p.nchunk = N <= 0 ? 1 : static_cast<int>((N + pc - 1) / pc);
+    p.nchunk_pad = (p.nchunk + kClusterChunks - 1) / kClusterChunks * kClusterChunks;
+    return p;
+}
+
+// Workspace of the sort: the per-chunk prefixes and the cluster totals (none for
+// the one-CTA sort).
+inline size_t sort_table_bytes(int nchunk_pad, int E_tot)
+{
+    return (static_cast<size_t>(nchunk_pad) + nchunk_pad / kClusterChunks) * static_cast<size_t>(E_tot) * 4;
+}
+
+inline size_t sort_ws_bytes(long long N, int E_tot)
+{
+    if (N <= kSortChunk) return 0;
+    return sort_table_bytes(sort_plan(N, E_tot).nchunk_pad, E_tot);
+}
+
+// Route CTAs the fused prefill path aims for: this GPU's 152 SMs times the
+// forward's resident CTAs per SM for the row width (a device with fewer SMs
+// runs the same chunks in more waves). R_min rows per CTA, capped so that a
+// chunk holds at most kSortChunk pairs.
+constexpr int kGpuSms = 152;
+// Resident CTAs per SM the forward's register budget is sized for (the row's
+// keys take 4*NV registers per lane).
+constexpr int fwd_min_blocks(int nv) { return nv >= 12 ? 2 : (nv >= 6 ? 3 : 4); }
+
+// Whether the fused call above the one-launch sizes has the route kernel count
+// the sort's chunks (rows held in registers, more pairs than the one-CTA sort
+// takes); otherwise it runs the forward and then moe_sort's launches.
+inline bool fused_counts_in_route(long long N, int nv_bucket) { return N > kSortChunk && nv_bucket <= kRegisterMaxNv; }
+
+struct FusedPlan {
+    int R_min, nchunk_max_pad;
+};
+
+inline FusedPlan fused_plan(int T, int topk, int nv_bucket)
+{
+    const int target = kGpuSms * fwd_min_blocks(nv_bucket);
+    int R = (T + target - 1) / target;
+    const int rmax = kSortChunk / topk;
+    R = R < 1 ? 1 : (R > rmax ? rmax : R);
+    FusedPlan f;
+    f.R_min = R;
+    const int n = (T + R - 1) / R;
+    f.nchunk_max_pad = (n + kClusterChunks - 1) / kClusterChunks * kClusterChunks;
+    return f;
+}
 
 // Persistent-grid size: min(units, SMs x resident CTAs) for a kernel.
 int persistent_grid(const void* func, int threads, size_t smem, long long units);

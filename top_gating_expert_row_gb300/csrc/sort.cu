@@ -1,31 +1,36 @@
-// Multi-CTA MoE sorting (FlyDSL PR 582, moe_sorting; layout as FlyDSL PR 947's
-// grouped GEMMs consume it). Two launches, no grid-wide waiting:
+// MoE sorting (FlyDSL PR 582, moe_sorting; layout as FlyDSL PR 947's grouped
+// GEMMs consume it). No grid-wide waiting anywhere: kernel boundaries and
+// thread-block cluster barriers are the only cross-CTA ordering.
 //
-//   k_sort_hist     CTA c counts the experts of flat pairs [c*4096, (c+1)*4096)
-//                   into ws[c][E_tot] (warp-aggregated shared atomics); ids
-//                   outside [0, E_tot) are dropped and flagged in *status
-//   k_sort_scatter  every CTA reads the whole (chunks x E_tot) count table,
-//                   derives the padded per-expert offsets (block scan) and its
-//                   own start inside each expert's range (counts of the chunks
-//                   before it), scatters its pairs stably, and writes the
-//                   sentinels / expert ids of its share of the experts
+//   k_sort_small    at most kSortChunk pairs: ONE CTA counts, scans, scatters
+//                   and pads (one launch)
+//   k_sort_hist     CTA c counts the experts of flat pairs [c*PC, (c+1)*PC);
+//                   clusters of 8 consecutive chunks turn their counts into
+//                   within-cluster prefixes pre[c][e] and cluster totals
+//                   ctot[g][e] (distributed shared memory); ids outside
+//                   [0, E_tot) are dropped and reported in *status
+//   k_sort_scatter  clusters of 8 again, one CTA per chunk: the cluster's CTAs
+//                   split the experts, sum the totals of the clusters before
+//                   theirs and of all clusters, scan the padded counts (slice
+//                   totals exchanged through distributed shared memory) and
+//                   gather every expert's offset; then each CTA scatters its
+//                   chunk's pairs stably and writes its share of the padded
+//                   blocks' sentinels and expert ids
 //
-// The kernel boundary is the only grid-wide ordering, so nothing spins.
+// Every CTA reads the cluster totals (chunks / 8 rows), never the whole
+// per-chunk table, so the cost grows about linearly with the pairs.
 #include "internal.h"
 #include "sort.cuh"
 
 namespace mr {
 
-__global__ void __launch_bounds__(kSortThreads) k_sort_hist(const int32_t* __restrict__ idx, int N,
-                                                            int E_tot, uint32_t* __restrict__ ws,
-                                                            int32_t* status)
+// Counts the experts of flat pairs [f0, f1) (f1 - f0 <= kSortChunk, at most
+// kSortChunk / kSortThreads per thread) into hist (shared, zeroed); ids outside
+// [0, E_tot) are skipped and reported in *status.
+__device__ __forceinline__ void cta_count(const int32_t* __restrict__ idx, int f0, int f1, int E_tot,
+                                          uint32_t* hist, int32_t* status)
 {
-    extern __shared__ __align__(16) uint32_t hist[];
     const int tid = threadIdx.x, lane = tid & 31;
-    for (int e = tid; e < E_tot; e += blockDim.x) hist[e] = 0u;
-    __syncthreads();
-    const int f0 = blockIdx.x * kSortChunk;
-    const int f1 = min(f0 + kSortChunk, N);
     bool bad = false;
     // every id of this thread loaded first (one memory latency, not one per step)
     constexpr int kSteps = kSortChunk / kSortThreads;
@@ -46,15 +51,13 @@ __global__ void __launch_bounds__(kSortThreads) k_sort_hist(const int32_t* __res
         warp_hist_add(hist, e, lane);
     }
     if (__any_sync(kFull, bad) && lane == 0) report_status(status, kStatusRange);
-    __syncthreads();
-    uint32_t* out = ws + static_cast<size_t>(blockIdx.x) * E_tot;
-    for (int e = tid; e < E_tot; e += blockDim.x) out[e] = hist[e];
 }
 
-__global__ void __launch_bounds__(kSortThreads) k_sort_scatter(
-    const int32_t* __restrict__ idx, const float* __restrict__ w, int N, int E_tot, int bm, int nchunk,
-    const uint32_t* __restrict__ ws, int32_t* __restrict__ ids, float* __restrict__ sw,
-    int32_t* __restrict__ eids, int32_t* __restrict__ npp)
+__global__ void __launch_bounds__(kSortThreads) k_sort_small(const int32_t* __restrict__ idx,
+                                                             const float* __restrict__ w, int N, int E_tot, int bm,
+                                                             int32_t* __restrict__ ids, float* __restrict__ sw,
+                                                             int32_t* __restrict__ eids, int32_t* __restrict__ npp,
+                                                             int32_t* status)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     unsigned char* p = smem;
@@ -63,53 +66,208 @@ __global__ void __launch_bounds__(kSortThreads) k_sort_scatter(
     uint32_t* base = reinterpret_cast<uint32_t*>(p); p += align16(E_tot * 4);
     uint32_t* tmp = reinterpret_cast<uint32_t*>(p); p += align16(33 * 4);
     uint16_t* wh = reinterpret_cast<uint16_t*>(p);
-    const int tid = threadIdx.x, c = blockIdx.x;
-
-    for (int e = tid; e < E_tot; e += blockDim.x) {
-        uint32_t before = 0u, total = 0u;
-#pragma unroll 8
-        for (int q = 0; q < nchunk; ++q) {
-            const uint32_t v = __ldg(ws + static_cast<size_t>(q) * E_tot + e);
-            before += (q < c) ? v : 0u;
-            total += v;
-        }
-        cnt[e] = total;
-        base[e] = before;
-        off[e] = (total + bm - 1) / bm * bm;
-    }
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E_tot; e += blockDim.x) cnt[e] = 0u;
+    __syncthreads();
+    cta_count(idx, 0, N, E_tot, cnt, status);
+    __syncthreads();
+    for (int e = tid; e < E_tot; e += blockDim.x) off[e] = (cnt[e] + bm - 1) / bm * bm;
     __syncthreads();
     const uint32_t P = cta_exclusive_scan(off, E_tot, tmp);
-    if (tid == 0) off[E_tot] = P;
-    for (int e = tid; e < E_tot; e += blockDim.x) base[e] += off[e];
-    if (c == 0 && tid == 0) *npp = static_cast<int32_t>(P);
+    if (tid == 0) {
+        off[E_tot] = P;
+        *npp = static_cast<int32_t>(P);
+    }
+    for (int e = tid; e < E_tot; e += blockDim.x) base[e] = off[e];
     __syncthreads();
-    const int f0 = c * kSortChunk;
-    const int f1 = min(f0 + kSortChunk, N);
-    cta_scatter(idx, w, f0, f1, E_tot, base, wh, ids, sw);
-    // this CTA's share of the experts' padding and block ids
-    const int share = (E_tot + nchunk - 1) / nchunk;
-    const int e0 = min(E_tot, c * share);
-    const int e1 = min(E_tot, e0 + share);
-    cta_fill_pads(off, cnt, e0, e1, bm, N, ids, sw, eids);
+    if (N > 0) cta_scatter(idx, w, 0, N, E_tot, base, wh, ids, sw);
+    cta_fill_pad_blocks(off, cnt, E_tot, 0, static_cast<int>(P) / bm, bm, N, ids, sw, eids);
+}
+
+__global__ void __cluster_dims__(kClusterChunks, 1, 1) __launch_bounds__(kSortThreads)
+    k_sort_hist(const int32_t* __restrict__ idx, int N, int PC, int E_tot, uint32_t* __restrict__ pre,
+                uint32_t* __restrict__ ctot, int32_t* status)
+{
+    extern __shared__ __align__(16) uint32_t hist[];
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E_tot; e += blockDim.x) hist[e] = 0u;
+    __syncthreads();
+    const long long f0l = static_cast<long long>(blockIdx.x) * PC;
+    const int f0 = static_cast<int>(f0l < N ? f0l : N);
+    const int f1 = min(f0 + PC, N);
+    if (f0 < f1) cta_count(idx, f0, f1, E_tot, hist, status);
+    __syncthreads();
+    cluster_prefix_counts(hist, E_tot, pre, ctot);
+}
+
+// Shared memory of k_sort_scatter: the CTA's expert slice (S = ceil(E_tot/8)
+// entries each) and the gathered per-expert arrays.
+struct ScatterLayout {
+    int s_bsum, s_tot, s_off, s_slice, tmp, base, off, cnt, wh, bytes;
+};
+
+__host__ __device__ inline ScatterLayout scatter_layout(int E_tot, int threads)
+{
+    const int S = (E_tot + kClusterChunks - 1) / kClusterChunks;
+    ScatterLayout L;
+    int o = 0;
+    L.s_bsum = o; o += align16(S * 4);
+    L.s_tot = o; o += align16(S * 4);
+    L.s_off = o; o += align16(S * 4);
+    L.s_slice = o; o += 16;
+    L.tmp = o; o += align16(33 * 4);
+    L.base = o; o += align16(E_tot * 4);
+    L.off = o; o += align16((E_tot + 1) * 4);
+    L.cnt = o; o += align16(E_tot * 4);
+    L.wh = o; o += align16((threads / 32) * E_tot * 2);
+    L.bytes = o;
+    return L;
+}
+
+__global__ void __cluster_dims__(kClusterChunks, 1, 1) __launch_bounds__(kSortThreads)
+    k_sort_scatter(const int32_t* __restrict__ idx, const float* __restrict__ w, int N, int PC, int E_tot, int bm,
+                   int ncl, const uint32_t* __restrict__ pre, const uint32_t* __restrict__ ctot,
+                   int32_t* __restrict__ ids, float* __restrict__ sw, int32_t* __restrict__ eids,
+                   int32_t* __restrict__ npp)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    const ScatterLayout L = scatter_layout(E_tot, blockDim.x);
+    uint32_t* s_bsum = reinterpret_cast<uint32_t*>(smem + L.s_bsum);
+    uint32_t* s_tot = reinterpret_cast<uint32_t*>(smem + L.s_tot);
+    uint32_t* s_off = reinterpret_cast<uint32_t*>(smem + L.s_off);
+    uint32_t* s_slice = reinterpret_cast<uint32_t*>(smem + L.s_slice);
+    uint32_t* tmp = reinterpret_cast<uint32_t*>(smem + L.tmp);
+    uint32_t* base = reinterpret_cast<uint32_t*>(smem + L.base);
+    uint32_t* off = reinterpret_cast<uint32_t*>(smem + L.off);
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + L.cnt);
+    uint16_t* wh = reinterpret_cast<uint16_t*>(smem + L.wh);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    const int c = blockIdx.x;
+    const int g = c / kClusterChunks;
+    const uint32_t r = cluster_ctarank();
+    const int S = (E_tot + kClusterChunks - 1) / kClusterChunks;
+    const int e0 = min(E_tot, static_cast<int>(r) * S), len = min(E_tot, e0 + S) - e0;
+
+    // 1. for the CTA's expert slice: pairs in the clusters before this one and
+    //    in all clusters. Lanes take 32 consecutive experts (coalesced rows of
+    //    ctot), the warps split the clusters between them.
+    for (int i = tid; i < len; i += blockDim.x) {
+        s_bsum[i] = 0u;
+        s_tot[i] = 0u;
+    }
+    __syncthreads();
+    {
+        const int nblk = (len + 31) / 32;
+        const int parts = max(1, nw / max(1, nblk));
+        const int per = (ncl + parts - 1) / parts;
+        for (int task = warp; task < nblk * parts; task += nw) {
+            const int eb = task % nblk, part = task / nblk;
+            const int i = eb * 32 + lane;
+            const int q0 = part * per, q1 = min(ncl, q0 + per);
+            uint32_t before = 0u, total = 0u;
+            if (i < len) {
+#pragma unroll 4
+                for (int q = q0; q < q1; ++q) {
+                    const uint32_t v = __ldg(ctot + static_cast<size_t>(q) * E_tot + e0 + i);
+                    before += q < g ? v : 0u;
+                    total += v;
+                }
+                if (total) {
+                    atomicAdd(s_bsum + i, before);
+                    atomicAdd(s_tot + i, total);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    // 2. padded counts of the slice, scanned within the slice
+    for (int i = tid; i < len; i += blockDim.x) s_off[i] = (s_tot[i] + bm - 1) / bm * bm;
+    __syncthreads();
+    const uint32_t P = cta_exclusive_scan(s_off, len, tmp);
+    if (tid == 0) s_slice[0] = P;
+    cluster_sync();
+    // 3. the slice's start from the other slices' totals; this cluster's base
+    //    for each expert of the slice
+    uint32_t soff = 0u, all = 0u;
+#pragma unroll
+    for (int q = 0; q < kClusterChunks; ++q) {
+        const uint32_t t = ld_shared_cluster(map_shared_rank(s_slice, static_cast<uint32_t>(q)));
+        soff += static_cast<uint32_t>(q) < r ? t : 0u;
+        all += t;
+    }
+    for (int i = tid; i < len; i += blockDim.x) {
+        s_off[i] += soff;
+        s_bsum[i] += s_off[i];
+    }
+    cluster_sync();
+    // 4. every expert's offset, count and base from its slice's CTA, plus this
+    //    chunk's prefix inside the cluster
+    {
+        const uint32_t* prow = pre + static_cast<size_t>(c) * E_tot;
+        for (int e = tid; e < E_tot; e += blockDim.x) {
+            const uint32_t q = static_cast<uint32_t>(e / S);
+            const uint32_t i4 = 4u * static_cast<uint32_t>(e - static_cast<int>(q) * S);
+            base[e] = ld_shared_cluster(map_shared_rank(s_bsum, q) + i4) + __ldg(prow + e);
+            off[e] = ld_shared_cluster(map_shared_rank(s_off, q) + i4);
+            cnt[e] = ld_shared_cluster(map_shared_rank(s_tot, q) + i4);
+        }
+        if (tid == 0) off[E_tot] = all;
+    }
+    cluster_sync();  // no CTA reads another CTA's shared memory after this point
+    if (c == 0 && tid == 0) *npp = static_cast<int32_t>(all);
+    // 5. this chunk's pairs
+    const long long f0l = static_cast<long long>(c) * PC;
+    const int f0 = static_cast<int>(f0l < N ? f0l : N);
+    const int f1 = min(f0 + PC, N);
+    if (f0 < f1) cta_scatter(idx, w, f0, f1, E_tot, base, wh, ids, sw);
+    // 6. the CTA's share of the padded blocks
+    const long long nb = all / static_cast<uint32_t>(bm);
+    const int G = gridDim.x;
+    const int b0 = static_cast<int>(nb * c / G), b1 = static_cast<int>(nb * (c + 1) / G);
+    cta_fill_pad_blocks(off, cnt, E_tot, b0, b1, bm, N, ids, sw, eids);
+}
+
+size_t scatter_smem_bytes(int E_tot) { return static_cast<size_t>(scatter_layout(E_tot, kSortThreads).bytes); }
+
+size_t small_sort_smem_bytes(int E_tot)
+{
+    return static_cast<size_t>(align16(E_tot * 4)) * 2 + align16((E_tot + 1) * 4) + align16(33 * 4) +
+           align16((kSortThreads / 32) * E_tot * 2);
+}
+
+int launch_sort_scatter(const int32_t* idx, const float* w, int N, int PC, int nchunk_pad, int E_tot, int block_m,
+                        const uint32_t* pre, const uint32_t* ctot, int32_t* ids, float* sw, int32_t* eids,
+                        int32_t* npp, cudaStream_t st)
+{
+    const size_t smem = scatter_smem_bytes(E_tot);
+    int err = ensure_smem(reinterpret_cast<const void*>(k_sort_scatter), smem);
+    if (err != cudaSuccess) return err;
+    k_sort_scatter<<<nchunk_pad, kSortThreads, smem, st>>>(idx, w, N, PC, E_tot, block_m, nchunk_pad / kClusterChunks,
+                                                          pre, ctot, ids, sw, eids, npp);
+    return cudaGetLastError();
 }
 
 int launch_sort(const int32_t* idx, const float* w, int N, int E_tot, int block_m, int32_t* ids, float* sw,
                 int32_t* eids, int32_t* npp, uint32_t* ws, int32_t* status, cudaStream_t st)
 {
-    const int nchunk = sort_chunks(N);
+    if (N <= kSortChunk) {
+        const size_t smem = small_sort_smem_bytes(E_tot);
+        int err = ensure_smem(reinterpret_cast<const void*>(k_sort_small), smem);
+        if (err != cudaSuccess) return err;
+        k_sort_small<<<1, kSortThreads, smem, st>>>(idx, w, N, E_tot, block_m, ids, sw, eids, npp, status);
+        return cudaGetLastError();
+    }
+    const SortPlan plan = sort_plan(N, E_tot);
+    uint32_t* pre = ws;
+    uint32_t* ctot = ws + static_cast<size_t>(plan.nchunk_pad) * E_tot;
     const size_t smem_h = static_cast<size_t>(E_tot) * 4;
     int err = ensure_smem(reinterpret_cast<const void*>(k_sort_hist), smem_h);
     if (err != cudaSuccess) return err;
-    k_sort_hist<<<nchunk, kSortThreads, smem_h, st>>>(idx, N, E_tot, ws, status);
+    k_sort_hist<<<plan.nchunk_pad, kSortThreads, smem_h, st>>>(idx, N, plan.pc, E_tot, pre, ctot, status);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    const size_t smem_s = static_cast<size_t>(align16(E_tot * 4)) * 2 + align16((E_tot + 1) * 4) +
-                          align16(33 * 4) + align16((kSortThreads / 32) * E_tot * 2);
-    err = ensure_smem(reinterpret_cast<const void*>(k_sort_scatter), smem_s);
-    if (err != cudaSuccess) return err;
-    k_sort_scatter<<<nchunk, kSortThreads, smem_s, st>>>(idx, w, N, E_tot, block_m, nchunk, ws, ids, sw,
-                                                         eids, npp);
-    return cudaGetLastError();
+    return launch_sort_scatter(idx, w, N, plan.pc, plan.nchunk_pad, E_tot, block_m, pre, ctot, ids, sw, eids, npp,
+                               st);
 }
 
 }  // namespace mr

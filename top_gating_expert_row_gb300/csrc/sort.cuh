@@ -1,24 +1,32 @@
-// CTA-level building blocks of the MoE sorting step (FlyDSL PR 582,
-// moe_sorting: bucket every (token, slot) pair by expert into block_m-padded
-// blocks; the padded layout is the one FlyDSL PR 947's grouped GEMMs consume,
-// where id = token*topk + slot and a sentinel past the last row contributes 0).
+// CTA- and cluster-level building blocks of the MoE sorting step (FlyDSL PR
+// 582, moe_sorting: bucket every (token, slot) pair by expert into
+// block_m-padded blocks; the padded layout is the one FlyDSL PR 947's grouped
+// GEMMs consume, where id = token*topk + slot and a sentinel past the last row
+// contributes 0).
 //
 //   histogram  warp-aggregated shared-memory counts: lanes holding the same
 //              expert id find each other with __match_any_sync and one leader
 //              adds the group's size
-//   scan       padded counts -> exclusive offsets (block scan over E_tot)
+//   cluster    the counts of 8 consecutive chunks (one thread-block cluster)
+//   prefix     become within-cluster exclusive prefixes and a cluster total,
+//              the CTAs splitting the experts and reading each other's counts
+//              through distributed shared memory
+//   scan       padded counts -> exclusive offsets (block scan over experts)
 //   scatter    stable: each warp owns a contiguous run of flat ids; per-warp
 //              per-expert counts give each warp its start inside the expert's
 //              range, and within a 32-entry step a pair's rank is the number of
 //              lower lanes holding the same expert
-//   pads       every padded position past an expert's pairs gets the sentinel,
-//              every block of an expert's range its id (a thread per expert)
+//   pads       a warp per block of block_m positions: the block's expert by a
+//              binary search over the offsets, the sentinel at every position
+//              past the expert's pairs, and the block's expert id
 #pragma once
 
 #include "common.cuh"
 
 namespace mr {
 
+constexpr int kSortThreads = 512;
+constexpr int kSortChunk = 4096;  // flat (token, slot) pairs per sort CTA, at most
 constexpr int kInvalidExpert = -1;
 
 // Warp-aggregated increment of hist[e] for each lane's expert e (lanes with
@@ -130,20 +138,70 @@ __device__ inline void cta_scatter(const int32_t* idx, const float* w, int f0, i
     }
 }
 
-// Sentinels and expert ids of experts [e0, e1), one thread per expert: the
-// padded tail of the expert's range, [off[e] + cnt[e], off[e+1]), gets the
-// sentinel (weight 0) and each block of the range gets the expert's id. off:
-// E_tot+1 exclusive offsets (multiples of bm), cnt: pairs per expert.
-__device__ inline void cta_fill_pads(const uint32_t* off, const uint32_t* cnt, int e0, int e1, int bm,
-                                     int32_t sentinel, int32_t* out_ids, float* out_w, int32_t* expert_ids)
+// Chunks of flat pairs per thread-block cluster of the sort (and of the route
+// kernel that feeds it).
+constexpr int kClusterChunks = 8;
+
+// Called by every thread of every CTA of a cluster of kClusterChunks CTAs
+// (blockIdx.x / kClusterChunks = cluster g, rank q = chunk g*8 + q), each with
+// its chunk's per-expert counts in hist[0..E_tot) (shared). Writes
+//   pre[(g*8 + q)*E_tot + e] = sum of the counts of chunks g*8 .. g*8+q-1
+//   ctot[g*E_tot + e]        = sum of the counts of the cluster's 8 chunks
+// The experts are split over the cluster's CTAs; the other CTAs' counts are
+// read through distributed shared memory. Starts and ends with a cluster
+// barrier, so no CTA leaves while its counts may still be read.
+__device__ inline void cluster_prefix_counts(const uint32_t* hist, int E_tot, uint32_t* pre, uint32_t* ctot)
 {
+    cluster_sync();
+    const uint32_t r = cluster_ctarank();
+    const size_t g = blockIdx.x / kClusterChunks;
+    const int S = (E_tot + kClusterChunks - 1) / kClusterChunks;
+    const int e0 = static_cast<int>(r) * S, e1 = min(E_tot, e0 + S);
+    uint32_t remote[kClusterChunks];
+#pragma unroll
+    for (int q = 0; q < kClusterChunks; ++q) remote[q] = map_shared_rank(hist, static_cast<uint32_t>(q));
     for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += blockDim.x) {
-        const uint32_t a = off[e], b = off[e + 1];
-        for (uint32_t p = a + cnt[e]; p < b; ++p) {
-            out_ids[p] = sentinel;
-            if (out_w) out_w[p] = 0.0f;
+        uint32_t v[kClusterChunks];
+#pragma unroll
+        for (int q = 0; q < kClusterChunks; ++q) v[q] = ld_shared_cluster(remote[q] + 4u * e);
+        uint32_t run = 0u;
+#pragma unroll
+        for (int q = 0; q < kClusterChunks; ++q) {
+            pre[(g * kClusterChunks + q) * E_tot + e] = run;
+            run += v[q];
         }
-        for (uint32_t blk = a / bm; blk < b / bm; ++blk) expert_ids[blk] = e;
+        ctot[g * E_tot + e] = run;
+    }
+    cluster_sync();
+}
+
+// Sentinels and expert ids of blocks [b0, b1) of the padded layout, a warp
+// per block. off: E_tot+1 exclusive offsets (multiples of bm, off[E_tot] the
+// padded total), cnt: pairs per expert (both shared). A block's expert is the
+// last e with off[e] <= its first position (an empty expert's range is empty,
+// so the search skips it); the block's positions past the expert's pairs get
+// the sentinel (weight 0).
+__device__ inline void cta_fill_pad_blocks(const uint32_t* off, const uint32_t* cnt, int E_tot, int b0, int b1,
+                                           int bm, int32_t sentinel, int32_t* out_ids, float* out_w,
+                                           int32_t* expert_ids)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int b = b0 + warp; b < b1; b += nw) {
+        const uint32_t p0 = static_cast<uint32_t>(b) * static_cast<uint32_t>(bm);
+        int lo = 0, hi = E_tot;  // off[lo] <= p0 < off[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (off[mid] <= p0) lo = mid;
+            else hi = mid;
+        }
+        const uint32_t filled = cnt[lo] > p0 - off[lo] ? cnt[lo] - (p0 - off[lo]) : 0u;  // real pairs in the block
+        for (int r = lane; r < bm; r += 32) {
+            if (static_cast<uint32_t>(r) >= filled) {
+                out_ids[p0 + r] = sentinel;
+                if (out_w) out_w[p0 + r] = 0.0f;
+            }
+        }
+        if (lane == 0) expert_ids[b] = lo;
     }
 }
 
