@@ -257,7 +257,8 @@ def time_kernels(mr, w, dev, stream, calls=20, replays=5) -> dict:
     fn_name = "softmax" if w.score_fn == synth.SOFTMAX else "sigmoid"
     for name, nb in step_bytes(w).items():
         it = iter(range(10 ** 9))
-        us = graph_us(lambda: sets[next(it) % len(sets)][name](), stream, calls, replays)
+        with plain_order(mr):
+            us = graph_us(lambda: sets[next(it) % len(sets)][name](), stream, calls, replays)
         gbs = nb / (us * 1e-6) / 1e9
         d = {"us": round(us, 2), "GB/s": round(gbs, 1)}
         page = PAGE_B300.get((name, fn_name, w.E, w.topk))
@@ -298,7 +299,8 @@ def bf16_rates(mr, dev, stream, calls=20, replays=5) -> dict:
     out = {"workload": w.name, "timing": f"CUDA graph, {calls} calls per replay over {len(sets)} buffer sets"}
     for name, nb in nbytes.items():
         it = iter(range(10 ** 9))
-        us = graph_us(lambda: sets[next(it) % len(sets)][name](), stream, calls, replays)
+        with plain_order(mr):
+            us = graph_us(lambda: sets[next(it) % len(sets)][name](), stream, calls, replays)
         gbs = nb / (us * 1e-6) / 1e9
         out[name] = {"us": round(us, 2), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / pk, 3)}
     return out
@@ -356,6 +358,11 @@ def decode_latency(mr, dev, stream, n_calls=200, Ts=synth.DECODE_TS, shape=synth
 
     noop = lambda st: L.moe_router_noop(st)  # noqa: E731
     floor = {"eager_us": round(eager(noop), 2), "graph_us": round(graph(noop), 2)}
+    mr.moe_router_set_launch_overlap(False)
+    try:
+        floor["graph_plain_us"] = round(graph(noop), 2)
+    finally:
+        mr.moe_router_set_launch_overlap(True)
     res["launch_floor"] = floor
     for T in Ts:
         w = shape(T)
@@ -379,11 +386,35 @@ def decode_latency(mr, dev, stream, n_calls=200, Ts=synth.DECODE_TS, shape=synth
 
         fe, fg = eager(fused), graph(fused)
         ue, ug = eager(unfused), graph(unfused)
+        # the same calls launched in plain stream order (no launch overlap)
+        mr.moe_router_set_launch_overlap(False)
+        try:
+            fgp, ugp = graph(fused), graph(unfused)
+        finally:
+            mr.moe_router_set_launch_overlap(True)
         res[f"T={T}"] = {"fused_eager_us": round(fe, 2), "fused_graph_us": round(fg, 2),
                          "unfused_eager_us": round(ue, 2), "unfused_graph_us": round(ug, 2),
+                         "fused_graph_plain_us": round(fgp, 2), "unfused_graph_plain_us": round(ugp, 2),
                          "fused_graph_minus_floor_us": round(fg - floor["graph_us"], 2),
                          "fused_eager_minus_floor_us": round(fe - floor["eager_us"], 2)}
+    res["note"] = ("graph_us: CUDA-graph replays with the launch overlap on (each call may start while the one "
+                   "before it finishes); graph_plain_us: plain stream order; the floor is the empty kernel "
+                   "launched the same way")
     return res
+
+
+class plain_order:
+    """Within this block the library launches in plain stream order (no launch
+    overlap), so back-to-back calls of one kernel are timed one after another."""
+
+    def __init__(self, mr):
+        self.mr = mr
+
+    def __enter__(self):
+        self.mr.moe_router_set_launch_overlap(False)
+
+    def __exit__(self, *exc):
+        self.mr.moe_router_set_launch_overlap(True)
 
 
 def graph_us(fn, stream, calls=20, replays=5) -> float:
@@ -443,13 +474,16 @@ def prefill_route_sort(mr, dev, stream, reps=20) -> dict:
     r_us = graph_us(route, stream, reps)
     s_us = graph_us(srt, stream, reps)
     f_us = graph_us(fused, stream, reps)
+    with plain_order(mr):
+        f_plain = graph_us(fused, stream, reps)
     rb = w.T * w.E * 2 + w.T * w.topk * 8 + w.E * 4
     npp = int(bufs["num_tokens_post_pad"].item())
     sb = w.T * w.topk * 8 + npp * 8 + (npp // w.block_m) * 4 + 4
     return {"workload": w.name, "route_us": round(r_us, 2), "sort_us": round(s_us, 2),
             "route_GB/s": round(rb / (r_us * 1e-6) / 1e9, 1), "sort_GB/s": round(sb / (s_us * 1e-6) / 1e9, 1),
             "route_plus_sort_us": round(r_us + s_us, 2), "fused_us": round(f_us, 2),
-            "fused_launches": "route counting the sort's chunks + scatter", "num_tokens_post_pad": npp,
+            "fused_plain_us": round(f_plain, 2),
+            "fused_launches": "route, then moe_sort's launches", "num_tokens_post_pad": npp,
             "timing": "CUDA graph, 20 calls per replay"}
 
 
@@ -482,7 +516,9 @@ def sort_scaling(mr, dev, stream, reps=20, shapes=SORT_SCALING) -> dict:
                 call()
         torch.cuda.synchronize()
         us = graph_us(call, stream, reps)
-        out[f"T={T} k={k} E_tot={E_tot} bm={bm}"] = {"pairs": T * k, "us": round(us, 2),
+        with plain_order(mr):
+            us_plain = graph_us(call, stream, reps)
+        out[f"T={T} k={k} E_tot={E_tot} bm={bm}"] = {"pairs": T * k, "us": round(us, 2), "plain_us": round(us_plain, 2),
                                                       "ns_per_kpair": round(us * 1e6 / (T * k), 1)}
     return out
 
@@ -500,14 +536,17 @@ def summary(line) -> dict:
         out[short] = [round(d[kd]["GB/s"] / pk, 2) for kd in ("fwd", "bwd", "aux_fwd", "aux_bwd") if kd in d]
     dec = line.get("decode")
     if dec:
-        out["decode_floor_us"] = [dec["launch_floor"]["graph_us"], dec["launch_floor"]["eager_us"]]
-        out["decode_us[fg,fe,ug,ue]"] = {
-            t.split("=")[1]: [dec[t]["fused_graph_us"], dec[t]["fused_eager_us"], dec[t]["unfused_graph_us"],
+        fl = dec["launch_floor"]
+        out["decode_floor_us[g,g_plain,e]"] = [fl["graph_us"], fl.get("graph_plain_us"), fl["eager_us"]]
+        out["decode_us[fg,fg_plain,fe,ug,ug_plain,ue]"] = {
+            t.split("=")[1]: [dec[t]["fused_graph_us"], dec[t].get("fused_graph_plain_us"), dec[t]["fused_eager_us"],
+                              dec[t]["unfused_graph_us"], dec[t].get("unfused_graph_plain_us"),
                               dec[t]["unfused_eager_us"]]
             for t in dec if t.startswith("T=") and int(t.split("=")[1]) <= 16}
     pf = line.get("prefill_route_sort")
     if pf:
-        out["prefill_us[route,sort,fused]"] = [pf["route_us"], pf["sort_us"], pf["fused_us"]]
+        out["prefill_us[route,sort,fused,fused_plain]"] = [pf["route_us"], pf["sort_us"], pf["fused_us"],
+                                                           pf["fused_plain_us"]]
     ss = line.get("sort_scaling")
     if ss:
         out["sort_us_by_pairs"] = {v["pairs"]: v["us"] for k, v in ss.items() if isinstance(v, dict)}
@@ -545,7 +584,8 @@ def aux_loss_rates(mr, w, dev, stream, reps=50) -> dict:
     pk = peaks()["hbm_gbs"]
     out = {"workload": f"T={T} E={E} topk={k} aux scores of the step", "timing": "CUDA graph, 20 calls per replay"}
     for n, fn in calls.items():
-        us = graph_us(fn, stream, 20, max(1, reps // 10))
+        with plain_order(mr):
+            us = graph_us(fn, stream, 20, max(1, reps // 10))
         gbs = nbytes[n] / (us * 1e-6) / 1e9
         out[n] = {"us": round(us, 2), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / pk, 3)}
     return out

@@ -307,6 +307,18 @@ int moe_router_set_topk_path(int select_threshold, int force_path);
 int moe_router_device_status(int32_t* out, int clear, mr_stream_t stream);
 
 /*
+ * Launch overlap (programmatic dependent launch). enable = 1 (the default; the
+ * environment variable MR_LAUNCH_OVERLAP=0 starts the process with it off):
+ * every kernel of the library is launched so that it may start while the
+ * previous kernel in the stream is still running; it does only its own set-up
+ * (shared memory, barriers) and then waits for that kernel to complete before
+ * it touches global memory, so results and stream order are unchanged and only
+ * the launch latency is hidden. enable = 0: plain stream order. Process-wide,
+ * read by every later launch. Returns MR_EINVAL for another value.
+ */
+int moe_router_set_launch_overlap(int enable);
+
+/*
  * Test hook for the bounded waits ([TE] "Hardening": device-side guards report
  * instead of trapping). tries: attempts of about a microsecond each before a wait of
  * the staged wide-row forward gives up (0 restores the default of 2^20, about a

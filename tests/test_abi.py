@@ -175,6 +175,13 @@ def test_noalloc_scratch_size_matches_the_header(lib):
     assert lib.moe_sort_noalloc_scratch_bytes() == int(m.group(1)) << int(m.group(2))
 
 
+def test_set_launch_overlap(lib):
+    assert lib._lib.moe_router_set_launch_overlap(2) == lib.MR_EINVAL
+    assert lib._lib.moe_router_set_launch_overlap(-1) == lib.MR_EINVAL
+    assert lib._lib.moe_router_set_launch_overlap(0) == lib.MR_OK
+    assert lib._lib.moe_router_set_launch_overlap(1) == lib.MR_OK
+
+
 def test_set_wait_test(lib):
     assert lib._lib.moe_router_set_wait_test(4, 2) == lib.MR_EINVAL
     assert lib._lib.moe_router_set_wait_test(4, -1) == lib.MR_EINVAL

@@ -77,8 +77,9 @@ def check_fwd(out, ref, w, rows=None, what=""):
         t = t if rows is None else t[torch.as_tensor(rows, device=t.device)]
         return t
 
-    assert_equal(sel(out["topk_idx"]), ref["topk_idx"], f"{what} topk_idx")
-    assert_close(sel(out["topk_w"]), ref["topk_w"], f"{what} topk_w")
+    if "topk_idx" in out:
+        assert_equal(sel(out["topk_idx"]), ref["topk_idx"], f"{what} topk_idx")
+        assert_close(sel(out["topk_w"]), ref["topk_w"], f"{what} topk_w")
     if "routing_map" in out:
         assert_equal(sel(out["routing_map"]), ref["routing_map"], f"{what} routing_map")
         assert_close(sel(out["intermediate"]), ref["intermediate"], f"{what} intermediate")
@@ -88,14 +89,15 @@ def check_fwd(out, ref, w, rows=None, what=""):
             assert_close(sel(out["probs"]), ref["probs"], f"{what} probs")
 
 
+@pytest.mark.parametrize("compact", [True, False], ids=["compact", "dense_only"])
 @pytest.mark.parametrize("path", [ARGMAX, SELECT], ids=["argmax", "select"])
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
-def test_fwd_matches_oracle(mr, orc, w, path):
+def test_fwd_matches_oracle(mr, orc, w, path, compact):
     x, b, xg, bg = gpu_inputs(w)
-    out = gpu_route(mr, w, xg, bg, path)
+    out = gpu_route(mr, w, xg, bg, path, compact=compact)
     torch.cuda.synchronize()
     check_fwd(out, oracle_route(orc, w, x, b), w, what=w.name)
-    if w.n_group == 0 and path == ARGMAX:
+    if w.n_group == 0 and path == ARGMAX and compact:
         note_near_ties(orc, w.name, x, w.topk - w.n_shared, w.score_fn, b)
 
 
@@ -117,16 +119,18 @@ def _tie_logits(kind, T, E):
     raise ValueError(kind)
 
 
+@pytest.mark.parametrize("compact", [True, False], ids=["compact", "dense_only"])
 @pytest.mark.parametrize("path", [ARGMAX, SELECT], ids=["argmax", "select"])
 @pytest.mark.parametrize("kind", ["integers", "all_equal", "signed_zeros", "saturated_sigmoid", "two_values"])
 @pytest.mark.parametrize("E,k,fn,T", [(512, 36, SM, 96), (256, 8, SG, 96), (2304, 36, SG, 96), (64, 3, SM, 96),
                                        (2304, 36, SM, 3500)])
-def test_ties_go_to_lower_index(mr, orc, kind, E, k, fn, T, path):
-    # T=3500 gives every CTA of the persistent softmax wide-row grid several rows
+def test_ties_go_to_lower_index(mr, orc, kind, E, k, fn, T, path, compact):
+    # T=3500 gives every CTA of the persistent softmax wide-row grid several rows;
+    # dense_only takes the set-only selection (no candidate rank)
     w = W(f"ties_{kind}", T, E, k, fn, renorm=1)
     x = _tie_logits(kind, w.T, E)
     xg = x.cuda()
-    out = gpu_route(mr, w, xg, None, path)
+    out = gpu_route(mr, w, xg, None, path, compact=compact)
     torch.cuda.synchronize()
     check_fwd(out, oracle_route(orc, w, x, None), w, what=f"{kind}")
 
@@ -156,9 +160,10 @@ def test_full_size_sampled_rows(mr, orc, w):
         assert torch.equal(m, out["routing_map"])
 
 
+@pytest.mark.parametrize("compact", [True, False], ids=["compact", "dense_only"])
 @pytest.mark.parametrize("path", [ARGMAX, SELECT], ids=["argmax", "select"])
 @pytest.mark.parametrize("E,k,fn", [(512, 36, SM), (512, 22, SG), (2304, 36, SM), (384, 8, SG)])
-def test_rows_of_varying_scale_every_row(mr, orc, E, k, fn, path):
+def test_rows_of_varying_scale_every_row(mr, orc, E, k, fn, path, compact):
     """Many rows per warp (T=8192 on the persistent grid), with per-row scales from
     1e-3 to 1e2, shifts and occasional constant rows, so the threshold a warp carries
     from one row to the next is often wrong; every row is checked."""
@@ -171,10 +176,10 @@ def test_rows_of_varying_scale_every_row(mr, orc, E, k, fn, path):
     x[::97] = 0.25  # constant rows: all ties
     x = x.contiguous()
     w = W("varying", T, E, k, fn, renorm=1)
-    out = gpu_route(mr, w, x.cuda(), None, path)
+    out = gpu_route(mr, w, x.cuda(), None, path, compact=compact)
     torch.cuda.synchronize()
     check_fwd(out, oracle_route(orc, w, x, None), w, what=f"varying E={E} k={k}")
-    if path == ARGMAX:
+    if path == ARGMAX and compact:
         note_near_ties(orc, f"varying scale E={E} k={k} fn={fn}", x, k, fn)
 
 
@@ -299,3 +304,20 @@ def test_device_exp_matches_its_specification_bit_for_bit(mr, orc):
     fin = np.isfinite(cuda_exp) & (np.abs(cuda_exp) >= np.finfo(np.float32).tiny)
     ulp = np.spacing(cuda_exp[fin].astype(np.float32)).astype(np.float64)
     assert np.max(np.abs(yc[fin].astype(np.float64) - cuda_exp[fin]) / ulp) <= 2.0
+
+
+@pytest.mark.parametrize("w", [synth.large_softmax(36), synth.large_softmax(8), synth.large_e_softmax(),
+                               synth.large_e_sigmoid()], ids=lambda w: w.name)
+def test_aux_scores_full_size_sampled_rows(mr, orc, w):
+    """The aux-scores forward at the benchmark's full sizes (its selection runs as a
+    set, with no candidate rank): 2048 sampled rows against the oracle, and the
+    map's row sums over every row."""
+    x, _, xg, _ = gpu_inputs(w)
+    out = mr.aux_scores(xg, w.topk, w.score_fn)
+    torch.cuda.synchronize()
+    rows = sample_rows(w.T, 2048)
+    ref = orc.aux_scores_fwd(x.float().numpy()[rows], w.topk, w.score_fn)
+    r = torch.as_tensor(rows, device="cuda")
+    assert_equal(out["routing_map"][r], ref["routing_map"], f"{w.name} aux routing_map")
+    assert_close(out["scores"][r], ref["scores"], f"{w.name} aux scores")
+    assert bool((out["routing_map"].sum(dim=1, dtype=torch.int32) == w.topk).all())

@@ -10,14 +10,18 @@ from parity import assert_close, assert_equal
 pytestmark = pytest.mark.gpu
 
 
-# One CTA up to 4096 pairs; above that chunks of 1024..4096 pairs in clusters of
-# 8 (a partial last cluster, fewer experts than a cluster has CTAs, 4096
-# experts over many chunks, about a million pairs).
+# One CTA up to 4096 pairs; then one thread-block cluster (16 CTAs x 1024 threads
+# x 2 pairs = 32768 pairs, or half that where the GPU allows clusters of 8 only;
+# both sides of both limits are here); above that chunks of 1024..4096 pairs in
+# clusters of 8 (a partial last cluster, fewer experts than a cluster has CTAs,
+# 4096 experts over many chunks, about a million pairs).
 SORT_CASES = [(16, 2, 8, 4, None), (16384, 9, 385, 64, 1.1), (16, 8, 256, 32, None), (1000, 4, 37, 1, None),
               (50, 3, 5, 7, 2.0), (4097, 6, 128, 16, None), (3, 1, 4096, 8, None), (8192, 36, 2304, 64, 0.8),
               (1, 1, 1, 1, None), (5000, 2, 3, 128, None), (1025, 4, 100, 16, None), (4096, 1, 64, 8, None),
               (20000, 3, 5, 3, None), (50000, 8, 4096, 32, 1.1), (131072, 8, 256, 32, 1.1),
-              (70001, 9, 385, 64, 1.1)]
+              (70001, 9, 385, 64, 1.1), (2048, 16, 64, 8, None), (2049, 16, 64, 8, None),
+              (1024, 16, 300, 16, 1.1), (1025, 16, 300, 16, None), (1500, 16, 2304, 32, 0.8),
+              (12000, 16, 2304, 32, 0.8)]
 
 
 @pytest.mark.parametrize("T,k,E_tot,bm,skew", SORT_CASES)
@@ -107,7 +111,7 @@ FUSED = [synth.decode(T) for T in synth.DECODE_TS] + [synth.decode_gpt_oss(T) fo
     synth.Workload("fallback_T300_grouped", 300, 384, 9, synth.SIGMOID, synth.BF16, renorm=1, scaling=2.827,
                    n_group=8, topk_group=4, n_shared=1, bias_range=0.05, block_m=64),
     synth.Workload("fallback_wide_T4_e2304", 4, 2304, 36, synth.SOFTMAX, synth.F32, block_m=8),
-    # above 4096 pairs (E <= 1024) the route kernel counts the sort's chunks itself
+    # above 4096 pairs: the forward, then the one-cluster sort (or the chunked one)
     synth.Workload("prefill_T600_e256_k8", 600, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
     synth.Workload("prefill_T5000_e100_k5_sigmoid", 5000, 100, 5, synth.SIGMOID, synth.F32, renorm=1, scaling=1.5,
                    bias_range=0.1, block_m=8),
@@ -162,9 +166,9 @@ def test_fused_route_sort_matches_oracle(mr, orc, w, path):
 @pytest.mark.parametrize("path", [0, 1, 2], ids=["auto", "argmax", "select"])
 def test_fused_prefill_full_size_every_row(mr, orc, path):
     """The prefill workload (T=16384, E=384 + 1 shared, topk=9, grouped sigmoid,
-    block_m=64) through moe_router_fused_fwd_sort, whose route kernel also counts
-    the sort's chunks: every row's top-k and the whole sorted layout against the
-    oracle."""
+    block_m=64) through moe_router_fused_fwd_sort (the forward, then the sort in
+    one launch of one thread-block cluster): every row's top-k and the whole
+    sorted layout against the oracle."""
     w = synth.prefill_grouped()
     x = w.make_logits()
     b = w.make_bias()

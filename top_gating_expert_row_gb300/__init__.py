@@ -55,6 +55,7 @@ _SIGS = {
     "moe_sort_noalloc": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_sort_noalloc_scratch_bytes": ([], _SZ),
     "moe_router_set_wait_test": ([ctypes.c_uint, _I], _I),
+    "moe_router_set_launch_overlap": ([_I], _I),
     "moe_router_fused_workspace_bytes": ([_PP, _I], _SZ),
     "moe_router_fused_fwd_sort": ([_PP, _P, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
     "moe_router_strerror": ([_I], ctypes.c_char_p),
@@ -246,6 +247,11 @@ def moe_router_fused_fwd_sort(p, logits, block_m, topk_idx, topk_w, sorted_token
 
 def moe_router_set_topk_path(select_threshold: int = 8, force_path: int = 0) -> int:
     return _ok(_lib.moe_router_set_topk_path(select_threshold, force_path), "moe_router_set_topk_path")
+
+
+def moe_router_set_launch_overlap(enable: bool = True) -> int:
+    """Programmatic dependent launch of the library's kernels (on by default)."""
+    return _ok(_lib.moe_router_set_launch_overlap(1 if enable else 0), "moe_router_set_launch_overlap")
 
 
 def moe_router_set_wait_test(tries: int = 0, drop_copies: int = 0) -> int:

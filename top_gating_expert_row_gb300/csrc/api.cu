@@ -60,6 +60,9 @@ int persistent_grid(const void* func, int threads, size_t smem, long long units)
     return static_cast<int>(g < 1 ? 1 : g);
 }
 
+// The limit is only ever raised: one entry per (kernel, device) remembers the
+// largest size set, so a later launch with less shared memory never lowers the
+// limit another size relies on.
 int ensure_smem(const void* func, size_t bytes)
 {
     if (bytes <= 48 * 1024) return cudaSuccess;
@@ -67,11 +70,14 @@ int ensure_smem(const void* func, size_t bytes)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(g_occ_mu);
+    SmemEntry* ent = nullptr;
     for (int i = 0; i < g_smem_n; ++i)
-        if (g_smem[i].func == func && g_smem[i].device == dev && g_smem[i].bytes >= bytes) return cudaSuccess;
+        if (g_smem[i].func == func && g_smem[i].device == dev) ent = &g_smem[i];
+    if (ent && ent->bytes >= bytes) return cudaSuccess;
     e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
     if (e != cudaSuccess) return e;
-    if (g_smem_n < 128) g_smem[g_smem_n++] = SmemEntry{func, dev, bytes};
+    if (ent) ent->bytes = bytes;
+    else if (g_smem_n < 128) g_smem[g_smem_n++] = SmemEntry{func, dev, bytes};
     return cudaSuccess;
 }
 
@@ -85,25 +91,12 @@ int launch_fused_s0_d0(const RouteArgs&, const SortArgs&, int, bool, cudaStream_
 int launch_fused_s0_d1(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
 int launch_fused_s1_d0(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
 int launch_fused_s1_d1(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
-int launch_fwd_hist_s0_d0(const RouteArgs&, int, bool, int, int, int, uint32_t*, uint32_t*, int*, int*, cudaStream_t);
-int launch_fwd_hist_s0_d1(const RouteArgs&, int, bool, int, int, int, uint32_t*, uint32_t*, int*, int*, cudaStream_t);
-int launch_fwd_hist_s1_d0(const RouteArgs&, int, bool, int, int, int, uint32_t*, uint32_t*, int*, int*, cudaStream_t);
-int launch_fwd_hist_s1_d1(const RouteArgs&, int, bool, int, int, int, uint32_t*, uint32_t*, int*, int*, cudaStream_t);
 
 int launch_fwd(int score_fn, int in_dtype, const RouteArgs& a, int nv_idx, bool select, cudaStream_t st)
 {
     if (score_fn == kSoftmax)
         return in_dtype ? launch_fwd_s0_d1(a, nv_idx, select, st) : launch_fwd_s0_d0(a, nv_idx, select, st);
     return in_dtype ? launch_fwd_s1_d1(a, nv_idx, select, st) : launch_fwd_s1_d0(a, nv_idx, select, st);
-}
-
-int launch_fwd_hist(int score_fn, int in_dtype, const RouteArgs& a, int nv_idx, bool select, int R_min,
-                    int nchunk_max_pad, int E_tot, uint32_t* pre, uint32_t* ctot, int* R_out, int* nchunk_pad_out,
-                    cudaStream_t st)
-{
-    auto f = score_fn == kSoftmax ? (in_dtype ? launch_fwd_hist_s0_d1 : launch_fwd_hist_s0_d0)
-                                  : (in_dtype ? launch_fwd_hist_s1_d1 : launch_fwd_hist_s1_d0);
-    return f(a, nv_idx, select, R_min, nchunk_max_pad, E_tot, pre, ctot, R_out, nchunk_pad_out, st);
 }
 
 int launch_fused_decode(int score_fn, int in_dtype, const RouteArgs& a, const SortArgs& s, int nv_idx,
@@ -114,6 +107,14 @@ int launch_fused_decode(int score_fn, int in_dtype, const RouteArgs& a, const So
     return in_dtype ? launch_fused_s1_d1(a, s, nv_idx, select, st) : launch_fused_s1_d0(a, s, nv_idx, select, st);
 }
 
+// ---- launch overlap ---------------------------------------------------------------------------
+
+namespace {
+std::atomic<int>& overlap_flag();
+}
+
+bool launch_overlap() { return overlap_flag().load(std::memory_order_relaxed) != 0; }
+
 // ---- diagnostics ------------------------------------------------------------------------------
 
 // Evaluates the specification through both device forms the kernels use, the
@@ -122,8 +123,10 @@ int launch_fused_decode(int score_fn, int in_dtype, const RouteArgs& a, const So
 // wherever the two forms disagree for a non-NaN input, and likewise where the
 // softmax-value exponential's packed form exp_value2 disagrees with its
 // scalar form exp_value on (-|x[i]|, -|x[i]|/2).
-__global__ void k_expf(const float* __restrict__ x, float* __restrict__ y, int n)
+__global__ void k_expf(const float* x, float* y, int n)
 {
+    pdl_trigger_small();
+    pdl_wait();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         const float v = x[i];
         const float s = exp_f32(v);
@@ -138,20 +141,24 @@ __global__ void k_expf(const float* __restrict__ x, float* __restrict__ y, int n
     }
 }
 
-__global__ void k_noop() {}
+// The decode launch floor: an empty kernel launched the way the routing
+// kernels are (it takes part in the launch overlap like them).
+__global__ void k_noop()
+{
+    pdl_trigger_small();
+    pdl_wait();
+}
 
 int launch_expf(const float* x, float* y, int n, cudaStream_t st)
 {
     const long long blocks = (static_cast<long long>(n) + 255) / 256;
     const int grid = static_cast<int>(blocks < 4096 ? blocks : 4096);
-    k_expf<<<grid, 256, 0, st>>>(x, y, n);
-    return cudaGetLastError();
+    return launch_kernel(k_expf, dim3(grid), dim3(256), 0, st, 0, x, y, n);
 }
 
 int launch_noop(cudaStream_t st)
 {
-    k_noop<<<1, 32, 0, st>>>();
-    return cudaGetLastError();
+    return launch_kernel(k_noop, dim3(1), dim3(32), 0, st, 0);
 }
 
 // ---- device status word ------------------------------------------------------------------------
@@ -168,6 +175,8 @@ static __device__ int32_t g_device_status;
 
 __global__ void k_take_status(int32_t* word, int32_t* out, int clear)
 {
+    pdl_trigger_small();
+    pdl_wait();
     out[0] = *word;
     if (clear) *word = 0;
 }
@@ -214,6 +223,17 @@ struct PathConfig {
     int forced() const { return force.load(std::memory_order_relaxed); }
 };
 PathConfig g_path;
+
+// Programmatic dependent launch of every kernel (moe_router_set_launch_overlap;
+// on unless the environment sets MR_LAUNCH_OVERLAP=0).
+std::atomic<int>& overlap_flag()
+{
+    static std::atomic<int> flag{[] {
+        const char* v = std::getenv("MR_LAUNCH_OVERLAP");
+        return (v && v[0] == '0') ? 0 : 1;
+    }()};
+    return flag;
+}
 
 // Test hook for the bounded waits (moe_router_set_wait_test).
 struct WaitTest {
@@ -356,6 +376,13 @@ const char* moe_router_strerror(int code)
         case MR_ETIMEOUT: return "MR_ETIMEOUT: a bounded in-kernel wait gave up (outputs not valid)";
     }
     return "unknown moe_router status";
+}
+
+int moe_router_set_launch_overlap(int enable)
+{
+    if (enable != 0 && enable != 1) return MR_EINVAL;
+    overlap_flag().store(enable, std::memory_order_relaxed);
+    return MR_OK;
 }
 
 int moe_router_set_wait_test(unsigned int tries, int drop_copies)
@@ -574,14 +601,7 @@ size_t moe_router_fused_workspace_bytes(const mr_router_params* p, int block_m)
     if (nv < 0) return 0;
     if (fused_one_launch(p->T, kNvBuckets[nv])) return 0;
     const size_t N = static_cast<size_t>(p->T) * p->topk;
-    const int E_tot = p->E + p->n_shared;
-    size_t table;
-    if (fused_counts_in_route(static_cast<long long>(N), kNvBuckets[nv])) {  // route + counts, then the scatter
-        table = sort_table_bytes(fused_plan(p->T, p->topk, kNvBuckets[nv]).nchunk_max_pad, E_tot);
-    } else {
-        table = sort_ws_bytes(static_cast<long long>(N), E_tot);
-    }
-    return align_up(N * 4, 256) * 2 + table;
+    return align_up(N * 4, 256) * 2 + sort_ws_bytes(static_cast<long long>(N), p->E + p->n_shared);
 }
 
 int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int block_m, int32_t* topk_idx,
@@ -626,20 +646,6 @@ int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int
     float* wt = topk_w ? topk_w : reinterpret_cast<float*>(w + align_up(N * 4, 256));
     uint32_t* sws = reinterpret_cast<uint32_t*>(w + align_up(N * 4, 256) * 2);
     const RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, idx, wt, status);
-    if (fused_counts_in_route(static_cast<long long>(N), kNvBuckets[nv])) {
-        // the route kernel counts its chunks' pairs for the sort, whose
-        // histogram launch is then not needed
-        const FusedPlan fp = fused_plan(p->T, p->topk, kNvBuckets[nv]);
-        uint32_t* pre = sws;
-        uint32_t* ctot = sws + static_cast<size_t>(fp.nchunk_max_pad) * E_tot;
-        int R = 0, nchunk_pad = 0;
-        int e = launch_fwd_hist(p->score_fn, p->in_dtype, a, nv, use_select(k_r), fp.R_min, fp.nchunk_max_pad, E_tot,
-                                pre, ctot, &R, &nchunk_pad, st);
-        if (e != cudaSuccess) return MR_ECUDA;
-        return from_cuda(launch_sort_scatter(idx, wt, static_cast<int>(N), R * p->topk, nchunk_pad, E_tot, block_m,
-                                             pre, ctot, sorted_token_ids, sorted_weights, expert_ids,
-                                             num_tokens_post_pad, st));
-    }
     int e = launch_fwd(p->score_fn, p->in_dtype, a, nv, use_select(k_r), st);
     if (e != cudaSuccess) return MR_ECUDA;
     return from_cuda(launch_sort(idx, wt, static_cast<int>(N), E_tot, block_m, sorted_token_ids, sorted_weights,
@@ -660,8 +666,8 @@ int moe_router_device_status(int32_t* out, int clear, mr_stream_t stream)
     if (!out) return MR_EINVAL;
     int32_t* word = device_status_address();
     if (!word) return MR_ECUDA;
-    k_take_status<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(word, out, clear);
-    return from_cuda(cudaGetLastError());
+    return from_cuda(launch_kernel(k_take_status, dim3(1), dim3(1), 0, reinterpret_cast<cudaStream_t>(stream), 0, word,
+                                   out, clear));
 }
 
 }  // extern "C"

@@ -38,10 +38,12 @@ struct Kahan {
     }
 };
 
-__global__ void __launch_bounds__(kAuxThreads) k_aux_colsum(const float* __restrict__ probs, int T, int E,
-                                                            int rows_per_chunk, int vec, float* __restrict__ partial,
+__global__ void __launch_bounds__(kAuxThreads) k_aux_colsum(const float* probs, int T, int E,
+                                                            int rows_per_chunk, int vec, float* partial,
                                                             unsigned int* done)
 {
+    pdl_trigger_small();
+    pdl_wait();
     __shared__ float red[kAuxWarps][128];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col0 = blockIdx.x * 128 + lane * 4;
@@ -95,11 +97,13 @@ __global__ void __launch_bounds__(kAuxThreads) k_aux_colsum(const float* __restr
 // order), their dot product with the counts in fp64, written to `dots`; the
 // CTA that finishes last (a counter, no waiting) adds the slab results in slab
 // order and writes the loss.
-__global__ void __launch_bounds__(kAuxThreads) k_aux_loss_final(const float* __restrict__ partial, int R, int E,
-                                                                const int32_t* __restrict__ tokens_per_expert,
+__global__ void __launch_bounds__(kAuxThreads) k_aux_loss_final(const float* partial, int R, int E,
+                                                                const int32_t* tokens_per_expert,
                                                                 double C, double* dots, unsigned int* done,
                                                                 float* loss)
 {
+    pdl_trigger_small();
+    pdl_wait();
     __shared__ float red[kAuxWarps][128];
     __shared__ bool last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -150,11 +154,13 @@ __global__ void __launch_bounds__(kAuxThreads) k_aux_loss_final(const float* __r
     }
 }
 
-__global__ void __launch_bounds__(kAuxThreads) k_aux_loss_bwd(const int32_t* __restrict__ tokens_per_expert,
-                                                              const float* __restrict__ grad_loss, double C, int T,
+__global__ void __launch_bounds__(kAuxThreads) k_aux_loss_bwd(const int32_t* tokens_per_expert,
+                                                              const float* grad_loss, double C, int T,
                                                               int E, int rows_per_chunk, int vec,
-                                                              float* __restrict__ grad_probs)
+                                                              float* grad_probs)
 {
+    pdl_trigger_small();
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col0 = blockIdx.x * 128 + lane * 4;
     const int t0 = blockIdx.y * rows_per_chunk;
@@ -189,9 +195,11 @@ __global__ void __launch_bounds__(kAuxThreads) k_aux_loss_bwd(const int32_t* __r
 // Counts: a CTA covers a 512-column slab (lane l on columns 16l..16l+15, one
 // 16-byte load per row) of a chunk of rows, eight rows in flight per warp; the
 // warps' counts are added in shared memory and then once per column into `out`.
-__global__ void __launch_bounds__(kAuxThreads) k_tokens_per_expert(const uint8_t* __restrict__ map, int T, int E,
+__global__ void __launch_bounds__(kAuxThreads) k_tokens_per_expert(const uint8_t* map, int T, int E,
                                                                    int rows_per_chunk, int vec, int32_t* out)
 {
+    pdl_trigger_small();
+    pdl_wait();
     __shared__ uint32_t red[kAuxWarps][512];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col0 = blockIdx.x * 512 + lane * 16;
@@ -290,11 +298,11 @@ int launch_aux_loss_fwd(const float* probs, const int32_t* tokens_per_expert, in
     unsigned int* done = reinterpret_cast<unsigned int*>(dots + S);
     const int rows = (T + R - 1) / R;
     const int vec = (E % 4 == 0) && (reinterpret_cast<uintptr_t>(probs) % 16 == 0);
-    k_aux_colsum<<<dim3(S, R), kAuxThreads, 0, st>>>(probs, T, E, rows, vec, partial, done);
-    cudaError_t e = cudaGetLastError();
+    const int e = launch_kernel(k_aux_colsum, dim3(S, R), dim3(kAuxThreads), 0, st, 0, probs, T, E, rows, vec, partial,
+                                done);
     if (e != cudaSuccess) return e;
-    k_aux_loss_final<<<S, kAuxThreads, 0, st>>>(partial, R, E, tokens_per_expert, C, dots, done, loss);
-    return cudaGetLastError();
+    return launch_kernel(k_aux_loss_final, dim3(S), dim3(kAuxThreads), 0, st, 0, partial, R, E, tokens_per_expert, C,
+                         dots, done, loss);
 }
 
 int launch_aux_loss_bwd(const int32_t* tokens_per_expert, const float* grad_loss, int T, int E, double C,
@@ -305,8 +313,8 @@ int launch_aux_loss_bwd(const int32_t* tokens_per_expert, const float* grad_loss
     const int rows = (T + R - 1) / R;
     const int S = (E + 127) / 128;
     const int vec = (E % 4 == 0) && (reinterpret_cast<uintptr_t>(grad_probs) % 16 == 0);
-    k_aux_loss_bwd<<<dim3(S, R), kAuxThreads, 0, st>>>(tokens_per_expert, grad_loss, C, T, E, rows, vec, grad_probs);
-    return cudaGetLastError();
+    return launch_kernel(k_aux_loss_bwd, dim3(S, R), dim3(kAuxThreads), 0, st, 0, tokens_per_expert, grad_loss, C, T, E,
+                         rows, vec, grad_probs);
 }
 
 int launch_tokens_per_expert(const uint8_t* map, int T, int E, int32_t* out, cudaStream_t st)
@@ -318,8 +326,7 @@ int launch_tokens_per_expert(const uint8_t* map, int T, int E, int32_t* out, cud
     const int rows = (T + R - 1) / R;
     const int S = (E + 511) / 512;
     const int vec = (E % 16 == 0) && (reinterpret_cast<uintptr_t>(map) % 16 == 0);
-    k_tokens_per_expert<<<dim3(S, R), kAuxThreads, 0, st>>>(map, T, E, rows, vec, out);
-    return cudaGetLastError();
+    return launch_kernel(k_tokens_per_expert, dim3(S, R), dim3(kAuxThreads), 0, st, 0, map, T, E, rows, vec, out);
 }
 
 }  // namespace mr

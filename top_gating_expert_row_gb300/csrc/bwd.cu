@@ -22,12 +22,14 @@ constexpr int kBwdThreads = 128;
 // GradT: the dtype of grad and dx (fp32, or bf16 for bf16 logits: the
 // gradient is computed in fp32 and rounded once when stored).
 template <int SCORE, int NV, bool HAS_MAP, typename GradT>
-__global__ void __launch_bounds__(kBwdThreads) k_router_bwd(const GradT* __restrict__ grad,
-                                                            const float* __restrict__ inter,
-                                                            const uint8_t* __restrict__ map,
-                                                            GradT* __restrict__ dx, int T, int E,
+__global__ void __launch_bounds__(kBwdThreads) k_router_bwd(const GradT* grad,
+                                                            const float* inter,
+                                                            const uint8_t* map,
+                                                            GradT* dx, int T, int E,
                                                             int renorm, float c, int vec)
 {
+    pdl_trigger_small();
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     constexpr bool kPacked = !std::is_same<GradT, float>::value;
     for (int t = blockIdx.x * nw + warp; t < T; t += gridDim.x * nw) {
@@ -157,8 +159,7 @@ int launch(BwdFn<GradT> f, const GradT* g, const float* s, const uint8_t* m, Gra
     const long long ctas_needed = (static_cast<long long>(T) + kBwdThreads / 32 - 1) / (kBwdThreads / 32);
     const int grid = persistent_grid(reinterpret_cast<const void*>(f), kBwdThreads, 0, ctas_needed);
     if (grid <= 0) return cudaErrorInvalidConfiguration;
-    f<<<grid, kBwdThreads, 0, st>>>(g, s, m, dx, T, E, renorm, scaling, vec ? 1 : 0);
-    return cudaGetLastError();
+    return launch_kernel(f, dim3(grid), dim3(kBwdThreads), 0, st, 0, g, s, m, dx, T, E, renorm, scaling, vec ? 1 : 0);
 }
 }  // namespace
 

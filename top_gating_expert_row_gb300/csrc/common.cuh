@@ -308,6 +308,36 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch. Every kernel of the library may call
+// pdl_trigger on entry (the next kernel in the stream may be launched now and
+// run its own entry while this one works) and calls pdl_wait before its first
+// access to global memory (it returns once the previous kernel in the stream
+// has completed and its writes are visible; at once for a kernel launched
+// without the overlap). Since every kernel waits for its predecessor, each also
+// completes after all the kernels before it.
+// ---------------------------------------------------------------------------
+// Under the overlap a kernel runs while its predecessor is still writing, so
+// nothing that kernel produced may be read through the non-coherent read-only
+// path (ld.global.nc: __ldg, or plain loads through const __restrict__
+// pointers, which the compiler may turn into it): that path assumes the data
+// stays unchanged for the whole life of the reading kernel, and an SM may keep
+// serving stale lines from it after the wait. The kernels therefore take no
+// __restrict__ pointers and load with coherent cache operators (__ldcs,
+// __ldcg, plain loads), which the wait's memory clobber keeps after it.
+//
+// Only small grids trigger on entry (pdl_trigger_small): a large grid's
+// dependents would be placed wherever its CTAs free slots first, unevenly, so
+// a large grid lets its dependents launch when it completes, as in plain
+// stream order.
+constexpr unsigned kPdlSmallGrid = 32;
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger_small()
+{
+    if (gridDim.x * gridDim.y * gridDim.z <= kPdlSmallGrid) pdl_trigger();
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // Thread-block clusters: rank, barrier and distributed shared memory.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -315,6 +345,13 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+    return n;
 }
 
 // Barrier over every thread of the cluster (all threads of all its CTAs must
@@ -325,20 +362,16 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Address of `p` (a variable in this CTA's shared memory) in the shared memory
-// of the cluster's CTA `rank` (the same variable in that CTA).
-__device__ __forceinline__ uint32_t map_shared_rank(const void* p, uint32_t rank)
+// Generic pointer to the same variable in the shared memory of the cluster's
+// CTA `rank`: plain loads through it reach that CTA's shared memory, and the
+// compiler is free to keep several in flight (the cluster barriers, whose asm
+// clobbers memory, still order them).
+template <typename T>
+__device__ __forceinline__ const T* cluster_peer(const T* p, uint32_t rank)
 {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t ld_shared_cluster(uint32_t addr)
-{
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
+    uint64_t r;
+    asm("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
+    return reinterpret_cast<const T*>(r);
 }
 
 // ---------------------------------------------------------------------------

@@ -5,17 +5,11 @@
 //   k_router_fwd     persistent grid, 8 warps per CTA, one token row per warp
 //                    at a time (TransformerEngine PR 3012, fused_topk_with_
 //                    score_function; also serves fused_score_for_moe_aux_loss)
-//   k_router_fwd_hist  the prefill route + sort's first launch: CTA c routes a
-//                    contiguous run of rows (its chunk of pairs), counts the
-//                    chunk's experts in shared memory, and its cluster of 8
-//                    turns the counts into the sort's prefixes (FlyDSL PR 582,
-//                    fusing the top-k gating with the sorting step)
 //   k_fused_decode   ONE CTA for T <= 16 tokens (T <= 64 for E <= 256, with 32
 //                    warps): warp t routes token t (and t + 32), then
 //                    the whole CTA histograms, scans and scatters the T*topk
 //                    pairs in shared memory (FlyDSL PR 582, fused top-k gating
 //                    + MoE sorting at decode sizes)
-#include <mutex>
 #include <type_traits>
 
 #include "internal.h"
@@ -43,10 +37,12 @@ using InT = float;
 constexpr int kScore = MR_SCORE_FN;
 
 // RANKW: candidates per lane in a pass of the candidate rank (3 only where the
-// candidate cap exceeds 64, see rank_candidates)
-template <int NV, bool SELECT, bool FULL, int RANKW = 2>
+// candidate cap exceeds 64, see rank_candidates). SET: no compact outputs, the
+// winners are selected as a set (route_row).
+template <int NV, bool SELECT, bool FULL, int RANKW = 2, bool SET = false>
 __global__ void __launch_bounds__(kFwdThreads, fwd_min_blocks(NV)) k_router_fwd(RouteArgs a)
 {
+    pdl_trigger_small();
     extern __shared__ __align__(16) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nw = blockDim.x >> 5;
@@ -55,12 +51,13 @@ __global__ void __launch_bounds__(kFwdThreads, fwd_min_blocks(NV)) k_router_fwd(
     const int stride = gridDim.x * nw;
     const uint32_t row_bytes = static_cast<uint32_t>(a.E) * sizeof(InT);
     uint32_t warm = 0u;  // threshold carried from this warp's previous row
+    pdl_wait();
     for (int t = blockIdx.x * nw + warp; t < a.T; t += stride) {
         // the warp's next row streams into L2 while this one is computed
         if (a.prefetch && lane == 0 && t + stride < a.T)
             prefetch_l2(static_cast<const InT*>(a.logits) + static_cast<size_t>(t + stride) * a.E, row_bytes);
-        const float scale = route_row<kScore, InT, NV, SELECT, FULL, RANKW>(a, t, wsm, L, lane, warm);
-        if (a.topk_idx || a.topk_w) {
+        const float scale = route_row<kScore, InT, NV, SELECT, FULL, RANKW, SET>(a, t, wsm, L, lane, warm);
+        if (!SET && (a.topk_idx || a.topk_w)) {
             const size_t o = static_cast<size_t>(t) * a.topk;
             emit_compact(a, wsm, L, scale, lane, a.topk_idx ? a.topk_idx + o : nullptr,
                          a.topk_w ? a.topk_w + o : nullptr);
@@ -69,55 +66,11 @@ __global__ void __launch_bounds__(kFwdThreads, fwd_min_blocks(NV)) k_router_fwd(
     }
 }
 
-// Route + the sort's counts: CTA c routes rows [c*R, min(T, (c+1)*R)) (pairs
-// [c*R*topk, ...), its sort chunk), writes the compact outputs, counts the
-// chunk's experts (routed winners and shared experts) in shared memory and
-// hands the counts to cluster_prefix_counts, whose pre / ctot feed
-// k_sort_scatter. Counted are exactly the ids written to topk_idx that lie in
-// [0, E_tot), the ids the scatter places.
-template <int NV, bool SELECT, bool FULL, int RANKW = 2>
-__global__ void __cluster_dims__(kClusterChunks, 1, 1) __launch_bounds__(kFwdThreads, fwd_min_blocks(NV))
-    k_router_fwd_hist(RouteArgs a, int R, int E_tot, uint32_t* pre, uint32_t* ctot)
-{
-    extern __shared__ __align__(16) unsigned char smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nw = blockDim.x >> 5;
-    const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, SELECT, a.n_group > 0);
-    unsigned char* wsm = smem + static_cast<size_t>(warp) * L.bytes;
-    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + static_cast<size_t>(nw) * L.bytes);
-    for (int e = threadIdx.x; e < E_tot; e += blockDim.x) hist[e] = 0u;
-    __syncthreads();
-    const long long r0l = static_cast<long long>(blockIdx.x) * R;
-    const int r0 = static_cast<int>(r0l < a.T ? r0l : a.T);
-    const int r1 = min(a.T, r0 + R);
-    const uint32_t row_bytes = static_cast<uint32_t>(a.E) * sizeof(InT);
-    uint32_t warm = 0u;
-    for (int t = r0 + warp; t < r1; t += nw) {
-        if (a.prefetch && lane == 0 && t + nw < r1)
-            prefetch_l2(static_cast<const InT*>(a.logits) + static_cast<size_t>(t + nw) * a.E, row_bytes);
-        const float scale = route_row<kScore, InT, NV, SELECT, FULL, RANKW>(a, t, wsm, L, lane, warm);
-        const size_t o = static_cast<size_t>(t) * a.topk;
-        emit_compact(a, wsm, L, scale, lane, a.topk_idx + o, a.topk_w ? a.topk_w + o : nullptr);
-        const uint32_t* win_idx = reinterpret_cast<const uint32_t*>(wsm + L.win_idx);
-        for (int j0 = 0; j0 < a.topk; j0 += 32) {
-            const int j = j0 + lane;
-            int e = kInvalidExpert;
-            if (j < a.topk) {
-                e = j < a.k_r ? static_cast<int>(win_idx[j]) : a.E + (j - a.k_r);  // as emit_compact writes it
-                if (e < 0 || e >= E_tot) e = kInvalidExpert;
-            }
-            warp_hist_add(hist, e, lane);
-        }
-        __syncwarp();
-    }
-    __syncthreads();
-    cluster_prefix_counts(hist, E_tot, pre, ctot);
-}
-
 // Wide rows (E > 1024): the row lives in shared memory, one warp per row.
 template <bool SELECT, bool FULL>
 __global__ void __launch_bounds__(kWideThreads, kWideMinBlocks) k_router_fwd_wide(RouteArgs a)
 {
+    pdl_trigger_small();
     extern __shared__ __align__(16) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nw = blockDim.x >> 5;
@@ -125,7 +78,6 @@ __global__ void __launch_bounds__(kWideThreads, kWideMinBlocks) k_router_fwd_wid
     unsigned char* wsm = smem + static_cast<size_t>(warp) * L.bytes;
     const int stride = gridDim.x * nw;
     const uint32_t row_bytes = static_cast<uint32_t>(a.E) * sizeof(InT);
-    const InT* rows = static_cast<const InT*>(a.logits);
     uint32_t warm = 0u;
     // FULL rows are staged in shared memory by bulk copies: the first one here,
     // each next one while the previous row writes its outputs
@@ -140,6 +92,10 @@ __global__ void __launch_bounds__(kWideThreads, kWideMinBlocks) k_router_fwd_wid
     if (FULL) {
         if (lane == 0) mbar_init(st.bar, 1);
         __syncwarp();
+    }
+    pdl_wait();
+    const InT* rows = static_cast<const InT*>(a.logits);
+    if (FULL) {
         if (lane == 0 && t < a.T) bulk_load_row(wsm + L.kbuf + st.off, rows + static_cast<size_t>(t) * a.E, row_bytes,
                                                 st.bar, st.drop);
     }
@@ -188,6 +144,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_fused_decode(RouteArgs a, SortAr
     // three block barriers separate the phases. The 32-warp form routes up to
     // 64 tokens (warp w: tokens w and w + 32) with 64-bit masks.
     using Mask = typename std::conditional<(THREADS > kFusedThreads), unsigned long long, uint32_t>::type;
+    pdl_trigger_small();
     extern __shared__ __align__(16) unsigned char smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5, nt = blockDim.x;
     const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, SELECT, a.n_group > 0);
@@ -203,6 +160,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_fused_decode(RouteArgs a, SortAr
     auto popc = [](Mask m) { return static_cast<uint32_t>(sizeof(Mask) == 8 ? __popcll(m) : __popc(static_cast<uint32_t>(m))); };
 
     for (int e = tid; e < E_tot; e += nt) mask[e] = 0u;
+    pdl_wait();
     {
         unsigned char* wsm = smem + static_cast<size_t>(warp) * L.bytes;
         uint32_t warm = 0u;
@@ -292,64 +250,18 @@ namespace {
 using FwdFn = void (*)(RouteArgs);
 using FusedFn = void (*)(RouteArgs, SortArgs);
 
-template <bool SELECT, bool FULL, int RANKW = 2>
+template <bool SELECT, bool FULL, int RANKW = 2, bool SET = false>
 FwdFn fwd_kernel(int nv_idx)
 {
     switch (kNvBuckets[nv_idx]) {
-        case 1: return k_router_fwd<1, SELECT, FULL, RANKW>;
-        case 2: return k_router_fwd<2, SELECT, FULL, RANKW>;
-        case 3: return k_router_fwd<3, SELECT, FULL, RANKW>;
-        case 4: return k_router_fwd<4, SELECT, FULL, RANKW>;
-        case 6: return k_router_fwd<6, SELECT, FULL, RANKW>;
-        case 8: return k_router_fwd<8, SELECT, FULL, RANKW>;
+        case 1: return k_router_fwd<1, SELECT, FULL, RANKW, SET>;
+        case 2: return k_router_fwd<2, SELECT, FULL, RANKW, SET>;
+        case 3: return k_router_fwd<3, SELECT, FULL, RANKW, SET>;
+        case 4: return k_router_fwd<4, SELECT, FULL, RANKW, SET>;
+        case 6: return k_router_fwd<6, SELECT, FULL, RANKW, SET>;
+        case 8: return k_router_fwd<8, SELECT, FULL, RANKW, SET>;
     }
     return nullptr;
-}
-
-using FwdHistFn = void (*)(RouteArgs, int, int, uint32_t*, uint32_t*);
-
-template <bool SELECT, bool FULL, int RANKW = 2>
-FwdHistFn fwd_hist_kernel(int nv_idx)
-{
-    switch (kNvBuckets[nv_idx]) {
-        case 1: return k_router_fwd_hist<1, SELECT, FULL, RANKW>;
-        case 2: return k_router_fwd_hist<2, SELECT, FULL, RANKW>;
-        case 3: return k_router_fwd_hist<3, SELECT, FULL, RANKW>;
-        case 4: return k_router_fwd_hist<4, SELECT, FULL, RANKW>;
-        case 6: return k_router_fwd_hist<6, SELECT, FULL, RANKW>;
-        case 8: return k_router_fwd_hist<8, SELECT, FULL, RANKW>;
-    }
-    return nullptr;
-}
-
-// Clusters of this kernel that fit on the device at once (cached per kernel,
-// shared-memory size and device; 0 if the query fails).
-int resident_clusters(const void* func, int threads, size_t smem)
-{
-    static std::mutex mu;
-    struct Entry {
-        const void* func;
-        size_t smem;
-        int dev, clusters;
-    };
-    static Entry cache[64];
-    static int n = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    std::lock_guard<std::mutex> lk(mu);
-    for (int i = 0; i < n; ++i)
-        if (cache[i].func == func && cache[i].smem == smem && cache[i].dev == dev) return cache[i].clusters;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kClusterChunks, 1, 1);
-    cfg.blockDim = dim3(threads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, func, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        clusters = 0;
-    }
-    if (n < 64) cache[n++] = Entry{func, smem, dev, clusters};
-    return clusters;
 }
 
 template <bool SELECT, bool FULL>
@@ -389,15 +301,19 @@ int MR_CAT(launch_fwd, MR_SUFFIX)(const RouteArgs& a, int nv_idx, bool select, c
         const long long ctas_needed = (static_cast<long long>(a.T) + kWideThreads / 32 - 1) / (kWideThreads / 32);
         const int grid = persistent_grid(reinterpret_cast<const void*>(f), kWideThreads, smem, ctas_needed);
         if (grid <= 0) return cudaErrorInvalidConfiguration;
-        f<<<grid, kWideThreads, smem, st>>>(a);
-        return cudaGetLastError();
+        return launch_kernel(f, dim3(grid), dim3(kWideThreads), smem, st, 0, a);
     }
     // every chunk whole and vector-aligned: the specialisation without edge tests
     const bool full = a.vec && a.E == 128 * kNvBuckets[nv_idx];
     // more than 64 candidates possible (k_r > 32): rank three per lane per pass
     const bool rank3 = full && a.stop > 64;
-    const FwdFn f = select ? (rank3 ? fwd_kernel<true, true, 3>(nv_idx)
-                                    : (full ? fwd_kernel<true, true>(nv_idx) : fwd_kernel<true, false>(nv_idx)))
+    // no compact outputs and more than 64 candidates possible (k_r > 32): the
+    // winners are selected as a set, without the candidate rank (at smaller k_r
+    // the rank costs less than the bisection rounds to the exact threshold)
+    const bool set_only = rank3 && !a.topk_idx && !a.topk_w;
+    const FwdFn f = select ? (set_only ? fwd_kernel<true, true, 2, true>(nv_idx)
+                              : rank3 ? fwd_kernel<true, true, 3>(nv_idx)
+                                      : (full ? fwd_kernel<true, true>(nv_idx) : fwd_kernel<true, false>(nv_idx)))
                            : (full ? fwd_kernel<false, true>(nv_idx) : fwd_kernel<false, false>(nv_idx));
     if (!f) return cudaErrorInvalidValue;
     const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, select, a.n_group > 0);
@@ -407,39 +323,7 @@ int MR_CAT(launch_fwd, MR_SUFFIX)(const RouteArgs& a, int nv_idx, bool select, c
     const long long ctas_needed = (static_cast<long long>(a.T) + kFwdThreads / 32 - 1) / (kFwdThreads / 32);
     const int grid = persistent_grid(reinterpret_cast<const void*>(f), kFwdThreads, smem, ctas_needed);
     if (grid <= 0) return cudaErrorInvalidConfiguration;
-    f<<<grid, kFwdThreads, smem, st>>>(a);
-    return cudaGetLastError();
-}
-
-int MR_CAT(launch_fwd_hist, MR_SUFFIX)(const RouteArgs& a, int nv_idx, bool select, int R_min, int nchunk_max_pad,
-                                      int E_tot, uint32_t* pre, uint32_t* ctot, int* R_out, int* nchunk_pad_out,
-                                      cudaStream_t st)
-{
-    const bool full = a.vec && a.E == 128 * kNvBuckets[nv_idx];
-    const bool rank3 = full && a.stop > 64;
-    const FwdHistFn f = select ? (rank3 ? fwd_hist_kernel<true, true, 3>(nv_idx)
-                                        : (full ? fwd_hist_kernel<true, true>(nv_idx) : fwd_hist_kernel<true, false>(nv_idx)))
-                               : (full ? fwd_hist_kernel<false, true>(nv_idx) : fwd_hist_kernel<false, false>(nv_idx));
-    if (!f) return cudaErrorInvalidValue;
-    const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, select, a.n_group > 0);
-    const size_t smem = static_cast<size_t>(L.bytes) * (kFwdThreads / 32) + static_cast<size_t>(align16(E_tot * 4));
-    int err = ensure_smem(reinterpret_cast<const void*>(f), smem);
-    if (err != cudaSuccess) return err;
-    // at least R_min rows per CTA, more if the grid would not fit on the GPU at once
-    int R = R_min;
-    const int fit = resident_clusters(reinterpret_cast<const void*>(f), kFwdThreads, smem);
-    if (fit > 0) {
-        const long long ctas = static_cast<long long>(fit) * kClusterChunks;
-        const int r_fit = static_cast<int>((a.T + ctas - 1) / ctas);
-        if (r_fit > R) R = min(r_fit, kSortChunk / a.topk);
-    }
-    const int nchunk = (a.T + R - 1) / R;
-    const int nchunk_pad = (nchunk + kClusterChunks - 1) / kClusterChunks * kClusterChunks;
-    if (nchunk_pad > nchunk_max_pad) return cudaErrorInvalidConfiguration;  // R >= R_min: never
-    f<<<nchunk_pad, kFwdThreads, smem, st>>>(a, R, E_tot, pre, ctot);
-    *R_out = R;
-    *nchunk_pad_out = nchunk_pad;
-    return cudaGetLastError();
+    return launch_kernel(f, dim3(grid), dim3(kFwdThreads), smem, st, 0, a);
 }
 
 int MR_CAT(launch_fused, MR_SUFFIX)(const RouteArgs& a, const SortArgs& s, int nv_idx, bool select,
@@ -460,8 +344,7 @@ int MR_CAT(launch_fused, MR_SUFFIX)(const RouteArgs& a, const SortArgs& s, int n
                         fused_sort_layout(a.T * a.topk, s.E_tot, s.block_m, wide ? 8 : 4).bytes;
     int err = ensure_smem(reinterpret_cast<const void*>(f), smem);
     if (err != cudaSuccess) return err;
-    f<<<1, threads, smem, st>>>(a, s);
-    return cudaGetLastError();
+    return launch_kernel(f, dim3(1), dim3(threads), smem, st, 0, a, s);
 }
 
 }  // namespace mr

@@ -42,6 +42,9 @@ inline bool fused_one_launch(int T, int nv_bucket)
 // The forward keeps rows of up to this many chunks in registers (E <= 1024);
 // wider rows take the shared-memory routine, two warps per CTA.
 constexpr int kRegisterMaxNv = 8;
+// Resident CTAs per SM the forward's register budget is sized for (the row's
+// keys take 4*NV registers per lane).
+constexpr int fwd_min_blocks(int nv) { return nv >= 12 ? 2 : (nv >= 6 ? 3 : 4); }
 constexpr int kWideThreads = 64;
 // Registers are capped so that shared memory, not registers, bounds residency
 // (a 9 KB key row per warp at E = 2304 allows about 22 warps per SM).
@@ -109,13 +112,6 @@ int launch_sort(const int32_t* idx, const float* w, int N, int E_tot, int block_
 int launch_sort_scatter(const int32_t* idx, const float* w, int N, int PC, int nchunk_pad, int E_tot, int block_m,
                         const uint32_t* pre, const uint32_t* ctot, int32_t* ids, float* sw, int32_t* eids,
                         int32_t* npp, cudaStream_t st);
-// Route + first sort stage in one launch (prefill sizes, E <= 1024): CTA c routes
-// rows [c*R, (c+1)*R) and counts their pairs; the clusters write pre / ctot.
-// R is at least R_min and chosen so that the grid fits on the GPU at once; the
-// rows per CTA and the padded CTA count used are returned.
-int launch_fwd_hist(int score_fn, int in_dtype, const RouteArgs& a, int nv_idx, bool select, int R_min,
-                    int nchunk_max_pad, int E_tot, uint32_t* pre, uint32_t* ctot, int* R_out, int* nchunk_pad_out,
-                    cudaStream_t st);
 int launch_expf(const float* x, float* y, int n, cudaStream_t st);
 int aux_chunks(long long T);
 size_t aux_workspace_bytes(long long T, int E);
@@ -162,35 +158,42 @@ inline size_t sort_ws_bytes(long long N, int E_tot)
     return sort_table_bytes(sort_plan(N, E_tot).nchunk_pad, E_tot);
 }
 
-// Route CTAs the fused prefill path aims for: this GPU's 152 SMs times the
-// forward's resident CTAs per SM for the row width (a device with fewer SMs
-// runs the same chunks in more waves). R_min rows per CTA, capped so that a
-// chunk holds at most kSortChunk pairs.
-constexpr int kGpuSms = 152;
-// Resident CTAs per SM the forward's register budget is sized for (the row's
-// keys take 4*NV registers per lane).
-constexpr int fwd_min_blocks(int nv) { return nv >= 12 ? 2 : (nv >= 6 ? 3 : 4); }
+// Whether launches let the next kernel of the stream start while this one
+// finishes (programmatic dependent launch; moe_router_set_launch_overlap).
+bool launch_overlap();
 
-// Whether the fused call above the one-launch sizes has the route kernel count
-// the sort's chunks (rows held in registers, more pairs than the one-CTA sort
-// takes); otherwise it runs the forward and then moe_sort's launches.
-inline bool fused_counts_in_route(long long N, int nv_bucket) { return N > kSortChunk && nv_bucket <= kRegisterMaxNv; }
-
-struct FusedPlan {
-    int R_min, nchunk_max_pad;
-};
-
-inline FusedPlan fused_plan(int T, int topk, int nv_bucket)
+// Launches kernel(args...) on st with `cluster` CTAs per cluster (0: none, or
+// the kernel's compile-time size) and, when launch_overlap(), the
+// programmatic-serialization attribute (the kernel may start before the
+// previous one in the stream completes; it waits for it in pdl_wait). Returns
+// a cudaError_t value.
+template <typename... KArgs, typename... Args>
+int launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cluster,
+                  Args... args)
 {
-    const int target = kGpuSms * fwd_min_blocks(nv_bucket);
-    int R = (T + target - 1) / target;
-    const int rmax = kSortChunk / topk;
-    R = R < 1 ? 1 : (R > rmax ? rmax : R);
-    FusedPlan f;
-    f.R_min = R;
-    const int n = (T + R - 1) / R;
-    f.nchunk_max_pad = (n + kClusterChunks - 1) / kClusterChunks * kClusterChunks;
-    return f;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (launch_overlap()) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster > 0) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // Persistent-grid size: min(units, SMs x resident CTAs) for a kernel.

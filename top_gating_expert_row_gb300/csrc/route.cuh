@@ -20,7 +20,10 @@
 //   5. emit     dense probs / routing_map / intermediate (compact topk_idx/w:
 //               emit_compact)
 //
-// Both selection paths produce the identical winner list.
+// Both selection paths produce the identical winner list. SET (threshold select
+// only; for calls without compact outputs) finds the winners as a set: the
+// bisection runs to the exact threshold and the winners are patched straight
+// from the registers, with no candidate list and no ranking.
 #pragma once
 
 #include <type_traits>
@@ -205,10 +208,11 @@ __device__ __forceinline__ void rank_candidates(const unsigned long long* cand, 
     }
 }
 
-template <int SCORE, typename InT, int NV, bool SELECT, bool FULL = false, int RANKW = 2>
+template <int SCORE, typename InT, int NV, bool SELECT, bool FULL = false, int RANKW = 2, bool SET = false>
 __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned char* wsm,
                                            const WarpLayout& L, int lane, uint32_t& warm)
 {
+    static_assert(!SET || SELECT, "the set-only selection is a form of the threshold select");
     float* vbuf = reinterpret_cast<float*>(wsm + L.vbuf);
     uint32_t* win_idx = reinterpret_cast<uint32_t*>(wsm + L.win_idx);
     float* win_val = reinterpret_cast<float*>(wsm + L.win_val);
@@ -296,11 +300,11 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
                 float b[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 if (a.bias) {
                     if (vec && whole(v)) {
-                        const float4 q = __ldg(reinterpret_cast<const float4*>(a.bias + e0));
+                        const float4 q = __ldcg(reinterpret_cast<const float4*>(a.bias + e0));
                         b[0] = q.x; b[1] = q.y; b[2] = q.z; b[3] = q.w;
                     } else {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) b[c] = inside(v, c) ? __ldg(a.bias + e0 + c) : 0.0f;
+                        for (int c = 0; c < 4; ++c) b[c] = inside(v, c) ? __ldcg(a.bias + e0 + c) : 0.0f;
                     }
                 }
                 const float2 s01 = sigmoid_f32x2(make_float2(x[v][0], x[v][1]));
@@ -364,6 +368,40 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
         __syncwarp();  // the staged keys are read no more; the region may be reused
     }
 
+    // dense rows of step 5: intermediate = s; probs and routing_map as zero
+    // vectors (the winners are patched in afterwards, after a __syncwarp)
+    InT* prow = a.probs ? static_cast<InT*>(a.probs) + static_cast<size_t>(t) * E : nullptr;
+    uint8_t* mrow = a.map ? a.map + static_cast<size_t>(t) * E : nullptr;
+    float* irow = a.inter ? a.inter + static_cast<size_t>(t) * E : nullptr;
+    auto dense_rows = [&]() {
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const int e0 = v * 128 + lane4;
+            if (!FULL && e0 >= E) continue;
+            if (vec && whole(v)) {
+                if (irow) {
+                    const float4 q = *reinterpret_cast<const float4*>(vbuf + e0);
+                    const float2 xy = __fmul2_rn(make_float2(q.x, q.y), make_float2(vmul, vmul));
+                    const float2 zw = __fmul2_rn(make_float2(q.z, q.w), make_float2(vmul, vmul));
+                    *reinterpret_cast<float4*>(irow + e0) = make_float4(xy.x, xy.y, zw.x, zw.y);
+                }
+                if (prow) {
+                    const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    store4<InT>(prow + e0, z);
+                }
+                if (mrow) *reinterpret_cast<uint32_t*>(mrow + e0) = 0u;
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (!inside(v, c)) break;
+                    if (irow) irow[e0 + c] = __fmul_rn(vbuf[e0 + c], vmul);
+                    if (prow) store_scalar<InT>(prow + e0 + c, 0.0f);
+                    if (mrow) mrow[e0 + c] = 0;
+                }
+            }
+        }
+    };
+
     // 3. selection
     if (!SELECT) {
         // k_r rounds of arg-max over the lanes' best keys. Each lane keeps its two
@@ -420,7 +458,9 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
         }
     } else {
         unsigned long long* cand = reinterpret_cast<unsigned long long*>(wsm + L.cand);
-        const uint32_t cap = static_cast<uint32_t>(a.stop);
+        // SET: the bisection runs until exactly k_r keys are >= lo (or the k_r-th
+        // key is tied at lo); otherwise it stops at `stop` candidates for the rank
+        const uint32_t cap = static_cast<uint32_t>(SET ? k_r : a.stop);
         const uint32_t n_valid = static_cast<uint32_t>(a.n_group > 0 ? a.topk_group * (E / a.n_group) : E);
         // Invariant: count(key >= lo) = cnt_lo >= k_r > count(key >= hi) = cnt_hi.
         // lo starts at 1, below every real key (count = n_valid); the row minimum
@@ -465,6 +505,62 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
                 if (km > lo && km < hi) mid = km;
             }
             split(mid);
+        }
+        if constexpr (SET) {
+            // The winners as a set (bit v*4 + c of the lane's elements): with
+            // exactly k_r keys >= lo, those; else hi == lo + 1, and the keys >= hi
+            // are followed by the keys equal to lo in index order.
+            static_assert(NV <= 8, "one bit per element of the lane");
+            uint32_t winmask = 0u;
+            if (cnt_lo <= cap) {
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        if (key[v][c] >= lo) winmask |= 1u << (v * 4 + c);
+            } else {
+                uint32_t base = cnt_hi;
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    uint32_t m4 = 0u;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) m4 += (key[v][c] == lo);
+                    const uint32_t off = warp_exclusive_scan(m4, lane);
+                    const uint32_t tot = __shfl_sync(kFull, off + m4, 31);
+                    uint32_t p = base + off;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        if (key[v][c] >= hi) {
+                            winmask |= 1u << (v * 4 + c);
+                        } else if (key[v][c] == lo) {
+                            if (p < static_cast<uint32_t>(k_r)) winmask |= 1u << (v * 4 + c);
+                            ++p;
+                        }
+                    }
+                    base += tot;
+                }
+            }
+            warm = lo;  // the next row's first pivot: this row's threshold
+            float ws = 0.0f;
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (winmask & (1u << (v * 4 + c))) ws = __fadd_rn(ws, __fmul_rn(vbuf[v * 128 + lane4 + c], vmul));
+            const float wsum = warp_sum(ws);
+            const float scale = a.renorm ? (wsum > 0.0f ? __fdiv_rn(a.scaling, wsum) : 0.0f) : a.scaling;
+            dense_rows();
+            __syncwarp();  // the winners' writes below land after every lane's zeros
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (winmask & (1u << (v * 4 + c))) {
+                        const int e = v * 128 + lane4 + c;
+                        if (prow) store_scalar<InT>(prow + e, __fmul_rn(__fmul_rn(vbuf[e], vmul), scale));
+                        if (mrow) mrow[e] = 1;
+                    }
+            return scale;
         }
         auto comp = [&](uint32_t k, int v, int c) {
             return (static_cast<unsigned long long>(k) << 32) |
@@ -545,35 +641,7 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
     //    vectors and the k_r winners are patched in afterwards (compact outputs:
     //    emit_compact)
     if (a.probs || a.map || a.inter) {
-        InT* prow = a.probs ? static_cast<InT*>(a.probs) + static_cast<size_t>(t) * E : nullptr;
-        uint8_t* mrow = a.map ? a.map + static_cast<size_t>(t) * E : nullptr;
-        float* irow = a.inter ? a.inter + static_cast<size_t>(t) * E : nullptr;
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            const int e0 = v * 128 + lane4;
-            if (!FULL && e0 >= E) continue;
-            if (vec && whole(v)) {
-                if (irow) {
-                    const float4 q = *reinterpret_cast<const float4*>(vbuf + e0);
-                    const float2 xy = __fmul2_rn(make_float2(q.x, q.y), make_float2(vmul, vmul));
-                    const float2 zw = __fmul2_rn(make_float2(q.z, q.w), make_float2(vmul, vmul));
-                    *reinterpret_cast<float4*>(irow + e0) = make_float4(xy.x, xy.y, zw.x, zw.y);
-                }
-                if (prow) {
-                    const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                    store4<InT>(prow + e0, z);
-                }
-                if (mrow) *reinterpret_cast<uint32_t*>(mrow + e0) = 0u;
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (!inside(v, c)) break;
-                    if (irow) irow[e0 + c] = __fmul_rn(vbuf[e0 + c], vmul);
-                    if (prow) store_scalar<InT>(prow + e0 + c, 0.0f);
-                    if (mrow) mrow[e0 + c] = 0;
-                }
-            }
-        }
+        dense_rows();
         __syncwarp();  // the winners' writes below land after the zeros above
         if (prow || mrow) {
             for (int j = lane; j < k_r; j += 32) {

@@ -129,11 +129,11 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
                 float b[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 if (a.bias) {
                     if (vec && whole(v)) {
-                        const float4 q = __ldg(reinterpret_cast<const float4*>(a.bias + e0));
+                        const float4 q = __ldcg(reinterpret_cast<const float4*>(a.bias + e0));
                         b[0] = q.x; b[1] = q.y; b[2] = q.z; b[3] = q.w;
                     } else {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) b[c] = (e0 + c < E) ? __ldg(a.bias + e0 + c) : 0.0f;
+                        for (int c = 0; c < 4; ++c) b[c] = (e0 + c < E) ? __ldcg(a.bias + e0 + c) : 0.0f;
                     }
                 }
                 const float2 s01 = sigmoid_f32x2(make_float2(x[u][0], x[u][1]));

@@ -4,6 +4,14 @@
 //
 //   k_sort_small    at most kSortChunk pairs: ONE CTA counts, scans, scatters
 //                   and pads (one launch)
+//   k_sort_cluster  up to cs*1024*2 pairs (cs = 16 CTAs where the GPU allows
+//                   clusters that large, else 8): ONE launch of one
+//                   thread-block cluster; each CTA keeps its share of the ids
+//                   in registers, counts them per warp, and the cluster's CTAs
+//                   prefix the counts across CTAs, scan the padded counts and
+//                   exchange the offsets through distributed shared memory
+//                   before every CTA places its pairs and pads its share of the
+//                   blocks (no workspace)
 //   k_sort_hist     CTA c counts the experts of flat pairs [c*PC, (c+1)*PC);
 //                   clusters of 8 consecutive chunks turn their counts into
 //                   within-cluster prefixes pre[c][e] and cluster totals
@@ -19,6 +27,8 @@
 //
 // Every CTA reads the cluster totals (chunks / 8 rows), never the whole
 // per-chunk table, so the cost grows about linearly with the pairs.
+#include <mutex>
+
 #include "internal.h"
 #include "sort.cuh"
 
@@ -27,7 +37,7 @@ namespace mr {
 // Counts the experts of flat pairs [f0, f1) (f1 - f0 <= kSortChunk, at most
 // kSortChunk / kSortThreads per thread) into hist (shared, zeroed); ids outside
 // [0, E_tot) are skipped and reported in *status.
-__device__ __forceinline__ void cta_count(const int32_t* __restrict__ idx, int f0, int f1, int E_tot,
+__device__ __forceinline__ void cta_count(const int32_t* idx, int f0, int f1, int E_tot,
                                           uint32_t* hist, int32_t* status)
 {
     const int tid = threadIdx.x, lane = tid & 31;
@@ -38,7 +48,7 @@ __device__ __forceinline__ void cta_count(const int32_t* __restrict__ idx, int f
 #pragma unroll
     for (int u = 0; u < kSteps; ++u) {
         const int i = f0 + u * kSortThreads + tid;
-        ev[u] = (i < f1) ? __ldg(idx + i) : kInvalidExpert;
+        ev[u] = (i < f1) ? __ldcg(idx + i) : kInvalidExpert;
     }
 #pragma unroll
     for (int u = 0; u < kSteps; ++u) {
@@ -53,12 +63,13 @@ __device__ __forceinline__ void cta_count(const int32_t* __restrict__ idx, int f
     if (__any_sync(kFull, bad) && lane == 0) report_status(status, kStatusRange);
 }
 
-__global__ void __launch_bounds__(kSortThreads) k_sort_small(const int32_t* __restrict__ idx,
-                                                             const float* __restrict__ w, int N, int E_tot, int bm,
-                                                             int32_t* __restrict__ ids, float* __restrict__ sw,
-                                                             int32_t* __restrict__ eids, int32_t* __restrict__ npp,
+__global__ void __launch_bounds__(kSortThreads) k_sort_small(const int32_t* idx,
+                                                             const float* w, int N, int E_tot, int bm,
+                                                             int32_t* ids, float* sw,
+                                                             int32_t* eids, int32_t* npp,
                                                              int32_t* status)
 {
+    pdl_trigger_small();
     extern __shared__ __align__(16) unsigned char smem[];
     unsigned char* p = smem;
     uint32_t* cnt = reinterpret_cast<uint32_t*>(p); p += align16(E_tot * 4);
@@ -69,6 +80,7 @@ __global__ void __launch_bounds__(kSortThreads) k_sort_small(const int32_t* __re
     const int tid = threadIdx.x;
     for (int e = tid; e < E_tot; e += blockDim.x) cnt[e] = 0u;
     __syncthreads();
+    pdl_wait();
     cta_count(idx, 0, N, E_tot, cnt, status);
     __syncthreads();
     for (int e = tid; e < E_tot; e += blockDim.x) off[e] = (cnt[e] + bm - 1) / bm * bm;
@@ -85,13 +97,15 @@ __global__ void __launch_bounds__(kSortThreads) k_sort_small(const int32_t* __re
 }
 
 __global__ void __cluster_dims__(kClusterChunks, 1, 1) __launch_bounds__(kSortThreads)
-    k_sort_hist(const int32_t* __restrict__ idx, int N, int PC, int E_tot, uint32_t* __restrict__ pre,
-                uint32_t* __restrict__ ctot, int32_t* status)
+    k_sort_hist(const int32_t* idx, int N, int PC, int E_tot, uint32_t* pre,
+                uint32_t* ctot, int32_t* status)
 {
+    pdl_trigger_small();
     extern __shared__ __align__(16) uint32_t hist[];
     const int tid = threadIdx.x;
     for (int e = tid; e < E_tot; e += blockDim.x) hist[e] = 0u;
     __syncthreads();
+    pdl_wait();
     const long long f0l = static_cast<long long>(blockIdx.x) * PC;
     const int f0 = static_cast<int>(f0l < N ? f0l : N);
     const int f1 = min(f0 + PC, N);
@@ -125,11 +139,12 @@ __host__ __device__ inline ScatterLayout scatter_layout(int E_tot, int threads)
 }
 
 __global__ void __cluster_dims__(kClusterChunks, 1, 1) __launch_bounds__(kSortThreads)
-    k_sort_scatter(const int32_t* __restrict__ idx, const float* __restrict__ w, int N, int PC, int E_tot, int bm,
-                   int ncl, const uint32_t* __restrict__ pre, const uint32_t* __restrict__ ctot,
-                   int32_t* __restrict__ ids, float* __restrict__ sw, int32_t* __restrict__ eids,
-                   int32_t* __restrict__ npp)
+    k_sort_scatter(const int32_t* idx, const float* w, int N, int PC, int E_tot, int bm,
+                   int ncl, const uint32_t* pre, const uint32_t* ctot,
+                   int32_t* ids, float* sw, int32_t* eids,
+                   int32_t* npp)
 {
+    pdl_trigger_small();
     extern __shared__ __align__(16) unsigned char smem[];
     const ScatterLayout L = scatter_layout(E_tot, blockDim.x);
     uint32_t* s_bsum = reinterpret_cast<uint32_t*>(smem + L.s_bsum);
@@ -156,6 +171,7 @@ __global__ void __cluster_dims__(kClusterChunks, 1, 1) __launch_bounds__(kSortTh
         s_tot[i] = 0u;
     }
     __syncthreads();
+    pdl_wait();
     {
         const int nblk = (len + 31) / 32;
         const int parts = max(1, nw / max(1, nblk));
@@ -168,7 +184,7 @@ __global__ void __cluster_dims__(kClusterChunks, 1, 1) __launch_bounds__(kSortTh
             if (i < len) {
 #pragma unroll 4
                 for (int q = q0; q < q1; ++q) {
-                    const uint32_t v = __ldg(ctot + static_cast<size_t>(q) * E_tot + e0 + i);
+                    const uint32_t v = __ldcg(ctot + static_cast<size_t>(q) * E_tot + e0 + i);
                     before += q < g ? v : 0u;
                     total += v;
                 }
@@ -191,7 +207,7 @@ __global__ void __cluster_dims__(kClusterChunks, 1, 1) __launch_bounds__(kSortTh
     uint32_t soff = 0u, all = 0u;
 #pragma unroll
     for (int q = 0; q < kClusterChunks; ++q) {
-        const uint32_t t = ld_shared_cluster(map_shared_rank(s_slice, static_cast<uint32_t>(q)));
+        const uint32_t t = *cluster_peer(s_slice, static_cast<uint32_t>(q));
         soff += static_cast<uint32_t>(q) < r ? t : 0u;
         all += t;
     }
@@ -206,10 +222,10 @@ __global__ void __cluster_dims__(kClusterChunks, 1, 1) __launch_bounds__(kSortTh
         const uint32_t* prow = pre + static_cast<size_t>(c) * E_tot;
         for (int e = tid; e < E_tot; e += blockDim.x) {
             const uint32_t q = static_cast<uint32_t>(e / S);
-            const uint32_t i4 = 4u * static_cast<uint32_t>(e - static_cast<int>(q) * S);
-            base[e] = ld_shared_cluster(map_shared_rank(s_bsum, q) + i4) + __ldg(prow + e);
-            off[e] = ld_shared_cluster(map_shared_rank(s_off, q) + i4);
-            cnt[e] = ld_shared_cluster(map_shared_rank(s_tot, q) + i4);
+            const int i = e - static_cast<int>(q) * S;
+            base[e] = cluster_peer(s_bsum, q)[i] + __ldcg(prow + e);
+            off[e] = cluster_peer(s_off, q)[i];
+            cnt[e] = cluster_peer(s_tot, q)[i];
         }
         if (tid == 0) off[E_tot] = all;
     }
@@ -224,6 +240,119 @@ __global__ void __cluster_dims__(kClusterChunks, 1, 1) __launch_bounds__(kSortTh
     const long long nb = all / static_cast<uint32_t>(bm);
     const int G = gridDim.x;
     const int b0 = static_cast<int>(nb * c / G), b1 = static_cast<int>(nb * (c + 1) / G);
+    cta_fill_pad_blocks(off, cnt, E_tot, b0, b1, bm, N, ids, sw, eids);
+}
+
+// Shared memory of k_sort_cluster for cs CTAs: per-warp counts, the CTA's
+// per-expert arrays, and its slice of the experts (S = ceil(E_tot / cs)).
+struct ClusterSortLayout {
+    int wh, hist, base, off, cnt, s_pre, s_tot, s_off, s_slice, tmp, bytes;
+};
+
+__host__ __device__ inline ClusterSortLayout cluster_sort_layout(int E_tot, int cs)
+{
+    const int S = (E_tot + cs - 1) / cs;
+    ClusterSortLayout L;
+    int o = 0;
+    L.wh = o; o += align16((kClusterSortThreads / 32) * E_tot * 2);
+    L.hist = o; o += align16(E_tot * 4);
+    L.base = o; o += align16(E_tot * 4);
+    L.off = o; o += align16((E_tot + 1) * 4);
+    L.cnt = o; o += align16(E_tot * 4);
+    L.s_pre = o; o += align16(cs * S * 4);
+    L.s_tot = o; o += align16(S * 4);
+    L.s_off = o; o += align16(S * 4);
+    L.s_slice = o; o += 16;
+    L.tmp = o; o += align16(33 * 4);
+    L.bytes = o;
+    return L;
+}
+
+// CTA r of the cluster handles flat pairs [r*P, (r+1)*P), P <= 1024 * 2.
+__global__ void __launch_bounds__(kClusterSortThreads, 1)
+    k_sort_cluster(const int32_t* idx, const float* w, int N, int P, int E_tot, int bm,
+                   int32_t* ids, float* sw, int32_t* eids,
+                   int32_t* npp, int32_t* status)
+{
+    pdl_trigger_small();
+    pdl_wait();
+    extern __shared__ __align__(16) unsigned char smem[];
+    const uint32_t cs = cluster_nctarank(), r = cluster_ctarank();
+    const ClusterSortLayout L = cluster_sort_layout(E_tot, static_cast<int>(cs));
+    uint16_t* wh = reinterpret_cast<uint16_t*>(smem + L.wh);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L.hist);
+    uint32_t* base = reinterpret_cast<uint32_t*>(smem + L.base);
+    uint32_t* off = reinterpret_cast<uint32_t*>(smem + L.off);
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + L.cnt);
+    uint32_t* s_pre = reinterpret_cast<uint32_t*>(smem + L.s_pre);
+    uint32_t* s_tot = reinterpret_cast<uint32_t*>(smem + L.s_tot);
+    uint32_t* s_off = reinterpret_cast<uint32_t*>(smem + L.s_off);
+    uint32_t* s_slice = reinterpret_cast<uint32_t*>(smem + L.s_slice);
+    uint32_t* tmp = reinterpret_cast<uint32_t*>(smem + L.tmp);
+    const int tid = threadIdx.x, lane = tid & 31, nw = blockDim.x >> 5;
+    const long long f0l = static_cast<long long>(r) * P;
+    const int f0 = static_cast<int>(f0l < N ? f0l : N), f1 = min(N, f0 + P);
+
+    // 1. the CTA's pairs into registers, counted per warp
+    WarpRuns<kClusterSortUseSteps> R;
+    const bool bad = warp_runs_count<kClusterSortUseSteps>(idx, w, f0, f1, E_tot, wh, R);
+    if (__any_sync(kFull, bad) && lane == 0) report_status(status, kStatusRange);
+    __syncthreads();
+    // 2. the CTA's count per expert; the warps' counts become exclusive prefixes
+    for (int e = tid; e < E_tot; e += blockDim.x) {
+        uint32_t run = 0u;
+        for (int q = 0; q < nw; ++q) {
+            const uint32_t c = wh[q * E_tot + e];
+            wh[q * E_tot + e] = static_cast<uint16_t>(run);
+            run += c;
+        }
+        hist[e] = run;
+    }
+    cluster_sync();
+    // 3. the CTA's slice of the experts: each CTA's exclusive prefix over the
+    //    cluster (counts read from the other CTAs), totals and padded counts
+    const int S = (E_tot + static_cast<int>(cs) - 1) / static_cast<int>(cs);
+    const int e0 = min(E_tot, static_cast<int>(r) * S), len = min(E_tot, e0 + S) - e0;
+    for (int i = tid; i < len; i += blockDim.x) {
+        uint32_t run = 0u;
+#pragma unroll 4
+        for (uint32_t q = 0; q < cs; ++q) {
+            const uint32_t v = cluster_peer(hist, q)[e0 + i];
+            s_pre[q * S + i] = run;
+            run += v;
+        }
+        s_tot[i] = run;
+        s_off[i] = (run + bm - 1) / bm * bm;
+    }
+    __syncthreads();
+    const uint32_t Ps = cta_exclusive_scan(s_off, len, tmp);
+    if (tid == 0) s_slice[0] = Ps;
+    cluster_sync();
+    // 4. the slice's start from the other slices' padded totals
+    uint32_t soff = 0u, all = 0u;
+    for (uint32_t q = 0; q < cs; ++q) {
+        const uint32_t t = *cluster_peer(s_slice, q);
+        soff += q < r ? t : 0u;
+        all += t;
+    }
+    for (int i = tid; i < len; i += blockDim.x) s_off[i] += soff;
+    cluster_sync();
+    // 5. every expert's offset, count and this CTA's base, from the slice owners
+    for (int e = tid; e < E_tot; e += blockDim.x) {
+        const uint32_t q = static_cast<uint32_t>(e / S);
+        const uint32_t i = static_cast<uint32_t>(e) - q * static_cast<uint32_t>(S);
+        const uint32_t o = cluster_peer(s_off, q)[i];
+        base[e] = o + cluster_peer(s_pre, q)[r * static_cast<uint32_t>(S) + i];
+        off[e] = o;
+        cnt[e] = cluster_peer(s_tot, q)[i];
+    }
+    if (tid == 0) off[E_tot] = all;
+    cluster_sync();  // no CTA reads another CTA's shared memory after this point
+    if (r == 0 && tid == 0) *npp = static_cast<int32_t>(all);
+    // 6. the pairs, and the CTA's share of the padded blocks
+    warp_runs_place<kClusterSortUseSteps>(R, E_tot, base, wh, ids, sw);
+    const long long nb = all / static_cast<uint32_t>(bm);
+    const int b0 = static_cast<int>(nb * r / cs), b1 = static_cast<int>(nb * (r + 1) / cs);
     cta_fill_pad_blocks(off, cnt, E_tot, b0, b1, bm, N, ids, sw, eids);
 }
 
@@ -242,20 +371,85 @@ int launch_sort_scatter(const int32_t* idx, const float* w, int N, int PC, int n
     const size_t smem = scatter_smem_bytes(E_tot);
     int err = ensure_smem(reinterpret_cast<const void*>(k_sort_scatter), smem);
     if (err != cudaSuccess) return err;
-    k_sort_scatter<<<nchunk_pad, kSortThreads, smem, st>>>(idx, w, N, PC, E_tot, block_m, nchunk_pad / kClusterChunks,
-                                                          pre, ctot, ids, sw, eids, npp);
-    return cudaGetLastError();
+    return launch_kernel(k_sort_scatter, dim3(nchunk_pad), dim3(kSortThreads), smem, st, 0, idx, w, N, PC, E_tot,
+                         block_m, nchunk_pad / kClusterChunks, pre, ctot, ids, sw, eids, npp);
 }
+
+namespace {
+// The largest cluster k_sort_cluster can use with E_tot experts on the current
+// device: 16 where the device schedules non-portable clusters of 16, else 8;
+// 0 if neither fits (the shared memory for E_tot does not). Cached.
+int cluster_sort_size(int E_tot)
+{
+    static std::mutex mu;
+    struct Entry {
+        int dev, E_tot, cs;
+    };
+    static Entry cache[64];
+    static int n = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < n; ++i)
+        if (cache[i].dev == dev && cache[i].E_tot == E_tot) return cache[i].cs;
+    const void* f = reinterpret_cast<const void*>(k_sort_cluster);
+    int cs = 0;
+    int maxsm = 0;
+    if (cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess) {
+        for (int want : {16, 8}) {
+            const size_t smem = static_cast<size_t>(cluster_sort_layout(E_tot, want).bytes);
+            if (smem > static_cast<size_t>(maxsm)) continue;
+            // raise-only: a smaller E_tot probed later must not lower the limit
+            // another size relies on
+            if (ensure_smem(f, smem) != cudaSuccess) continue;
+            if (want > 8 && cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+                continue;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(want, 1, 1);
+            cfg.blockDim = dim3(kClusterSortThreads, 1, 1);
+            cfg.dynamicSmemBytes = smem;
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = want;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, f, &cfg) == cudaSuccess && clusters >= 1) {
+                cs = want;
+                break;
+            }
+        }
+    }
+    cudaGetLastError();  // a refused size above is not an error of the call
+    if (n < 64) cache[n++] = Entry{dev, E_tot, cs};
+    return cs;
+}
+}  // namespace
 
 int launch_sort(const int32_t* idx, const float* w, int N, int E_tot, int block_m, int32_t* ids, float* sw,
                 int32_t* eids, int32_t* npp, uint32_t* ws, int32_t* status, cudaStream_t st)
 {
+    if (N > kSortChunk) {
+        const int cs = cluster_sort_size(E_tot);
+        const long long per_cta = static_cast<long long>(kClusterSortThreads) * kClusterSortUseSteps;
+        if (cs > 0 && N <= cs * per_cta) {
+            // pairs per CTA: whole steps of the CTA's threads
+            const long long P = ((N + cs - 1) / cs + kClusterSortThreads - 1) / kClusterSortThreads * kClusterSortThreads;
+            const size_t smem = static_cast<size_t>(cluster_sort_layout(E_tot, cs).bytes);
+            const int err = ensure_smem(reinterpret_cast<const void*>(k_sort_cluster), smem);
+            if (err != cudaSuccess) return err;
+            return launch_kernel(k_sort_cluster, dim3(cs), dim3(kClusterSortThreads), smem, st, cs, idx, w, N,
+                                 static_cast<int>(P), E_tot, block_m, ids, sw, eids, npp, status);
+        }
+    }
     if (N <= kSortChunk) {
         const size_t smem = small_sort_smem_bytes(E_tot);
         int err = ensure_smem(reinterpret_cast<const void*>(k_sort_small), smem);
         if (err != cudaSuccess) return err;
-        k_sort_small<<<1, kSortThreads, smem, st>>>(idx, w, N, E_tot, block_m, ids, sw, eids, npp, status);
-        return cudaGetLastError();
+        return launch_kernel(k_sort_small, dim3(1), dim3(kSortThreads), smem, st, 0, idx, w, N, E_tot, block_m, ids, sw,
+                             eids, npp, status);
     }
     const SortPlan plan = sort_plan(N, E_tot);
     uint32_t* pre = ws;
@@ -263,8 +457,8 @@ int launch_sort(const int32_t* idx, const float* w, int N, int E_tot, int block_
     const size_t smem_h = static_cast<size_t>(E_tot) * 4;
     int err = ensure_smem(reinterpret_cast<const void*>(k_sort_hist), smem_h);
     if (err != cudaSuccess) return err;
-    k_sort_hist<<<plan.nchunk_pad, kSortThreads, smem_h, st>>>(idx, N, plan.pc, E_tot, pre, ctot, status);
-    err = cudaGetLastError();
+    err = launch_kernel(k_sort_hist, dim3(plan.nchunk_pad), dim3(kSortThreads), smem_h, st, 0, idx, N, plan.pc, E_tot,
+                        pre, ctot, status);
     if (err != cudaSuccess) return err;
     return launch_sort_scatter(idx, w, N, plan.pc, plan.nchunk_pad, E_tot, block_m, pre, ctot, ids, sw, eids, npp,
                                st);

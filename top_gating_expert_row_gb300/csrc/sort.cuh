@@ -27,6 +27,11 @@ namespace mr {
 
 constexpr int kSortThreads = 512;
 constexpr int kSortChunk = 4096;  // flat (token, slot) pairs per sort CTA, at most
+// the one-cluster sort: CTAs of 1024 threads, up to 2 pairs per thread (each
+// warp walks its pairs in serial steps of 32; with more steps the chunked
+// sort's many more warps win)
+constexpr int kClusterSortThreads = 1024;
+constexpr int kClusterSortUseSteps = 2;
 constexpr int kInvalidExpert = -1;
 
 // Warp-aggregated increment of hist[e] for each lane's expert e (lanes with
@@ -72,46 +77,96 @@ __device__ inline uint32_t cta_exclusive_scan(uint32_t* a, int n, uint32_t* tmp)
     return total;
 }
 
-// Stable scatter of flat ids [f0, f1), f1 - f0 <= kSortChunk, by a CTA of at
-// least kSortThreads threads (the sort's CTAs have 512, the fused decode's 512
-// or 1024): then no warp owns more than kMaxSteps steps of 32 ids, the number
-// each warp keeps in registers. base[e] is the absolute position of the first
-// pair of expert e handled by this CTA. wh: nwarps*E_tot 16-bit counters
-// (shared). Pairs with ids outside [0, E_tot) are skipped.
-__device__ inline void cta_scatter(const int32_t* idx, const float* w, int f0, int f1, int E_tot,
-                            const uint32_t* base, uint16_t* wh, int32_t* out_ids, float* out_w)
+// Stable placement of flat ids [f0, f1) by a CTA, in two halves so that the
+// positions can be settled in between (by the CTA alone or by its cluster):
+//   warp_runs_count  each warp owns a contiguous run of ceil(n / warps) ids
+//                    rounded up to 32 (at most STEPS steps of 32, kept in
+//                    registers with their weights) and counts its run's pairs
+//                    per expert into wh[warp][e] (16-bit, shared)
+//   warp_runs_place  writes each pair at base[e] + wh[warp][e] (the warps
+//                    before it, after the caller's exclusive scan over warps)
+//                    + its rank among the warp's earlier pairs of e (per step,
+//                    the lower lanes holding the same expert)
+// Pairs with ids outside [0, E_tot) are skipped.
+template <int STEPS>
+struct WarpRuns {
+    int ev[STEPS];
+    float wv[STEPS];
+    int r0, r1;
+};
+
+// Returns whether any of the thread's ids lay outside [0, E_tot).
+template <int STEPS>
+__device__ __forceinline__ bool warp_runs_count(const int32_t* idx, const float* w, int f0, int f1, int E_tot,
+                                                uint16_t* wh, WarpRuns<STEPS>& R)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     const int n = f1 - f0;
     const int sub = ((n + nw - 1) / nw + 31) & ~31;
-    const int r0 = f0 + warp * sub;
-    const int r1 = min(r0 + sub, f1);
+    R.r0 = min(f1, f0 + warp * sub);
+    R.r1 = min(R.r0 + sub, f1);
     uint16_t* mine = wh + warp * E_tot;
     for (int i = tid; i < nw * E_tot; i += blockDim.x) wh[i] = 0;
-    // the warp's ids, loaded once (all steps in flight) and kept for both passes;
-    // a warp owns ceil(n / warps) ids rounded up to 32, at most kMaxSteps steps
-    // of 32 for n <= kSortChunk and at least kSortThreads / 32 warps
-    constexpr int kMaxSteps = (kSortChunk + kSortThreads - 1) / kSortThreads;
-    int ev[kMaxSteps];
-    float wv[kMaxSteps];  // and their weights
+    // the warp's ids and weights, loaded once (all steps in flight)
+    bool bad = false;
 #pragma unroll
-    for (int u = 0; u < kMaxSteps; ++u) {
-        const int i = r0 + u * 32 + lane;
-        int e = (i < r1) ? idx[i] : kInvalidExpert;
-        ev[u] = (e >= E_tot) ? kInvalidExpert : e;
-        wv[u] = (w && i < r1) ? w[i] : 0.0f;
+    for (int u = 0; u < STEPS; ++u) {
+        const int i = R.r0 + u * 32 + lane;
+        const int e = (i < R.r1) ? idx[i] : kInvalidExpert;
+        bad |= i < R.r1 && (e < 0 || e >= E_tot);
+        R.ev[u] = (e < 0 || e >= E_tot) ? kInvalidExpert : e;
+        R.wv[u] = (w && i < R.r1) ? w[i] : 0.0f;
     }
     __syncthreads();
 #pragma unroll
-    for (int u = 0; u < kMaxSteps; ++u) {
-        if (r0 + u * 32 >= r1) break;
-        const int e = ev[u];
+    for (int u = 0; u < STEPS; ++u) {
+        if (R.r0 + u * 32 >= R.r1) break;
+        const int e = R.ev[u];
         const unsigned peers = __match_any_sync(kFull, e);
         if (e >= 0 && lane == __ffs(peers) - 1) mine[e] = static_cast<uint16_t>(mine[e] + __popc(peers));
         __syncwarp();
     }
+    return bad;
+}
+
+template <int STEPS>
+__device__ __forceinline__ void warp_runs_place(const WarpRuns<STEPS>& R, int E_tot, const uint32_t* base,
+                                                uint16_t* wh, int32_t* out_ids, float* out_w)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint16_t* mine = wh + warp * E_tot;
+    const unsigned lt = lanemask_lt();
+#pragma unroll
+    for (int u = 0; u < STEPS; ++u) {
+        if (R.r0 + u * 32 >= R.r1) break;
+        const int i = R.r0 + u * 32 + lane;
+        const int e = R.ev[u];
+        const unsigned peers = __match_any_sync(kFull, e);
+        if (e >= 0) {
+            const uint32_t pos = base[e] + mine[e] + __popc(peers & lt);
+            out_ids[pos] = i;
+            if (out_w) out_w[pos] = R.wv[u];
+        }
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) mine[e] = static_cast<uint16_t>(mine[e] + __popc(peers));
+        __syncwarp();
+    }
+}
+
+// Stable scatter of flat ids [f0, f1), f1 - f0 <= kSortChunk, by a CTA of at
+// least kSortThreads threads (then no warp owns more than kSortChunk /
+// kSortThreads steps of 32). base[e] is the absolute position of the first
+// pair of expert e handled by this CTA. wh: nwarps*E_tot 16-bit counters
+// (shared).
+__device__ inline void cta_scatter(const int32_t* idx, const float* w, int f0, int f1, int E_tot,
+                                   const uint32_t* base, uint16_t* wh, int32_t* out_ids, float* out_w)
+{
+    constexpr int kSteps = (kSortChunk + kSortThreads - 1) / kSortThreads;
+    const int nw = blockDim.x >> 5;
+    WarpRuns<kSteps> R;
+    warp_runs_count<kSteps>(idx, w, f0, f1, E_tot, wh, R);
     __syncthreads();
-    for (int e = tid; e < E_tot; e += blockDim.x) {
+    for (int e = threadIdx.x; e < E_tot; e += blockDim.x) {
         uint32_t run = 0u;
         for (int q = 0; q < nw; ++q) {
             const uint32_t c = wh[q * E_tot + e];
@@ -120,22 +175,7 @@ __device__ inline void cta_scatter(const int32_t* idx, const float* w, int f0, i
         }
     }
     __syncthreads();
-    const unsigned lt = lanemask_lt();
-#pragma unroll
-    for (int u = 0; u < kMaxSteps; ++u) {
-        if (r0 + u * 32 >= r1) break;
-        const int i = r0 + u * 32 + lane;
-        const int e = ev[u];
-        const unsigned peers = __match_any_sync(kFull, e);
-        if (e >= 0) {
-            const uint32_t pos = base[e] + mine[e] + __popc(peers & lt);
-            out_ids[pos] = i;
-            if (out_w) out_w[pos] = wv[u];
-        }
-        __syncwarp();
-        if (e >= 0 && lane == __ffs(peers) - 1) mine[e] = static_cast<uint16_t>(mine[e] + __popc(peers));
-        __syncwarp();
-    }
+    warp_runs_place<kSteps>(R, E_tot, base, wh, out_ids, out_w);
 }
 
 // Chunks of flat pairs per thread-block cluster of the sort (and of the route
@@ -157,13 +197,13 @@ __device__ inline void cluster_prefix_counts(const uint32_t* hist, int E_tot, ui
     const size_t g = blockIdx.x / kClusterChunks;
     const int S = (E_tot + kClusterChunks - 1) / kClusterChunks;
     const int e0 = static_cast<int>(r) * S, e1 = min(E_tot, e0 + S);
-    uint32_t remote[kClusterChunks];
+    const uint32_t* remote[kClusterChunks];
 #pragma unroll
-    for (int q = 0; q < kClusterChunks; ++q) remote[q] = map_shared_rank(hist, static_cast<uint32_t>(q));
+    for (int q = 0; q < kClusterChunks; ++q) remote[q] = cluster_peer(hist, static_cast<uint32_t>(q));
     for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += blockDim.x) {
         uint32_t v[kClusterChunks];
 #pragma unroll
-        for (int q = 0; q < kClusterChunks; ++q) v[q] = ld_shared_cluster(remote[q] + 4u * e);
+        for (int q = 0; q < kClusterChunks; ++q) v[q] = remote[q][e];
         uint32_t run = 0u;
 #pragma unroll
         for (int q = 0; q < kClusterChunks; ++q) {
