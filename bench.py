@@ -306,7 +306,7 @@ def bf16_rates(mr, dev, stream, calls=20, replays=5) -> dict:
     return out
 
 
-def decode_latency(mr, dev, stream, n_calls=200, Ts=synth.DECODE_TS, shape=synth.decode) -> dict:
+def decode_latency(mr, dev, stream, n_calls=200, Ts=synth.DECODE_BENCH_TS, shape=synth.decode) -> dict:
     """Fused vs unfused decode route+sort (default E=256, topk=8, bf16), eager and graph."""
     L = mr._lib
     res = {}
@@ -779,7 +779,7 @@ def main():
                     help="step: the timed step only; decode: the decode latency table only "
                          "(both used for profiling captures)")
     ap.add_argument("--decode-calls", type=int, default=200, help="calls per decode timing loop")
-    ap.add_argument("--decode-ts", default=",".join(str(t) for t in synth.DECODE_TS),
+    ap.add_argument("--decode-ts", default=",".join(str(t) for t in synth.DECODE_BENCH_TS),
                     help="decode token counts, comma separated")
     ap.add_argument("--workload", choices=sorted(STEP_WORKLOADS), default="softmax_T8192_E2304_k36",
                     help="workload of the timed step (default: the headline one)")
@@ -802,7 +802,7 @@ def main():
         if rank == 0:
             ts = tuple(int(t) for t in args.decode_ts.split(","))
             print(json.dumps({"decode_gpt_oss": decode_latency(mr, dev, torch.cuda.Stream(device=dev),
-                                                               args.decode_calls, (1, 4, 16, 32, 64),
+                                                               args.decode_calls, (1, 4, 16, 32, 64, 128, 256),
                                                                synth.decode_gpt_oss)}), flush=True)
             print(json.dumps({"decode": decode_latency(mr, dev, torch.cuda.Stream(device=dev),
                                                        args.decode_calls, ts)}), flush=True)
@@ -897,7 +897,7 @@ def main():
         line["e2e"] = e2e_rate(mr, w, dev, stream)
         if rank == 0:
             line["decode"] = decode_latency(mr, dev, stream, args.decode_calls)
-            line["decode_gpt_oss"] = decode_latency(mr, dev, stream, args.decode_calls, (1, 4, 16, 32, 64),
+            line["decode_gpt_oss"] = decode_latency(mr, dev, stream, args.decode_calls, (1, 4, 16, 32, 64, 128, 256),
                                                     synth.decode_gpt_oss)
             line["prefill_route_sort"] = prefill_route_sort(mr, dev, stream)
             line["sort_scaling"] = sort_scaling(mr, dev, stream)

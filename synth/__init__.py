@@ -150,6 +150,8 @@ def decode_gpt_oss(T: int) -> Workload:
 
 
 DECODE_TS = (1, 2, 4, 8, 12, 16, 24, 32, 48, 64)
+# decode and small-batch sizes of the benchmark's latency tables (to 256 tokens)
+DECODE_BENCH_TS = DECODE_TS + (96, 128, 192, 256)
 
 
 def large_softmax(topk: int) -> Workload:

@@ -111,6 +111,14 @@ FUSED = [synth.decode(T) for T in synth.DECODE_TS] + [synth.decode_gpt_oss(T) fo
     synth.Workload("fallback_T300_grouped", 300, 384, 9, synth.SIGMOID, synth.BF16, renorm=1, scaling=2.827,
                    n_group=8, topk_group=4, n_shared=1, bias_range=0.05, block_m=64),
     synth.Workload("fallback_wide_T4_e2304", 4, 2304, 36, synth.SOFTMAX, synth.F32, block_m=8),
+    # one thread-block cluster, a warp per token, up to 512 tokens
+    synth.Workload("cluster_T128_e256_k8", 128, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
+    synth.Workload("cluster_T512_e256_k8", 512, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
+    synth.Workload("cluster_T256_e128_k4", 256, 128, 4, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
+    synth.Workload("cluster_T100_e1024_k36", 100, 1024, 36, synth.SOFTMAX, synth.F32, block_m=16),
+    synth.Workload("cluster_T333_e100_sigmoid", 333, 100, 6, synth.SIGMOID, synth.F32, renorm=1, scaling=1.5,
+                   bias_range=0.1, block_m=8),
+    synth.Workload("separate_T513_e256_k8", 513, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
     # above 4096 pairs: the forward, then the one-cluster sort (or the chunked one)
     synth.Workload("prefill_T600_e256_k8", 600, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
     synth.Workload("prefill_T5000_e100_k5_sigmoid", 5000, 100, 5, synth.SIGMOID, synth.F32, renorm=1, scaling=1.5,

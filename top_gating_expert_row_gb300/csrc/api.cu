@@ -81,8 +81,56 @@ int ensure_smem(const void* func, size_t bytes)
     return cudaSuccess;
 }
 
+bool cluster_fits(const void* func, int threads, size_t smem, int cs)
+{
+    struct Entry {
+        const void* func;
+        size_t smem;
+        int dev, cs;
+        bool fits;
+    };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int n = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        for (int i = 0; i < n; ++i)
+            if (cache[i].func == func && cache[i].smem == smem && cache[i].dev == dev && cache[i].cs == cs)
+                return cache[i].fits;
+    }
+    bool fits = false;
+    int maxsm = 0;
+    if (cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+        smem <= static_cast<size_t>(maxsm) && ensure_smem(func, smem) == cudaSuccess &&
+        (cs <= 8 || cudaFuncSetAttribute(func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess)) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cs, 1, 1);
+        cfg.blockDim = dim3(threads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = cs;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        fits = cudaOccupancyMaxActiveClusters(&clusters, func, &cfg) == cudaSuccess && clusters >= 1;
+    }
+    cudaGetLastError();  // a refused size is not an error of the call
+    std::lock_guard<std::mutex> lk(mu);
+    if (n < 64) cache[n++] = Entry{func, smem, dev, cs, fits};
+    return fits;
+}
+
 // ---- per-(score, dtype) launchers defined in fwd.cu compilations --------------------------------
 
+int launch_fused_cluster_s0_d0(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
+int launch_fused_cluster_s0_d1(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
+int launch_fused_cluster_s1_d0(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
+int launch_fused_cluster_s1_d1(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
 int launch_fwd_s0_d0(const RouteArgs&, int, bool, cudaStream_t);
 int launch_fwd_s0_d1(const RouteArgs&, int, bool, cudaStream_t);
 int launch_fwd_s1_d0(const RouteArgs&, int, bool, cudaStream_t);
@@ -97,6 +145,14 @@ int launch_fwd(int score_fn, int in_dtype, const RouteArgs& a, int nv_idx, bool 
     if (score_fn == kSoftmax)
         return in_dtype ? launch_fwd_s0_d1(a, nv_idx, select, st) : launch_fwd_s0_d0(a, nv_idx, select, st);
     return in_dtype ? launch_fwd_s1_d1(a, nv_idx, select, st) : launch_fwd_s1_d0(a, nv_idx, select, st);
+}
+
+int launch_fused_cluster(int score_fn, int in_dtype, const RouteArgs& a, const SortArgs& s, int nv_idx, bool select,
+                         cudaStream_t st)
+{
+    auto f = score_fn == kSoftmax ? (in_dtype ? launch_fused_cluster_s0_d1 : launch_fused_cluster_s0_d0)
+                                  : (in_dtype ? launch_fused_cluster_s1_d1 : launch_fused_cluster_s1_d0);
+    return f(a, s, nv_idx, select, st);
 }
 
 int launch_fused_decode(int score_fn, int in_dtype, const RouteArgs& a, const SortArgs& s, int nv_idx,
@@ -619,6 +675,17 @@ int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int
     const int nv = nv_index(p->E);
     if (nv < 0) return MR_EUNSUPPORTED;
     const int k_r = p->topk - p->n_shared;
+    // above 16 tokens, rows held in registers: one launch of one thread-block
+    // cluster when one fits (else the one-CTA kernel up to 64 tokens, or the
+    // separate launches)
+    if (p->T > 16 && p->T <= kFusedClusterMaxTokens && kNvBuckets[nv] <= kRegisterMaxNv) {
+        RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, topk_idx, topk_w, status);
+        SortArgs s{sorted_token_ids, sorted_weights, expert_ids, num_tokens_post_pad, E_tot, block_m,
+                   log2_if_pow2(block_m)};
+        const int e = launch_fused_cluster(p->score_fn, p->in_dtype, a, s, nv, use_select(k_r), st);
+        if (e != cudaErrorNotSupported) return from_cuda(e);
+        cudaGetLastError();
+    }
     if (fused_one_launch(p->T, kNvBuckets[nv])) {
         RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, topk_idx, topk_w, status);
         SortArgs s{sorted_token_ids, sorted_weights, expert_ids, num_tokens_post_pad, E_tot, block_m,

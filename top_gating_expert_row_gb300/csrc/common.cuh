@@ -362,6 +362,13 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of cluster_sync: arrive (does not block) and wait (blocks
+// until every thread of the cluster has arrived). A CTA that reads another
+// CTA's shared memory arrives once its last such read is done and waits before
+// it exits, so no CTA leaves while its shared memory may still be read.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
 // Generic pointer to the same variable in the shared memory of the cluster's
 // CTA `rank`: plain loads through it reach that CTA's shared memory, and the
 // compiler is free to keep several in flight (the cluster barriers, whose asm

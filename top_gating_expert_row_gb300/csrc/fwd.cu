@@ -10,6 +10,10 @@
 //                    the whole CTA histograms, scans and scatters the T*topk
 //                    pairs in shared memory (FlyDSL PR 582, fused top-k gating
 //                    + MoE sorting at decode sizes)
+//   k_fused_cluster  ONE thread-block cluster for up to 32 tokens per CTA:
+//                    each warp routes a token, the CTAs keep their pairs in
+//                    shared memory and the cluster sorts them together
+//                    (cluster_sort_runs), so larger batches stay one launch
 #include <type_traits>
 
 #include "internal.h"
@@ -245,6 +249,53 @@ __global__ void __launch_bounds__(THREADS, 1) k_fused_decode(RouteArgs a, SortAr
     }
 }
 
+// Fused route + sort in one launch of one thread-block cluster (cs CTAs of 32
+// warps): CTA r routes tokens [r*TP, min(T, (r+1)*TP)), a warp per token,
+// writes the compact outputs and keeps the pairs in shared memory, then the
+// cluster sorts all T*topk pairs (each CTA places its own pairs).
+template <int NV, bool SELECT, bool FULL>
+__global__ void __launch_bounds__(kClusterSortThreads, 1) k_fused_cluster(RouteArgs a, SortArgs s, int TP)
+{
+    pdl_trigger_small();
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, SELECT, a.n_group > 0);
+    const int pairs = align16(TP * a.topk * 4);
+    int32_t* s_idx = reinterpret_cast<int32_t*>(smem + static_cast<size_t>(nw) * L.bytes);
+    float* s_w = reinterpret_cast<float*>(smem + static_cast<size_t>(nw) * L.bytes + pairs);
+    unsigned char* sort_smem = smem + static_cast<size_t>(nw) * L.bytes + 2 * pairs;
+    const int r = static_cast<int>(cluster_ctarank());
+    const int t0 = min(a.T, r * TP), t1 = min(a.T, t0 + TP);
+    pdl_wait();
+    {
+        unsigned char* wsm = smem + static_cast<size_t>(warp) * L.bytes;
+        uint32_t warm = 0u;
+        for (int tok = t0 + warp; tok < t1; tok += nw) {
+            const float scale = route_row<kScore, InT, NV, SELECT, FULL>(a, tok, wsm, L, lane, warm);
+            const size_t o = static_cast<size_t>(tok) * a.topk;
+            const int lo = (tok - t0) * a.topk;
+            const uint32_t* win_idx = reinterpret_cast<const uint32_t*>(wsm + L.win_idx);
+            const float* win_val = reinterpret_cast<const float*>(wsm + L.win_val);
+            for (int j = lane; j < a.topk; j += 32) {  // compact outputs, to shared and global
+                const bool routed = j < a.k_r;
+                const int32_t id = routed ? static_cast<int32_t>(win_idx[j]) : a.E + (j - a.k_r);
+                const float wv = routed ? __fmul_rn(win_val[j], scale) : a.shared_weight;
+                s_idx[lo + j] = id;
+                s_w[lo + j] = wv;
+                if (a.topk_idx) a.topk_idx[o + j] = id;
+                if (a.topk_w) a.topk_w[o + j] = wv;
+            }
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    const int f0 = t0 * a.topk, f1 = t1 * a.topk;
+    WarpRuns<kClusterSortUseSteps> R;
+    const bool bad = warp_runs_load<kClusterSortUseSteps>(s_idx, s_w, f0, f0, f1, s.E_tot, R);
+    cluster_sort_runs<kClusterSortUseSteps>(R, bad, a.T * a.topk, s.E_tot, s.block_m, sort_smem, s.ids, s.w,
+                                            s.expert_ids, s.num_post_pad, a.status);
+}
+
 namespace {
 
 using FwdFn = void (*)(RouteArgs);
@@ -260,6 +311,22 @@ FwdFn fwd_kernel(int nv_idx)
         case 4: return k_router_fwd<4, SELECT, FULL, RANKW, SET>;
         case 6: return k_router_fwd<6, SELECT, FULL, RANKW, SET>;
         case 8: return k_router_fwd<8, SELECT, FULL, RANKW, SET>;
+    }
+    return nullptr;
+}
+
+using ClusterFn = void (*)(RouteArgs, SortArgs, int);
+
+template <bool SELECT, bool FULL>
+ClusterFn cluster_kernel(int nv_idx)
+{
+    switch (kNvBuckets[nv_idx]) {
+        case 1: return k_fused_cluster<1, SELECT, FULL>;
+        case 2: return k_fused_cluster<2, SELECT, FULL>;
+        case 3: return k_fused_cluster<3, SELECT, FULL>;
+        case 4: return k_fused_cluster<4, SELECT, FULL>;
+        case 6: return k_fused_cluster<6, SELECT, FULL>;
+        case 8: return k_fused_cluster<8, SELECT, FULL>;
     }
     return nullptr;
 }
@@ -324,6 +391,30 @@ int MR_CAT(launch_fwd, MR_SUFFIX)(const RouteArgs& a, int nv_idx, bool select, c
     const int grid = persistent_grid(reinterpret_cast<const void*>(f), kFwdThreads, smem, ctas_needed);
     if (grid <= 0) return cudaErrorInvalidConfiguration;
     return launch_kernel(f, dim3(grid), dim3(kFwdThreads), smem, st, 0, a);
+}
+
+// The cluster-fused call: returns cudaErrorNotSupported (nothing launched)
+// when no cluster of this kernel fits the device for these sizes (the caller
+// then runs the separate launches).
+int MR_CAT(launch_fused_cluster, MR_SUFFIX)(const RouteArgs& a, const SortArgs& s, int nv_idx, bool select,
+                                            cudaStream_t st)
+{
+    if (kNvBuckets[nv_idx] > kRegisterMaxNv) return cudaErrorNotSupported;
+    const bool full = a.vec && a.E == 128 * kNvBuckets[nv_idx];
+    const ClusterFn f = select ? (full ? cluster_kernel<true, true>(nv_idx) : cluster_kernel<true, false>(nv_idx))
+                               : (full ? cluster_kernel<false, true>(nv_idx) : cluster_kernel<false, false>(nv_idx));
+    if (!f) return cudaErrorNotSupported;
+    const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, select, a.n_group > 0);
+    for (int cs : {16, 8}) {
+        const int TP = (a.T + cs - 1) / cs;
+        if (TP > kClusterSortThreads / 32 || TP * a.topk > kClusterSortThreads * kClusterSortUseSteps) continue;
+        const size_t smem = static_cast<size_t>(L.bytes) * (kClusterSortThreads / 32) +
+                            2 * static_cast<size_t>(align16(TP * a.topk * 4)) +
+                            static_cast<size_t>(cluster_sort_layout(s.E_tot).bytes);
+        if (!cluster_fits(reinterpret_cast<const void*>(f), kClusterSortThreads, smem, cs)) continue;
+        return launch_kernel(f, dim3(cs), dim3(kClusterSortThreads), smem, st, cs, a, s, TP);
+    }
+    return cudaErrorNotSupported;
 }
 
 int MR_CAT(launch_fused, MR_SUFFIX)(const RouteArgs& a, const SortArgs& s, int nv_idx, bool select,

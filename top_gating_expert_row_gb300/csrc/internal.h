@@ -99,6 +99,12 @@ int launch_fwd(int score_fn, int in_dtype, const RouteArgs& a, int nv_idx, bool 
                cudaStream_t st);
 int launch_fused_decode(int score_fn, int in_dtype, const RouteArgs& a, const SortArgs& s,
                         int nv_idx, bool select, cudaStream_t st);
+// The fused call as one launch of one thread-block cluster (a warp per token);
+// cudaErrorNotSupported, with nothing launched, when no cluster fits.
+int launch_fused_cluster(int score_fn, int in_dtype, const RouteArgs& a, const SortArgs& s, int nv_idx,
+                         bool select, cudaStream_t st);
+// Tokens the cluster-fused call takes at most (32 per CTA, 16 CTAs).
+constexpr int kFusedClusterMaxTokens = 512;
 int launch_bwd(int score_fn, int nv_idx, const float* g, const float* s, const uint8_t* m,
                float* dx, int T, int E, int renorm, float scaling, bool vec, cudaStream_t st);
 int launch_bwd_bf16(int score_fn, int nv_idx, const __nv_bfloat16* g, const float* s, const uint8_t* m,
@@ -200,5 +206,10 @@ int launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, 
 int persistent_grid(const void* func, int threads, size_t smem, long long units);
 // Raise a kernel's dynamic shared-memory limit when needed.
 int ensure_smem(const void* func, size_t smem);
+// Whether a cluster of cs CTAs of this kernel (threads each, smem bytes of
+// dynamic shared memory) fits on the current device; sets the kernel's
+// shared-memory limit and, for cs > 8, allows non-portable cluster sizes.
+// Cached.
+bool cluster_fits(const void* func, int threads, size_t smem, int cs);
 
 }  // namespace mr

@@ -27,8 +27,6 @@
 //
 // Every CTA reads the cluster totals (chunks / 8 rows), never the whole
 // per-chunk table, so the cost grows about linearly with the pairs.
-#include <mutex>
-
 #include "internal.h"
 #include "sort.cuh"
 
@@ -243,117 +241,20 @@ __global__ void __cluster_dims__(kClusterChunks, 1, 1) __launch_bounds__(kSortTh
     cta_fill_pad_blocks(off, cnt, E_tot, b0, b1, bm, N, ids, sw, eids);
 }
 
-// Shared memory of k_sort_cluster for cs CTAs: per-warp counts, the CTA's
-// per-expert arrays, and its slice of the experts (S = ceil(E_tot / cs)).
-struct ClusterSortLayout {
-    int wh, hist, base, off, cnt, s_pre, s_tot, s_off, s_slice, tmp, bytes;
-};
-
-__host__ __device__ inline ClusterSortLayout cluster_sort_layout(int E_tot, int cs)
-{
-    const int S = (E_tot + cs - 1) / cs;
-    ClusterSortLayout L;
-    int o = 0;
-    L.wh = o; o += align16((kClusterSortThreads / 32) * E_tot * 2);
-    L.hist = o; o += align16(E_tot * 4);
-    L.base = o; o += align16(E_tot * 4);
-    L.off = o; o += align16((E_tot + 1) * 4);
-    L.cnt = o; o += align16(E_tot * 4);
-    L.s_pre = o; o += align16(cs * S * 4);
-    L.s_tot = o; o += align16(S * 4);
-    L.s_off = o; o += align16(S * 4);
-    L.s_slice = o; o += 16;
-    L.tmp = o; o += align16(33 * 4);
-    L.bytes = o;
-    return L;
-}
-
 // CTA r of the cluster handles flat pairs [r*P, (r+1)*P), P <= 1024 * 2.
 __global__ void __launch_bounds__(kClusterSortThreads, 1)
-    k_sort_cluster(const int32_t* idx, const float* w, int N, int P, int E_tot, int bm,
-                   int32_t* ids, float* sw, int32_t* eids,
-                   int32_t* npp, int32_t* status)
+    k_sort_cluster(const int32_t* idx, const float* w, int N, int P, int E_tot, int bm, int32_t* ids, float* sw,
+                   int32_t* eids, int32_t* npp, int32_t* status)
 {
     pdl_trigger_small();
     pdl_wait();
     extern __shared__ __align__(16) unsigned char smem[];
-    const uint32_t cs = cluster_nctarank(), r = cluster_ctarank();
-    const ClusterSortLayout L = cluster_sort_layout(E_tot, static_cast<int>(cs));
-    uint16_t* wh = reinterpret_cast<uint16_t*>(smem + L.wh);
-    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L.hist);
-    uint32_t* base = reinterpret_cast<uint32_t*>(smem + L.base);
-    uint32_t* off = reinterpret_cast<uint32_t*>(smem + L.off);
-    uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + L.cnt);
-    uint32_t* s_pre = reinterpret_cast<uint32_t*>(smem + L.s_pre);
-    uint32_t* s_tot = reinterpret_cast<uint32_t*>(smem + L.s_tot);
-    uint32_t* s_off = reinterpret_cast<uint32_t*>(smem + L.s_off);
-    uint32_t* s_slice = reinterpret_cast<uint32_t*>(smem + L.s_slice);
-    uint32_t* tmp = reinterpret_cast<uint32_t*>(smem + L.tmp);
-    const int tid = threadIdx.x, lane = tid & 31, nw = blockDim.x >> 5;
+    const uint32_t r = cluster_ctarank();
     const long long f0l = static_cast<long long>(r) * P;
     const int f0 = static_cast<int>(f0l < N ? f0l : N), f1 = min(N, f0 + P);
-
-    // 1. the CTA's pairs into registers, counted per warp
     WarpRuns<kClusterSortUseSteps> R;
-    const bool bad = warp_runs_count<kClusterSortUseSteps>(idx, w, f0, f1, E_tot, wh, R);
-    if (__any_sync(kFull, bad) && lane == 0) report_status(status, kStatusRange);
-    __syncthreads();
-    // 2. the CTA's count per expert; the warps' counts become exclusive prefixes
-    for (int e = tid; e < E_tot; e += blockDim.x) {
-        uint32_t run = 0u;
-        for (int q = 0; q < nw; ++q) {
-            const uint32_t c = wh[q * E_tot + e];
-            wh[q * E_tot + e] = static_cast<uint16_t>(run);
-            run += c;
-        }
-        hist[e] = run;
-    }
-    cluster_sync();
-    // 3. the CTA's slice of the experts: each CTA's exclusive prefix over the
-    //    cluster (counts read from the other CTAs), totals and padded counts
-    const int S = (E_tot + static_cast<int>(cs) - 1) / static_cast<int>(cs);
-    const int e0 = min(E_tot, static_cast<int>(r) * S), len = min(E_tot, e0 + S) - e0;
-    for (int i = tid; i < len; i += blockDim.x) {
-        uint32_t run = 0u;
-#pragma unroll 4
-        for (uint32_t q = 0; q < cs; ++q) {
-            const uint32_t v = cluster_peer(hist, q)[e0 + i];
-            s_pre[q * S + i] = run;
-            run += v;
-        }
-        s_tot[i] = run;
-        s_off[i] = (run + bm - 1) / bm * bm;
-    }
-    __syncthreads();
-    const uint32_t Ps = cta_exclusive_scan(s_off, len, tmp);
-    if (tid == 0) s_slice[0] = Ps;
-    cluster_sync();
-    // 4. the slice's start from the other slices' padded totals
-    uint32_t soff = 0u, all = 0u;
-    for (uint32_t q = 0; q < cs; ++q) {
-        const uint32_t t = *cluster_peer(s_slice, q);
-        soff += q < r ? t : 0u;
-        all += t;
-    }
-    for (int i = tid; i < len; i += blockDim.x) s_off[i] += soff;
-    cluster_sync();
-    // 5. every expert's offset, count and this CTA's base, from the slice owners
-    for (int e = tid; e < E_tot; e += blockDim.x) {
-        const uint32_t q = static_cast<uint32_t>(e / S);
-        const uint32_t i = static_cast<uint32_t>(e) - q * static_cast<uint32_t>(S);
-        const uint32_t o = cluster_peer(s_off, q)[i];
-        base[e] = o + cluster_peer(s_pre, q)[r * static_cast<uint32_t>(S) + i];
-        off[e] = o;
-        cnt[e] = cluster_peer(s_tot, q)[i];
-    }
-    if (tid == 0) off[E_tot] = all;
-    cluster_sync();  // no CTA reads another CTA's shared memory after this point
-    if (r == 0 && tid == 0) *npp = static_cast<int32_t>(all);
-    // 6. the pairs, and the CTA's share of the padded blocks
-    warp_runs_place<kClusterSortUseSteps>(R, E_tot, base, wh, ids, sw);
-    const long long nb = all / static_cast<uint32_t>(bm);
-    const int b0 = static_cast<int>(nb * r / cs), b1 = static_cast<int>(nb * (r + 1) / cs);
-    cta_fill_pad_blocks(off, cnt, E_tot, b0, b1, bm, N, ids, sw, eids);
+    const bool bad = warp_runs_load<kClusterSortUseSteps>(idx, w, 0, f0, f1, E_tot, R);
+    cluster_sort_runs<kClusterSortUseSteps>(R, bad, N, E_tot, bm, smem, ids, sw, eids, npp, status);
 }
 
 size_t scatter_smem_bytes(int E_tot) { return static_cast<size_t>(scatter_layout(E_tot, kSortThreads).bytes); }
@@ -378,53 +279,14 @@ int launch_sort_scatter(const int32_t* idx, const float* w, int N, int PC, int n
 namespace {
 // The largest cluster k_sort_cluster can use with E_tot experts on the current
 // device: 16 where the device schedules non-portable clusters of 16, else 8;
-// 0 if neither fits (the shared memory for E_tot does not). Cached.
+// 0 if neither fits (the shared memory for E_tot does not).
 int cluster_sort_size(int E_tot)
 {
-    static std::mutex mu;
-    struct Entry {
-        int dev, E_tot, cs;
-    };
-    static Entry cache[64];
-    static int n = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    std::lock_guard<std::mutex> lk(mu);
-    for (int i = 0; i < n; ++i)
-        if (cache[i].dev == dev && cache[i].E_tot == E_tot) return cache[i].cs;
     const void* f = reinterpret_cast<const void*>(k_sort_cluster);
-    int cs = 0;
-    int maxsm = 0;
-    if (cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess) {
-        for (int want : {16, 8}) {
-            const size_t smem = static_cast<size_t>(cluster_sort_layout(E_tot, want).bytes);
-            if (smem > static_cast<size_t>(maxsm)) continue;
-            // raise-only: a smaller E_tot probed later must not lower the limit
-            // another size relies on
-            if (ensure_smem(f, smem) != cudaSuccess) continue;
-            if (want > 8 && cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-                continue;
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(want, 1, 1);
-            cfg.blockDim = dim3(kClusterSortThreads, 1, 1);
-            cfg.dynamicSmemBytes = smem;
-            cudaLaunchAttribute attr;
-            attr.id = cudaLaunchAttributeClusterDimension;
-            attr.val.clusterDim.x = want;
-            attr.val.clusterDim.y = 1;
-            attr.val.clusterDim.z = 1;
-            cfg.attrs = &attr;
-            cfg.numAttrs = 1;
-            int clusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&clusters, f, &cfg) == cudaSuccess && clusters >= 1) {
-                cs = want;
-                break;
-            }
-        }
-    }
-    cudaGetLastError();  // a refused size above is not an error of the call
-    if (n < 64) cache[n++] = Entry{dev, E_tot, cs};
-    return cs;
+    for (int cs : {16, 8})
+        if (cluster_fits(f, kClusterSortThreads, static_cast<size_t>(cluster_sort_layout(E_tot).bytes), cs))
+            return cs;
+    return 0;
 }
 }  // namespace
 
@@ -437,7 +299,7 @@ int launch_sort(const int32_t* idx, const float* w, int N, int E_tot, int block_
         if (cs > 0 && N <= cs * per_cta) {
             // pairs per CTA: whole steps of the CTA's threads
             const long long P = ((N + cs - 1) / cs + kClusterSortThreads - 1) / kClusterSortThreads * kClusterSortThreads;
-            const size_t smem = static_cast<size_t>(cluster_sort_layout(E_tot, cs).bytes);
+            const size_t smem = static_cast<size_t>(cluster_sort_layout(E_tot).bytes);
             const int err = ensure_smem(reinterpret_cast<const void*>(k_sort_cluster), smem);
             if (err != cudaSuccess) return err;
             return launch_kernel(k_sort_cluster, dim3(cs), dim3(kClusterSortThreads), smem, st, cs, idx, w, N,

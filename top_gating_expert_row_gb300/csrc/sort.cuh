@@ -95,28 +95,38 @@ struct WarpRuns {
     int r0, r1;
 };
 
-// Returns whether any of the thread's ids lay outside [0, E_tot).
+// The warp's run of flat pairs [f0, f1) into R (pair i is idx[i - base],
+// w[i - base]; global or shared memory). Returns whether any of the thread's
+// ids lay outside [0, E_tot).
 template <int STEPS>
-__device__ __forceinline__ bool warp_runs_count(const int32_t* idx, const float* w, int f0, int f1, int E_tot,
-                                                uint16_t* wh, WarpRuns<STEPS>& R)
+__device__ __forceinline__ bool warp_runs_load(const int32_t* idx, const float* w, int base, int f0, int f1, int E_tot,
+                                               WarpRuns<STEPS>& R)
 {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int n = f1 - f0;
     const int sub = ((n + nw - 1) / nw + 31) & ~31;
     R.r0 = min(f1, f0 + warp * sub);
     R.r1 = min(R.r0 + sub, f1);
-    uint16_t* mine = wh + warp * E_tot;
-    for (int i = tid; i < nw * E_tot; i += blockDim.x) wh[i] = 0;
     // the warp's ids and weights, loaded once (all steps in flight)
     bool bad = false;
 #pragma unroll
     for (int u = 0; u < STEPS; ++u) {
         const int i = R.r0 + u * 32 + lane;
-        const int e = (i < R.r1) ? idx[i] : kInvalidExpert;
+        const int e = (i < R.r1) ? idx[i - base] : kInvalidExpert;
         bad |= i < R.r1 && (e < 0 || e >= E_tot);
         R.ev[u] = (e < 0 || e >= E_tot) ? kInvalidExpert : e;
-        R.wv[u] = (w && i < R.r1) ? w[i] : 0.0f;
+        R.wv[u] = (w && i < R.r1) ? w[i - base] : 0.0f;
     }
+    return bad;
+}
+
+// The per-warp counts of the loaded runs into wh[warp][e].
+template <int STEPS>
+__device__ __forceinline__ void warp_runs_tally(int E_tot, uint16_t* wh, const WarpRuns<STEPS>& R)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    uint16_t* mine = wh + warp * E_tot;
+    for (int i = tid; i < nw * E_tot; i += blockDim.x) wh[i] = 0;
     __syncthreads();
 #pragma unroll
     for (int u = 0; u < STEPS; ++u) {
@@ -126,6 +136,15 @@ __device__ __forceinline__ bool warp_runs_count(const int32_t* idx, const float*
         if (e >= 0 && lane == __ffs(peers) - 1) mine[e] = static_cast<uint16_t>(mine[e] + __popc(peers));
         __syncwarp();
     }
+}
+
+// warp_runs_load (from pair 0 of idx / w) and warp_runs_tally.
+template <int STEPS>
+__device__ __forceinline__ bool warp_runs_count(const int32_t* idx, const float* w, int f0, int f1, int E_tot,
+                                                uint16_t* wh, WarpRuns<STEPS>& R)
+{
+    const bool bad = warp_runs_load<STEPS>(idx, w, 0, f0, f1, E_tot, R);
+    warp_runs_tally<STEPS>(E_tot, wh, R);
     return bad;
 }
 
@@ -243,6 +262,96 @@ __device__ inline void cta_fill_pad_blocks(const uint32_t* off, const uint32_t* 
         }
         if (lane == 0) expert_ids[b] = lo;
     }
+}
+
+// Shared memory of the one-cluster sort: per-warp counts and the CTA's
+// per-expert arrays.
+struct ClusterSortLayout {
+    int wh, hist, before, base, off, cnt, tmp, bytes;
+};
+
+__host__ __device__ inline ClusterSortLayout cluster_sort_layout(int E_tot)
+{
+    ClusterSortLayout L;
+    int o = 0;
+    L.wh = o; o += align16((kClusterSortThreads / 32) * E_tot * 2);
+    L.hist = o; o += align16(E_tot * 4);
+    L.before = o; o += align16(E_tot * 4);
+    L.base = o; o += align16(E_tot * 4);
+    L.off = o; o += align16((E_tot + 1) * 4);
+    L.cnt = o; o += align16(E_tot * 4);
+    L.tmp = o; o += align16(33 * 4);
+    L.bytes = o;
+    return L;
+}
+
+// The sort of one thread-block cluster (cs CTAs, each with the runs of its
+// pairs already loaded into R): per-warp counts and each CTA's count per
+// expert; after one cluster barrier every CTA reads all CTAs' counts through
+// distributed shared memory (its exclusive prefix over the CTAs before it and
+// the totals), scans the padded totals itself, and places its pairs and its
+// share of the padded blocks. The CTA arrives at a second barrier once its
+// remote reads are done and waits on it only before it exits. `smem` is the
+// CTA's region of cluster_sort_layout(E_tot).bytes. Called by every thread of
+// every CTA of the cluster.
+template <int STEPS>
+__device__ __forceinline__ void cluster_sort_runs(WarpRuns<STEPS>& R, bool bad, int N, int E_tot, int bm,
+                                                  unsigned char* smem, int32_t* ids, float* sw, int32_t* eids,
+                                                  int32_t* npp, int32_t* status)
+{
+    const uint32_t cs = cluster_nctarank(), r = cluster_ctarank();
+    const ClusterSortLayout L = cluster_sort_layout(E_tot);
+    uint16_t* wh = reinterpret_cast<uint16_t*>(smem + L.wh);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L.hist);
+    uint32_t* before = reinterpret_cast<uint32_t*>(smem + L.before);
+    uint32_t* base = reinterpret_cast<uint32_t*>(smem + L.base);
+    uint32_t* off = reinterpret_cast<uint32_t*>(smem + L.off);
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + L.cnt);
+    uint32_t* tmp = reinterpret_cast<uint32_t*>(smem + L.tmp);
+    const int tid = threadIdx.x, lane = tid & 31, nw = blockDim.x >> 5;
+
+    // 1. the CTA's pairs (in registers), counted per warp
+    warp_runs_tally<STEPS>(E_tot, wh, R);
+    if (__any_sync(kFull, bad) && lane == 0) report_status(status, kStatusRange);
+    __syncthreads();
+    // 2. the CTA's count per expert; the warps' counts become exclusive prefixes
+    for (int e = tid; e < E_tot; e += blockDim.x) {
+        uint32_t run = 0u;
+        for (int q = 0; q < nw; ++q) {
+            const uint32_t c = wh[q * E_tot + e];
+            wh[q * E_tot + e] = static_cast<uint16_t>(run);
+            run += c;
+        }
+        hist[e] = run;
+    }
+    cluster_sync();
+    // 3. every CTA's count of every expert: the CTAs before this one, and all
+    for (int e = tid; e < E_tot; e += blockDim.x) {
+        uint32_t b = 0u, t = 0u;
+#pragma unroll 4
+        for (uint32_t q = 0; q < cs; ++q) {
+            const uint32_t v = cluster_peer(hist, q)[e];
+            b += q < r ? v : 0u;
+            t += v;
+        }
+        before[e] = b;
+        cnt[e] = t;
+        off[e] = (t + bm - 1) / bm * bm;
+    }
+    cluster_arrive();  // this CTA reads no other CTA's shared memory after this
+    __syncthreads();
+    // 4. padded offsets, this CTA's base per expert
+    const uint32_t all = cta_exclusive_scan(off, E_tot, tmp);
+    if (tid == 0) off[E_tot] = all;
+    for (int e = tid; e < E_tot; e += blockDim.x) base[e] = off[e] + before[e];
+    __syncthreads();
+    if (r == 0 && tid == 0) *npp = static_cast<int32_t>(all);
+    // 5. the pairs, and the CTA's share of the padded blocks
+    warp_runs_place<STEPS>(R, E_tot, base, wh, ids, sw);
+    const long long nb = all / static_cast<uint32_t>(bm);
+    const int b0 = static_cast<int>(nb * r / cs), b1 = static_cast<int>(nb * (r + 1) / cs);
+    cta_fill_pad_blocks(off, cnt, E_tot, b0, b1, bm, N, ids, sw, eids);
+    cluster_wait();  // no CTA leaves while another may still read its counts
 }
 
 }  // namespace mr
