@@ -365,6 +365,7 @@ RouteArgs route_args(const mr_router_params* p, const void* logits, void* probs,
     const unsigned tries = g_wait_test.tries.load(std::memory_order_relaxed);
     a.wait_tries = tries ? tries : kWaitLimit;
     a.drop_copies = g_wait_test.drop.load(std::memory_order_relaxed);
+    a.warm_code = 0;
     const uintptr_t in_al = p->in_dtype == MR_BF16 ? 8 : 16;
     a.vec = (p->E % 4 == 0) && aligned(logits, in_al) && aligned(probs, in_al) && aligned(inter, 16) &&
             aligned(map, 4) && aligned(p->bias, 16);
@@ -694,6 +695,7 @@ int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int
         // arg-max path has the shorter code, so it is the default up to k_r = 32
         const int f = g_path.forced();
         const bool sel = f == 2 || (f == 0 && k_r > 32);
+        a.warm_code = launch_overlap() ? 1 : 0;
         const int nw = (p->T > 16 ? kFusedWideThreads : kFusedThreads) / 32;
         const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, sel, a.n_group > 0);
         const size_t smem = static_cast<size_t>(L.bytes) * nw +

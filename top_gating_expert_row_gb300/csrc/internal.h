@@ -72,10 +72,10 @@ inline int log2_if_pow2(int x)
 }
 
 // Shared memory of the fused decode kernel after the warp regions: the T*topk
-// pairs, one token bitmask per expert, the padded offsets and the
+// pairs, one token bitmask per expert, the padded offsets, the counts and the
 // block -> expert map.
 struct FusedSortLayout {
-    int idx, w, mask, off, blk, bytes;
+    int idx, w, mask, off, cnt, blk, bytes;
 };
 
 // mask_bytes: bytes of one expert's token mask (4 for T <= 32, 8 for T <= 64)
@@ -89,6 +89,7 @@ __host__ __device__ inline FusedSortLayout fused_sort_layout(int N, int E_tot, i
     F.w = o; o += align16(N * 4);
     F.mask = o; o += align16(E_tot * mask_bytes);
     F.off = o; o += align16((E_tot + 1) * 4);
+    F.cnt = o; o += align16(E_tot * 4);
     F.blk = o; o += align16((nblk > 0 ? nblk : 1) * 4);
     F.bytes = o;
     return F;

@@ -49,6 +49,7 @@ struct RouteArgs {
     int32_t* status;      // device status word, raised to kStatusTimeout when a bounded wait gives up
     uint32_t wait_tries;  // attempts (about 1 us each) before a bounded wait gives up
     int drop_copies;      // test mode: arm the staging barriers but issue no copies
+    int warm_code;        // fused decode under the launch overlap: warm-up pass before the wait
 };
 
 // Byte offsets of one warp's shared-memory region (same formula on host and device).

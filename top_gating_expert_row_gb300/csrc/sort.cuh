@@ -197,6 +197,24 @@ __device__ inline void cta_scatter(const int32_t* idx, const float* w, int f0, i
     warp_runs_place<kSteps>(R, E_tot, base, wh, out_ids, out_w);
 }
 
+// Sentinels and expert ids by expert, a warp per expert (the lanes cover the
+// expert's padded positions and blocks): for sorts with few pairs per expert,
+// where a search per block costs more than a look at every expert.
+__device__ inline void cta_fill_pads_by_expert(const uint32_t* off, const uint32_t* cnt, int E_tot, int bm,
+                                               int32_t sentinel, int32_t* out_ids, float* out_w, int32_t* expert_ids)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int e = warp; e < E_tot; e += nw) {
+        const uint32_t a = off[e], b = off[e + 1];
+        if (a == b) continue;
+        for (uint32_t p = a + cnt[e] + lane; p < b; p += 32) {
+            out_ids[p] = sentinel;
+            if (out_w) out_w[p] = 0.0f;
+        }
+        for (uint32_t blk = a / bm + lane; blk < b / bm; blk += 32) expert_ids[blk] = e;
+    }
+}
+
 // Chunks of flat pairs per thread-block cluster of the sort (and of the route
 // kernel that feeds it).
 constexpr int kClusterChunks = 8;
