@@ -904,7 +904,8 @@ def main():
             line["aux_loss"] = aux_loss_rates(mr, w, dev, stream)
             line["bf16"] = bf16_rates(mr, dev, stream)
             breakdown = {}
-            for wl in [synth.large_softmax(k) for k in synth.LARGE_TOPKS] + [synth.large_e_sigmoid()]:
+            for wl in [synth.large_softmax(k) for k in synth.LARGE_TOPKS] + [synth.large_e_sigmoid(),
+                                                                             synth.widest_softmax()]:
                 breakdown[wl.name] = time_kernels(mr, wl, dev, stream)
             # the step's own kernels isolated: rotated buffer sets beyond L2, so the
             # backward kernels read inputs the forward did not just leave in L2

@@ -67,7 +67,9 @@ typedef enum { MR_SOFTMAX = 0, MR_SIGMOID = 1 } mr_score_fn;
 typedef enum { MR_F32 = 0, MR_BF16 = 1 } mr_dtype;
 
 /* Library limits (MR_EUNSUPPORTED beyond them). */
-#define MR_MAX_EXPERTS 2304      /* E, routed experts per token row (held in registers) */
+#define MR_MAX_EXPERTS 8192      /* E, routed experts per token row (rows wider than 1024
+                                    are held in shared memory; [TE] flowchart: radix top-k
+                                    while num_experts <= 8160) */
 #define MR_MAX_TOPK 256          /* topk - n_shared, routed slots */
 #define MR_MAX_GROUPS 32         /* n_group */
 #define MR_MAX_GROUP_TOPK 8      /* (topk - n_shared) / topk_group, keys summed per group */

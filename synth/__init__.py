@@ -173,6 +173,11 @@ def large_e_sigmoid() -> Workload:
                     scaling=2.5, bias_range=0.1)
 
 
+def widest_softmax() -> Workload:
+    """T=8192, E=8160 (the widest row the pages' radix path takes), topk=36, fp32 N(0,1), softmax."""
+    return Workload("softmax_T8192_E8160_k36", 8192, 8160, 36, SOFTMAX, F32)
+
+
 def prefill_grouped() -> Workload:
     """T=16384, E=384 (+1 shared), topk=9, bf16 N(0,1)+Zipf(1.1) offsets, sigmoid + bias
     U(-0.05,0.05), 8 groups of 48 keep 4, renorm, scaling 2.827, block_m=64."""

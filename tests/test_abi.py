@@ -84,7 +84,7 @@ def _fwd(lib, p, logits=FAKE, probs=FAKE):
     (dict(n_group=4, topk_group=3, score_fn=1), 1),           # k_r % topk_group != 0
     (dict(n_group=32, topk_group=1, topk=4, score_fn=1), 1),  # k_r/topk_group > E/n_group
     (dict(T=1 << 20, E=2048), 1),                             # T*E > INT_MAX
-    (dict(E=4096, topk=8), 2),                                # beyond the register-resident width
+    (dict(E=9000, topk=8), 2),                                # beyond MR_MAX_EXPERTS (8192)
     (dict(E=512, topk=300), 2),                               # k_r beyond MR_MAX_TOPK
     (dict(n_group=64, topk_group=2, E=128, score_fn=1), 2),   # more groups than lanes
     (dict(E=256, topk=32, n_group=2, topk_group=2, score_fn=1), 2),  # 16 keys per group score
@@ -116,7 +116,7 @@ def test_bwd_and_aux_reject(lib):
     cp = _p(lib).c()
     assert lib._lib.moe_router_bwd(ctypes.byref(cp), None, FAKE, FAKE, FAKE, None) == 1
     assert lib._lib.moe_router_bwd(ctypes.byref(cp), FAKE, FAKE, None, FAKE, None) == 1
-    cp = _p(lib, E=3000).c()
+    cp = _p(lib, E=9000).c()
     assert lib._lib.moe_router_bwd(ctypes.byref(cp), FAKE, FAKE, FAKE, FAKE, None) == 2
     assert lib._lib.moe_aux_scores_fwd(4, 64, 65, 0, 0, FAKE, FAKE, None, None) == 1
     assert lib._lib.moe_aux_scores_fwd(4, 64, 4, 0, 0, FAKE, None, None, None) == 1
@@ -151,6 +151,16 @@ def test_sort_sizes_and_rejects(lib):
     assert call(T=4096, wsb=0) == 1               # workspace too small
     assert call(E_tot=5000) == 2                  # beyond MR_MAX_SORT_EXPERTS
     assert call(T=1 << 28, topk=16) == 1          # T*topk >= INT_MAX
+
+
+def test_wide_rows_accepted_up_to_the_limit(lib):
+    # rows up to 8192 experts are routed (held in shared memory); their sort is
+    # limited to 4096 experts, so the fused call refuses wider rows
+    assert lib.moe_router_fused_workspace_bytes(_p(lib, T=100, E=8192, topk=8), 8) == 0
+    assert lib.moe_router_fused_workspace_bytes(_p(lib, T=100, E=4096, topk=8), 8) > 0
+    cp = _p(lib, T=100, E=8160, topk=8).c()
+    f = lib._lib.moe_router_fused_fwd_sort
+    assert f(ctypes.byref(cp), FAKE, 8, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, None, None) == 2
 
 
 def test_fused_rejects(lib):
@@ -202,7 +212,7 @@ def test_bwd_dtype_rejects(lib):
     assert f(ctypes.byref(cp), 5, FAKE, FAKE, FAKE, FAKE, None) == lib.MR_EINVAL
     assert f(ctypes.byref(cp), lib.MR_BF16, None, FAKE, FAKE, FAKE, None) == lib.MR_EINVAL
     assert f(ctypes.byref(cp), lib.MR_BF16, FAKE, FAKE, FAKE, None, None) == lib.MR_EINVAL
-    assert f(ctypes.byref(_p(lib, E=3000).c()), lib.MR_BF16, FAKE, FAKE, FAKE, FAKE, None) == lib.MR_EUNSUPPORTED
+    assert f(ctypes.byref(_p(lib, E=9000).c()), lib.MR_BF16, FAKE, FAKE, FAKE, FAKE, None) == lib.MR_EUNSUPPORTED
     assert f(ctypes.byref(_p(lib, T=0).c()), lib.MR_BF16, FAKE, FAKE, FAKE, FAKE, None) == lib.MR_OK
 
 

@@ -45,6 +45,11 @@ CASES = [
     W("e192_g4_k8_m4", 70, 192, 8, SG, renorm=1, n_group=4, topk_group=2, n_shared=2, shared_weight=0.5),
     W("e48_g3_k6_m2", 70, 48, 6, SG, n_group=3, topk_group=3),
     W("bf16_e2304_k36", 64, 2304, 36, SM, BF16),
+    # rows wider than the register-resident buckets, up to the library's limit
+    W("e4096_k36", 64, 4096, 36),
+    W("e5000_k20_sigmoid_ragged", 30, 5000, 20, SG, renorm=1),
+    W("e8160_k36_sigmoid_bias", 40, 8160, 36, SG, renorm=1, scaling=2.5, bias_range=0.1),
+    W("e8192_k8_bf16", 50, 8192, 8, SM, BF16),
 ]
 
 
@@ -186,7 +191,10 @@ def test_rows_of_varying_scale_every_row(mr, orc, E, k, fn, path, compact):
 BWD_CASES = [synth.tiny(), W("e512_k22", 300, 512, 22, sigma=2.0), W("e512_k22_sig", 300, 512, 22, SG),
              W("e2304_k36", 150, 2304, 36), W("e2304_k36_sig", 150, 2304, 36, SG, renorm=1, scaling=2.5,
                                                  bias_range=0.1),
-             W("e100_k5_renorm", 90, 100, 5, SM, renorm=1, scaling=0.7), W("e37_sig", 40, 37, 4, SG, renorm=1)]
+             W("e100_k5_renorm", 90, 100, 5, SM, renorm=1, scaling=0.7), W("e37_sig", 40, 37, 4, SG, renorm=1),
+             W("e4096_k36_wide", 60, 4096, 36), W("e8160_k36_sig_wide", 40, 8160, 36, SG, renorm=1, scaling=2.5,
+                                                  bias_range=0.1),
+             W("e8192_k8_renorm_wide", 40, 8192, 8, SM, renorm=1, scaling=1.5), W("e5001_sig_wide", 30, 5001, 9, SG)]
 
 
 @pytest.mark.parametrize("w", BWD_CASES, ids=lambda w: w.name)
@@ -206,7 +214,8 @@ BWD_BF16_CASES = [W("e2304_k36_bf16", 150, 2304, 36, SM, BF16), W("e2304_k36_sig
                                                                    renorm=1, scaling=2.5, bias_range=0.1),
                   W("e512_k22_bf16", 300, 512, 22, SM, BF16, sigma=2.0),
                   W("e100_k5_renorm_bf16", 90, 100, 5, SM, BF16, renorm=1, scaling=0.7),
-                  W("e37_sig_bf16", 40, 37, 4, SG, BF16, renorm=1)]
+                  W("e37_sig_bf16", 40, 37, 4, SG, BF16, renorm=1),
+                  W("e8192_k36_bf16_wide", 40, 8192, 36, SM, BF16)]
 
 
 @pytest.mark.parametrize("w", BWD_BF16_CASES, ids=lambda w: w.name)
@@ -243,7 +252,8 @@ def test_bwd_full_size_sampled_rows(mr, orc, w):
 
 AUX_CASES = [W("aux_e512_k22", 300, 512, 22, sigma=2.0), W("aux_e512_k22_sig", 300, 512, 22, SG),
              W("aux_e2304_k36", 100, 2304, 36), W("aux_e2304_k36_sig", 100, 2304, 36, SG),
-             W("aux_e8_k2", 16, 8, 2), W("aux_e100_k5_bf16", 80, 100, 5, SG, BF16)]
+             W("aux_e8_k2", 16, 8, 2), W("aux_e100_k5_bf16", 80, 100, 5, SG, BF16),
+             W("aux_e8160_k36", 40, 8160, 36), W("aux_e6000_k22_sig", 30, 6000, 22, SG)]
 
 
 @pytest.mark.parametrize("w", AUX_CASES, ids=lambda w: w.name)

@@ -28,6 +28,8 @@ STAGED = [
     W("staged_e2304_k36_bf16_sigmoid_bias", 6500, 2304, 36, SG, BF16, renorm=1, scaling=2.5, bias_range=0.1),
     W("staged_e1536_k100_f32_sigmoid", 6500, 1536, 100, SG, F32, renorm=1),
     W("staged_e2304_k8_f32_softmax", 6500, 2304, 8, SM, F32),
+    W("staged_e8192_k36_f32_softmax", 3000, 8192, 36, SM, F32),
+    W("staged_e8064_k22_bf16_sigmoid", 3000, 8064, 22, SG, BF16, renorm=1, bias_range=0.1),
 ]
 
 

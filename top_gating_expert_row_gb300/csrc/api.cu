@@ -467,7 +467,7 @@ int moe_router_fwd(const mr_router_params* p, const void* logits, void* probs, u
     if (!probs && !routing_map && !intermediate && !topk_idx && !topk_w) return MR_EINVAL;
     if (p->T == 0) return MR_OK;
     const RouteArgs a = route_args(p, logits, probs, routing_map, intermediate, topk_idx, topk_w, status);
-    const int nv = nv_index(p->E);
+    const int nv = fwd_nv_index(p->E, MR_MAX_EXPERTS);
     if (nv < 0) return MR_EUNSUPPORTED;
     return from_cuda(launch_fwd(p->score_fn, p->in_dtype, a, nv, use_select(a.k_r),
                                 reinterpret_cast<cudaStream_t>(stream)));
@@ -489,7 +489,7 @@ int moe_aux_scores_fwd(int T, int E, int topk, int score_fn, int in_dtype, const
     if (!logits || (!scores && !routing_map)) return MR_EINVAL;
     if (T == 0) return MR_OK;
     const RouteArgs a = route_args(&p, logits, nullptr, routing_map, scores, nullptr, nullptr, nullptr);
-    const int nv = nv_index(E);
+    const int nv = fwd_nv_index(E, MR_MAX_EXPERTS);
     if (nv < 0) return MR_EUNSUPPORTED;
     return from_cuda(launch_fwd(score_fn, in_dtype, a, nv, use_select(a.k_r), reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -654,7 +654,8 @@ int moe_sort_noalloc(const int32_t* topk_idx, const float* topk_w, int T, int to
 size_t moe_router_fused_workspace_bytes(const mr_router_params* p, int block_m)
 {
     if (check_router(p) != MR_OK || block_m < 1) return 0;
-    const int nv = nv_index(p->E);
+    if (check_sort(p->T, p->topk, p->E + p->n_shared, block_m) != MR_OK) return 0;
+    const int nv = fwd_nv_index(p->E, MR_MAX_EXPERTS);
     if (nv < 0) return 0;
     if (fused_one_launch(p->T, kNvBuckets[nv])) return 0;
     const size_t N = static_cast<size_t>(p->T) * p->topk;
@@ -673,7 +674,7 @@ int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int
     if (rc != MR_OK) return rc;
     if (!logits || !sorted_token_ids || !expert_ids || !num_tokens_post_pad) return MR_EINVAL;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int nv = nv_index(p->E);
+    const int nv = fwd_nv_index(p->E, MR_MAX_EXPERTS);
     if (nv < 0) return MR_EUNSUPPORTED;
     const int k_r = p->topk - p->n_shared;
     // above 16 tokens, rows held in registers: one launch of one thread-block

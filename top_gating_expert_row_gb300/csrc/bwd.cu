@@ -131,13 +131,103 @@ __global__ void __launch_bounds__(kBwdThreads) k_router_bwd(const GradT* grad,
     }
 }
 
+// Rows too wide to hold in registers (E > 2304): one warp per row, two passes
+// over the row in global memory (the second mostly from L2). Pass 1 sums
+// A = sum m s and B = sum m s g; the softmax correction sum_j s_j ds_j then has
+// the closed form c*B without renorm and 0 with it (the renormalised weights'
+// gradient sums to zero against s), and pass 2 forms each element's gradient.
+template <int SCORE, bool HAS_MAP, typename GradT>
+__global__ void __launch_bounds__(kBwdThreads) k_router_bwd_wide(const GradT* grad, const float* inter,
+                                                                 const uint8_t* map, GradT* dx, int T, int E,
+                                                                 int renorm, float c, int vec)
+{
+    pdl_trigger_small();
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const bool rn = HAS_MAP && renorm;
+    // four consecutive elements starting at e0 (g, s, m), any alignment
+    auto load = [&](size_t ro, int e0, float (&g)[4], float (&sv)[4], uint32_t& m, bool first) {
+        if (vec && e0 + 4 <= E) {
+            if constexpr (std::is_same<GradT, float>::value) {
+                const float4 a = first ? __ldcg(reinterpret_cast<const float4*>(grad + ro + e0))
+                                       : __ldcs(reinterpret_cast<const float4*>(grad + ro + e0));
+                g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w;
+            } else {
+                const uint2 q = first ? __ldcg(reinterpret_cast<const uint2*>(grad + ro + e0))
+                                      : __ldcs(reinterpret_cast<const uint2*>(grad + ro + e0));
+                g[0] = bf16_bits_to_f32(q.x & 0xffffu); g[1] = bf16_bits_to_f32(q.x >> 16);
+                g[2] = bf16_bits_to_f32(q.y & 0xffffu); g[3] = bf16_bits_to_f32(q.y >> 16);
+            }
+            const float4 b = first ? __ldcg(reinterpret_cast<const float4*>(inter + ro + e0))
+                                   : __ldcs(reinterpret_cast<const float4*>(inter + ro + e0));
+            sv[0] = b.x; sv[1] = b.y; sv[2] = b.z; sv[3] = b.w;
+            m = HAS_MAP ? (first ? __ldcg(reinterpret_cast<const unsigned int*>(map + ro + e0))
+                                 : __ldcs(reinterpret_cast<const unsigned int*>(map + ro + e0)))
+                        : 0x01010101u;
+        } else {
+            m = 0u;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const bool in = e0 + q < E;
+                g[q] = in ? load_scalar<GradT>(grad + ro + e0 + q) : 0.0f;
+                sv[q] = in ? inter[ro + e0 + q] : 0.0f;
+                const uint32_t mb = in ? (HAS_MAP ? static_cast<uint32_t>(map[ro + e0 + q] != 0) : 1u) : 0u;
+                m |= mb << (8 * q);
+            }
+        }
+    };
+    for (int t = blockIdx.x * nw + warp; t < T; t += gridDim.x * nw) {
+        const size_t ro = static_cast<size_t>(t) * E;
+        float A = 0.0f, B = 0.0f;
+        if (rn || SCORE == kSoftmax) {
+            for (int e0 = lane * 4; e0 < E; e0 += 128) {
+                float g[4], sv[4];
+                uint32_t m;
+                load(ro, e0, g, sv, m, true);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if ((m >> (8 * q)) & 0xffu) {
+                        A += sv[q];
+                        B += sv[q] * g[q];
+                    }
+            }
+            A = warp_sum(A);
+            B = warp_sum(B);
+        }
+        const float cA = (rn && A != 0.0f) ? c / A : 0.0f;
+        const float BA = (rn && A != 0.0f) ? B / A : 0.0f;
+        const float D = (SCORE == kSoftmax && !rn) ? c * B : 0.0f;
+        GradT* out = dx + ro;
+        for (int e0 = lane * 4; e0 < E; e0 += 128) {
+            float g[4], sv[4], r[4];
+            uint32_t m;
+            load(ro, e0, g, sv, m, false);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const bool mk = (m >> (8 * q)) & 0xffu;
+                const float ds = mk ? (rn ? cA * (g[q] - BA) : c * g[q]) : 0.0f;
+                r[q] = (SCORE == kSoftmax) ? sv[q] * (ds - D) : ds * sv[q] * (1.0f - sv[q]);
+            }
+            if (vec && e0 + 4 <= E) {
+                store4_stream<GradT>(out + e0, r);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (e0 + q < E) store_scalar<GradT>(out + e0 + q, r[q]);
+            }
+        }
+    }
+}
+
 namespace {
 template <typename GradT>
 using BwdFn = void (*)(const GradT*, const float*, const uint8_t*, GradT*, int, int, int, float, int);
 
+// nv_idx < 0: rows wider than the register-resident buckets
 template <int SCORE, bool HAS_MAP, typename GradT>
 BwdFn<GradT> bwd_kernel(int nv_idx)
 {
+    if (nv_idx < 0) return k_router_bwd_wide<SCORE, HAS_MAP, GradT>;
     switch (kNvBuckets[nv_idx]) {
         case 1: return k_router_bwd<SCORE, 1, HAS_MAP, GradT>;
         case 2: return k_router_bwd<SCORE, 2, HAS_MAP, GradT>;

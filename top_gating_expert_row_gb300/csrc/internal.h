@@ -27,6 +27,16 @@ inline int nv_index(int E)
     return -1;
 }
 
+// The forward's row bucket for E: the register-resident buckets up to 2304,
+// the last (shared-memory rows, any width up to MR_MAX_EXPERTS) beyond; -1 past
+// MR_MAX_EXPERTS (passed in as max_e).
+inline int fwd_nv_index(int E, int max_e)
+{
+    const int i = nv_index(E);
+    if (i >= 0) return i;
+    return E <= max_e ? kNumNv - 1 : -1;
+}
+
 // The one-CTA fused decode kernel keeps rows up to this many chunks (E <= 1024).
 constexpr int kFusedMaxNv = 8;
 // 16 < T <= 64 (E <= 256): the same one-CTA kernel with 32 warps, each routing
