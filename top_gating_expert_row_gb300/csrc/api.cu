@@ -37,7 +37,7 @@ int g_smem_n = 0;
 int g_sm_count[64] = {0};
 }  // namespace
 
-int persistent_grid(const void* func, int threads, size_t smem, long long units)
+int persistent_grid(const void* func, int threads, size_t smem, long long units, bool balance)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -56,8 +56,18 @@ int persistent_grid(const void* func, int threads, size_t smem, long long units)
     }
     if (blocks < 1) return -1;
     const long long cap = static_cast<long long>(blocks) * g_sm_count[dev];
-    const long long g = units < cap ? units : cap;
-    return static_cast<int>(g < 1 ? 1 : g);
+    long long g = units < cap ? units : cap;
+    if (g < 1) return 1;
+    if (balance) {
+        // as many CTAs as give every CTA the same number of rounds: with the
+        // full capacity the last round runs on only part of the GPU, while the
+        // same rounds on fewer CTAs keep every SM busy to the end (the backward,
+        // bound by memory, gains; the forwards lose more latency hiding than the
+        // idle tail costs them)
+        const long long rounds = (units + g - 1) / g;
+        g = (units + rounds - 1) / rounds;
+    }
+    return static_cast<int>(g);
 }
 
 // The limit is only ever raised: one entry per (kernel, device) remembers the

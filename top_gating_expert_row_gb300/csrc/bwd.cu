@@ -247,7 +247,7 @@ int launch(BwdFn<GradT> f, const GradT* g, const float* s, const uint8_t* m, Gra
 {
     if (!f) return cudaErrorInvalidValue;
     const long long ctas_needed = (static_cast<long long>(T) + kBwdThreads / 32 - 1) / (kBwdThreads / 32);
-    const int grid = persistent_grid(reinterpret_cast<const void*>(f), kBwdThreads, 0, ctas_needed);
+    const int grid = persistent_grid(reinterpret_cast<const void*>(f), kBwdThreads, 0, ctas_needed, true);
     if (grid <= 0) return cudaErrorInvalidConfiguration;
     return launch_kernel(f, dim3(grid), dim3(kBwdThreads), 0, st, 0, g, s, m, dx, T, E, renorm, scaling, vec ? 1 : 0);
 }

@@ -53,8 +53,10 @@ inline bool fused_one_launch(int T, int nv_bucket)
 // wider rows take the shared-memory routine, two warps per CTA.
 constexpr int kRegisterMaxNv = 8;
 // Resident CTAs per SM the forward's register budget is sized for (the row's
-// keys take 4*NV registers per lane).
-constexpr int fwd_min_blocks(int nv) { return nv >= 12 ? 2 : (nv >= 6 ? 3 : 4); }
+// keys take 4*NV registers per lane). At NV = 4 (E = 512) five CTAs (48
+// registers, a few bytes of spills) measured faster than four; at NV = 3 the
+// spills cost more than the extra CTA gains.
+constexpr int fwd_min_blocks(int nv) { return nv >= 12 ? 2 : (nv >= 6 ? 3 : (nv == 4 ? 5 : 4)); }
 constexpr int kWideThreads = 64;
 // Registers are capped so that shared memory, not registers, bounds residency
 // (a 9 KB key row per warp at E = 2304 allows about 22 warps per SM).
@@ -213,8 +215,9 @@ int launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, 
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Persistent-grid size: min(units, SMs x resident CTAs) for a kernel.
-int persistent_grid(const void* func, int threads, size_t smem, long long units);
+// Persistent-grid size: min(units, SMs x resident CTAs) for a kernel; with
+// balance, reduced to the fewest CTAs that take the same number of rounds.
+int persistent_grid(const void* func, int threads, size_t smem, long long units, bool balance = false);
 // Raise a kernel's dynamic shared-memory limit when needed.
 int ensure_smem(const void* func, size_t smem);
 // Whether a cluster of cs CTAs of this kernel (threads each, smem bytes of
