@@ -690,11 +690,16 @@ int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int
     // above 16 tokens, rows held in registers: one launch of one thread-block
     // cluster when one fits (else the one-CTA kernel up to 64 tokens, or the
     // separate launches)
+    // a warp routes one token in either one-launch form, so the arg-max path
+    // (the shorter chain of dependent steps for one row) is the default up to
+    // k_r = 32
+    const int force = g_path.forced();
+    const bool decode_select = force == 2 || (force == 0 && k_r > 32);
     if (p->T > 16 && p->T <= kFusedClusterMaxTokens && kNvBuckets[nv] <= kRegisterMaxNv) {
         RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, topk_idx, topk_w, status);
         SortArgs s{sorted_token_ids, sorted_weights, expert_ids, num_tokens_post_pad, E_tot, block_m,
                    log2_if_pow2(block_m)};
-        const int e = launch_fused_cluster(p->score_fn, p->in_dtype, a, s, nv, use_select(k_r), st);
+        const int e = launch_fused_cluster(p->score_fn, p->in_dtype, a, s, nv, decode_select, st);
         if (e != cudaErrorNotSupported) return from_cuda(e);
         cudaGetLastError();
     }
@@ -702,10 +707,7 @@ int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int
         RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, topk_idx, topk_w, status);
         SortArgs s{sorted_token_ids, sorted_weights, expert_ids, num_tokens_post_pad, E_tot, block_m,
                    log2_if_pow2(block_m)};
-        // a one-CTA decode launch is bound by instruction fetch on a cold SM: the
-        // arg-max path has the shorter code, so it is the default up to k_r = 32
-        const int f = g_path.forced();
-        const bool sel = f == 2 || (f == 0 && k_r > 32);
+        const bool sel = decode_select;
         a.warm_code = launch_overlap() ? 1 : 0;
         const int nw = (p->T > 16 ? kFusedWideThreads : kFusedThreads) / 32;
         const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, sel, a.n_group > 0);
