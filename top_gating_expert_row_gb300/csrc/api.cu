@@ -2,7 +2,9 @@
 // enqueued), path and grid selection, and the launches. Host checks follow
 // TransformerEngine PR 3012 "Hardening" (T*E <= INT_MAX, topk in [1, E],
 // topk % group_topk == 0) plus this library's own limits.
+#include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <climits>
 #include <cstdlib>
 #include <cstring>
@@ -320,6 +322,29 @@ int select_stop(int k_r)
     return (s + 31) & ~31;
 }
 
+// Rung of the lanes'-maxima ladder (warp_kth_largest) tried as a pivot when a
+// row has no usable previous threshold: the first j whose expected count of
+// keys at or above it reaches max(k_r + 4, 1.4 k_r) (capped at stop), for rows
+// of n similar entries over the lanes that hold any (a lane holds 4 of every
+// 128 experts: all 32 lanes from n = 128 on). The j-th largest of L lane
+// maxima sits near the (L + 1 - j) / (L + 1) quantile of a lane's maximum,
+// i.e. that quantile's m-th root (m = n / L keys per lane) for one key. With
+// k_r <= L the rung is at least k_r, so its count never falls short of k_r.
+int route_rung(int n, int k_r, int stop)
+{
+    if (k_r < 1 || n < 1) return 0;
+    const int lanes = n >= 128 ? 32 : (n + 3) / 4;
+    const double m = static_cast<double>(n) / lanes;
+    const double target = std::min<double>(stop, std::max(k_r + 4.0, 1.4 * k_r));
+    int j = lanes;
+    for (int r = 1; r <= lanes; ++r)
+        if (n * (1.0 - std::pow((lanes + 1.0 - r) / (lanes + 1.0), 1.0 / m)) >= target) {
+            j = r;
+            break;
+        }
+    return k_r <= lanes && j < k_r ? k_r : j;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int from_cuda(int e) { return e == cudaSuccess ? MR_OK : MR_ECUDA; }
@@ -371,6 +396,7 @@ RouteArgs route_args(const mr_router_params* p, const void* logits, void* probs,
     a.scaling = p->scaling;
     a.shared_weight = p->shared_weight;
     a.stop = select_stop(a.k_r);
+    a.rung = route_rung(a.n_group > 0 ? a.topk_group * (a.E / a.n_group) : a.E, a.k_r, a.stop);
     a.status = status ? status : device_status_address();
     const unsigned tries = g_wait_test.tries.load(std::memory_order_relaxed);
     a.wait_tries = tries ? tries : kWaitLimit;

@@ -50,6 +50,7 @@ struct RouteArgs {
     uint32_t wait_tries;  // attempts (about 1 us each) before a bounded wait gives up
     int drop_copies;      // test mode: arm the staging barriers but issue no copies
     int warm_code;        // fused decode under the launch overlap: warm-up pass before the wait
+    int rung;             // SELECT: rung of the lane-maxima ladder tried as a pivot (1..32, 0: none)
 };
 
 // Byte offsets of one warp's shared-memory region (same formula on host and device).
@@ -147,6 +148,30 @@ __device__ void group_limit(uint32_t* skeys, int E, int G, int gk, int m, int la
             for (int i = lane; i < gs; i += 32) skeys[q * gs + i] = 0u;
 }
 
+// The j-th largest (1 <= j <= 32) of the 32 lanes' values, returned to every
+// lane: a bitonic sort of the warp's values (ascending by lane), then a
+// broadcast from lane 32 - j.
+//
+// Used as a bisection pivot, the j-th largest of the lanes' row maxima bounds
+// the count from below: at least j keys (each of those lanes' maxima) are >= it.
+// On rows of similar entries, with m keys per lane, about
+// E * (1 - ((33 - j) / 33)^(1/m)) keys are; the host picks j for the count it
+// wants (route_rung), so a row with no usable previous threshold still starts
+// with one pivot that usually leaves between k_r and `stop` candidates.
+__device__ __forceinline__ uint32_t warp_kth_largest(uint32_t v, int j, int lane)
+{
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const uint32_t o = __shfl_xor_sync(kFull, v, stride);
+            const bool ascending = (lane & size) == 0;
+            const bool lower = (lane & stride) == 0;
+            v = (lower == ascending) ? min(v, o) : max(v, o);
+        }
+    return __shfl_sync(kFull, v, 32 - j);
+}
+
 // ---------------------------------------------------------------------------
 // route_row: the whole forward for token t. Winners are left in the warp's
 // shared region (win_idx / win_val = their score s, k_r entries in selection
@@ -230,6 +255,7 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
     uint32_t key[NV][4];
     float vmul = 1.0f;  // vbuf * vmul = s
     uint32_t kmax;
+    uint32_t lane_max;  // the largest of this lane's keys
 
     // 1. load, selection keys, scores into vbuf; padding keys are 0
     {
@@ -263,7 +289,8 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
                         if (inside(v, c)) vbuf[e0 + c] = x[v][c];
                 }
             }
-            kmax = __reduce_max_sync(kFull, max(max(lm[0], lm[1]), max(lm[2], lm[3])));
+            lane_max = max(max(lm[0], lm[1]), max(lm[2], lm[3]));
+            kmax = __reduce_max_sync(kFull, lane_max);
             const float m = float_of(kmax);
             // exp(x - max) in place over the row buffer (exp_value: only the value
             // matters here); a rolled loop keeps the code short (the row's chunks
@@ -324,7 +351,8 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
                         if (inside(v, c)) vbuf[e0 + c] = sv[c];
                 }
             }
-            kmax = __reduce_max_sync(kFull, max(max(lm[0], lm[1]), max(lm[2], lm[3])));
+            lane_max = max(max(lm[0], lm[1]), max(lm[2], lm[3]));
+            kmax = __reduce_max_sync(kFull, lane_max);
         }
     }
 
@@ -365,6 +393,7 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
                 key[v][c] = keep ? key[v][c] : 0u;
                 lmax = max(lmax, key[v][c]);
             }
+        lane_max = lmax;
         kmax = __reduce_max_sync(kFull, lmax);
         __syncwarp();  // the staged keys are read no more; the region may be reused
     }
@@ -489,6 +518,17 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
         // warm start: the previous row's threshold (rows of one batch are alike,
         // so it usually leaves between k_r and `stop` candidates in one pass)
         if (cnt_lo > cap && warm > lo && warm < hi) split(warm);
+        // no previous threshold, or it left too few or too many candidates: a
+        // rung of the lanes' maxima; when that leaves too few, the lowest rung
+        // (at least 32 keys reach it) before the row minimum is needed
+        if (cnt_lo > cap && a.rung > 0) {
+            const uint32_t r = warp_kth_largest(lane_max, a.rung, lane);
+            if (r > lo && r < hi) split(r);
+            if (cnt_lo > cap && lo == 1u) {
+                const uint32_t r32 = __reduce_min_sync(kFull, lane_max);
+                if (r32 > lo && r32 < hi) split(r32);
+            }
+        }
         if (cnt_lo > cap && lo == 1u) {
             uint32_t ln[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
 #pragma unroll

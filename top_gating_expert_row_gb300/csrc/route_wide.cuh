@@ -166,16 +166,90 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
     const bool warm_tested = has_warm && wpiv <= kmax;
     const uint32_t cnt_w = warm_tested ? __reduce_add_sync(kFull, cw) : 0u;
     const uint32_t cap = static_cast<uint32_t>(a.stop);
-    // softmax: with k_r <= count(key >= warm) <= cap the candidates are known
-    // now and the exp pass below writes them out as it reads the keys
-    const bool fused_pick = SCORE == kSoftmax && warm_tested && cnt_w >= static_cast<uint32_t>(k_r) && cnt_w <= cap;
     unsigned long long* cand = reinterpret_cast<unsigned long long*>(wsm + L.cand);
     auto comp = [&](uint32_t k, uint32_t idx) {
         return (static_cast<unsigned long long>(k) << 32) | static_cast<uint32_t>(~idx);
     };
+
+    // Threshold select state. Invariant: count(key >= lo) = cnt_lo >= k_r >
+    // count(key >= hi) = cnt_hi; lane_lo / lane_hi are this lane's counts (-1:
+    // not yet counted). lo starts at 1, below every real key.
+    const uint32_t n_valid = static_cast<uint32_t>(a.n_group > 0 ? a.topk_group * (E / a.n_group) : E);
+    uint32_t lo = 1u, hi = 0u;
+    uint32_t cnt_lo = n_valid, cnt_hi = 0u;
+    int lane_lo = -1, lane_hi = 0;
+    auto count_ge = [&](uint32_t piv) {
+        uint32_t c0 = 0u, c1 = 0u;
+#pragma unroll 4
+        for (int v = 0; v < nv; ++v) {
+            const uint4 q = k4(v);
+            c0 += (q.x >= piv) + (q.y >= piv);
+            c1 += (q.z >= piv) + (q.w >= piv);
+        }
+        return c0 + c1;
+    };
+    auto split = [&](uint32_t piv) {
+        const uint32_t c = count_ge(piv);
+        const uint32_t tot = __reduce_add_sync(kFull, c);
+        if (tot >= static_cast<uint32_t>(k_r)) {
+            lo = piv; cnt_lo = tot; lane_lo = static_cast<int>(c);
+        } else {
+            hi = piv; cnt_hi = tot; lane_hi = static_cast<int>(c);
+        }
+    };
+    // Bisection until at most cap keys are >= lo, or the k_r-th key is tied at
+    // lo (hi == lo + 1). Pivots: the previous row's threshold (counted with the
+    // keys), a rung of the lanes' maxima (then the lowest rung, at least 32
+    // keys reach it, when that left too few), then value-space midpoints, then
+    // key-space midpoints (at most 64 rounds in all).
+    auto bisect = [&]() {
+        hi = kmax + 1u;
+        if (warm_tested) {
+            if (cnt_w >= static_cast<uint32_t>(k_r)) {
+                lo = wpiv; cnt_lo = cnt_w; lane_lo = static_cast<int>(cw);
+            } else {
+                hi = wpiv; cnt_hi = cnt_w; lane_hi = static_cast<int>(cw);
+            }
+        }
+        if (cnt_lo > cap && a.rung > 0) {
+            const uint32_t r = warp_kth_largest(lm, a.rung, lane);
+            if (r > lo && r < hi) split(r);
+            if (cnt_lo > cap && lo == 1u) {
+                const uint32_t r32 = __reduce_min_sync(kFull, lm);
+                if (r32 > lo && r32 < hi) split(r32);
+            }
+        }
+        for (int it = 0; it < 64 && cnt_lo > cap && hi - lo > 1u; ++it) {
+            if (lo == 1u) {  // a real lower end: the row's smallest key
+                uint32_t ln = 0xffffffffu;
+                for (int v = 0; v < nv; ++v) {
+                    const uint4 q = k4(v);
+                    ln = min(ln, min(min(q.x - 1u, q.y - 1u), min(q.z - 1u, q.w - 1u)));  // 0 wraps to the top
+                }
+                lo = __reduce_min_sync(kFull, ln) + 1u;
+                if (!(cnt_lo > cap && hi - lo > 1u)) break;
+            }
+            uint32_t piv = lo + ((hi - lo) >> 1);
+            if (it < 8) {
+                const float fm = __fadd_rn(__fmul_rn(float_of(lo), 0.5f), __fmul_rn(float_of(hi - 1u), 0.5f));
+                const uint32_t km = key_of(fm);
+                if (km > lo && km < hi) piv = km;
+            }
+            split(piv);
+        }
+    };
+    // Softmax rows without groups select before the exp pass: once at most cap
+    // keys are >= lo, the exp pass writes those candidates out as it reads the
+    // keys (no pass of its own). With groups the exp pass must see every key
+    // before the group limit drops some, so the selection comes after it.
+    const bool early = SELECT && SCORE == kSoftmax && a.n_group == 0;
+    if (early) bisect();
+    const bool fused_pick = early && cnt_lo <= cap;
+    if (fused_pick && lane_lo < 0) lane_lo = static_cast<int>(count_ge(lo));
     if (SCORE == kSoftmax) {
         m = float_of(kmax);
-        uint32_t cpos = fused_pick ? warp_exclusive_scan(cw, lane) : 0u;
+        uint32_t cpos = fused_pick ? warp_exclusive_scan(static_cast<uint32_t>(lane_lo), lane) : 0u;
+        const uint32_t ppiv = lo;  // fused_pick: candidates are the keys >= lo
         float2 sum01 = make_float2(0.0f, 0.0f), sum23 = make_float2(0.0f, 0.0f);
         const float2 negm = make_float2(-m, -m);
         // batches of kExpBatch chunks, keys loaded first: with generic pointers
@@ -205,7 +279,7 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
                     const uint32_t e0i = static_cast<uint32_t>(v * 128 + lane4);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const bool in = kq[c] >= wpiv;
+                        const bool in = kq[c] >= ppiv;
                         if (in) cand[cpos] = comp(kq[c], e0i + c);
                         cpos += in ? 1u : 0u;
                     }
@@ -281,60 +355,7 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
             Ip = widx;
         }
     } else {
-        const uint32_t n_valid = static_cast<uint32_t>(a.n_group > 0 ? a.topk_group * (E / a.n_group) : E);
-        uint32_t lo = 1u, hi = kmax + 1u;
-        uint32_t cnt_lo = n_valid, cnt_hi = 0u;
-        int lane_lo = -1, lane_hi = 0;
-        if (warm_tested) {  // the count made with the keys is the first bisection step
-            if (cnt_w >= static_cast<uint32_t>(k_r)) {
-                lo = wpiv; cnt_lo = cnt_w; lane_lo = static_cast<int>(cw);
-            } else {
-                hi = wpiv; cnt_hi = cnt_w; lane_hi = static_cast<int>(cw);
-            }
-        }
-        auto count_ge = [&](uint32_t piv) {
-            uint32_t c0 = 0u, c1 = 0u;
-#pragma unroll 4
-            for (int v = 0; v < nv; ++v) {
-                const uint4 q = k4(v);
-                c0 += (q.x >= piv) + (q.y >= piv);
-                c1 += (q.z >= piv) + (q.w >= piv);
-            }
-            return c0 + c1;
-        };
-        // Invariant: count(key >= lo) = cnt_lo >= k_r > count(key >= hi) = cnt_hi.
-        // Pivots: the previous row's threshold first, then value-space midpoints,
-        // then key-space midpoints (at most 64 rounds in all).
-        for (int it = warm_tested ? 0 : -1; it < 64 && cnt_lo > cap && hi - lo > 1u; ++it) {
-            uint32_t piv;
-            if (it < 0) {
-                if (!(warm > lo && warm < hi)) continue;
-                piv = warm;
-            } else {
-                if (lo == 1u) {  // a real lower end: the row's smallest key
-                    uint32_t ln = 0xffffffffu;
-                    for (int v = 0; v < nv; ++v) {
-                        const uint4 q = k4(v);
-                        ln = min(ln, min(min(q.x - 1u, q.y - 1u), min(q.z - 1u, q.w - 1u)));  // 0 wraps to the top
-                    }
-                    lo = __reduce_min_sync(kFull, ln) + 1u;
-                    if (!(cnt_lo > cap && hi - lo > 1u)) break;
-                }
-                piv = lo + ((hi - lo) >> 1);
-                if (it < 8) {
-                    const float fm = __fadd_rn(__fmul_rn(float_of(lo), 0.5f), __fmul_rn(float_of(hi - 1u), 0.5f));
-                    const uint32_t km = key_of(fm);
-                    if (km > lo && km < hi) piv = km;
-                }
-            }
-            const uint32_t c = count_ge(piv);
-            const uint32_t tot = __reduce_add_sync(kFull, c);
-            if (tot >= static_cast<uint32_t>(k_r)) {
-                lo = piv; cnt_lo = tot; lane_lo = static_cast<int>(c);
-            } else {
-                hi = piv; cnt_hi = tot; lane_hi = static_cast<int>(c);
-            }
-        }
+        if (!early) bisect();
         uint32_t n;
         if (fused_pick) {
             n = cnt_lo;  // written by the exp pass
