@@ -335,9 +335,13 @@ int moe_router_set_wait_test(unsigned int tries, int drop_copies);
 /* Diagnostics (not part of the routing path):
  * moe_router_expf evaluates the library's device fp32 exponential on n values
  *   (x, y: device fp32 [n]); used to check it bit-for-bit against its specification.
+ * moe_router_exp_value evaluates the exponential the softmax forward uses for its
+ *   numerators exp(x - max) on n values (defined for x <= 0; x, y: device fp32 [n]);
+ *   used to check its error against exp in double precision.
  * moe_router_noop launches an empty kernel through the same path as the other calls:
  *   the launch-latency floor the fused decode call is measured against. */
 int moe_router_expf(const float* x, float* y, int n, mr_stream_t stream);
+int moe_router_exp_value(const float* x, float* y, int n, mr_stream_t stream);
 int moe_router_noop(mr_stream_t stream);
 
 #ifdef __cplusplus

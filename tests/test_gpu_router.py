@@ -316,6 +316,31 @@ def test_device_exp_matches_its_specification_bit_for_bit(mr, orc):
     assert np.max(np.abs(yc[fin].astype(np.float64) - cuda_exp[fin]) / ulp) <= 2.0
 
 
+def test_softmax_value_exp_error_bound(mr):
+    """The exponential of the softmax numerators exp(x - max), x - max <= 0, against
+    exp in double precision: relative error at most 2^-21 plus ln 2 * |x log2 e| *
+    2^-24 (the one rounding of x log2 e) where the result is a normal fp32 number;
+    below that it flushes towards zero (absolute error under 2^-126)."""
+    gen = torch.Generator().manual_seed(11)
+    x = torch.cat([torch.linspace(-104.0, 0.0, 1 << 21), -torch.rand(1 << 20, generator=gen) * 16.0,
+                   -torch.rand(1 << 18, generator=gen) * 1e-3,
+                   torch.tensor([0.0, -0.0, -1e-30, -0.5, -1.0, -87.0, -87.4, -88.0, -200.0, float("-inf")])])
+    x = x.to(torch.float32).contiguous()
+    y = torch.empty_like(x, device="cuda")
+    mr.moe_router_exp_value(x.cuda(), y)
+    torch.cuda.synchronize()
+    xd = x.numpy().astype(np.float64)
+    yd = y.cpu().numpy().astype(np.float64)
+    ref = np.exp(xd)
+    tiny = float(np.finfo(np.float32).tiny)
+    normal = ref >= tiny
+    bound = 2.0 ** -21 + np.abs(xd[normal]) * 2.0 ** -24  # ln 2 * |x log2 e| = |x|
+    rel = np.abs(yd[normal] - ref[normal]) / ref[normal]
+    assert np.all(rel <= bound), f"max relative error {rel.max():.3g}"
+    assert np.all(np.abs(yd[~normal] - ref[~normal]) <= tiny)
+    assert np.all(yd[x.numpy() == 0.0] == 1.0)
+
+
 @pytest.mark.parametrize("w", [synth.large_softmax(36), synth.large_softmax(8), synth.large_e_softmax(),
                                synth.large_e_sigmoid()], ids=lambda w: w.name)
 def test_aux_scores_full_size_sampled_rows(mr, orc, w):

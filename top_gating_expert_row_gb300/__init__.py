@@ -61,6 +61,7 @@ _SIGS = {
     "moe_router_strerror": ([_I], ctypes.c_char_p),
     "moe_router_set_topk_path": ([_I, _I], _I),
     "moe_router_expf": ([_P, _P, _I, _P], _I),
+    "moe_router_exp_value": ([_P, _P, _I, _P], _I),
     "moe_router_noop": ([_P], _I),
     "moe_router_device_status": ([_P, _I, _P], _I),
     "moe_router_bwd_dtype": ([_PP, _I, _P, _P, _P, _P, _P], _I),
@@ -261,6 +262,10 @@ def moe_router_set_wait_test(tries: int = 0, drop_copies: int = 0) -> int:
 
 def moe_router_expf(x, y, stream=None) -> int:
     return _ok(_lib.moe_router_expf(_ptr(x), _ptr(y), x.numel(), _stream(stream)), "moe_router_expf")
+
+
+def moe_router_exp_value(x, y, stream=None) -> int:
+    return _ok(_lib.moe_router_exp_value(_ptr(x), _ptr(y), x.numel(), _stream(stream)), "moe_router_exp_value")
 
 
 def moe_router_noop(stream=None) -> int:

@@ -209,6 +209,14 @@ __global__ void k_expf(const float* x, float* y, int n)
     }
 }
 
+// The softmax-value exponential on each input (the forward's numerators).
+__global__ void k_exp_value(const float* x, float* y, int n)
+{
+    pdl_trigger_small();
+    pdl_wait();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) y[i] = exp_value(x[i]);
+}
+
 // The decode launch floor: an empty kernel launched the way the routing
 // kernels are (it takes part in the launch overlap like them).
 __global__ void k_noop()
@@ -765,6 +773,16 @@ int moe_router_expf(const float* x, float* y, int n, mr_stream_t stream)
     if (n < 0 || (n > 0 && (!x || !y))) return MR_EINVAL;
     if (n == 0) return MR_OK;
     return from_cuda(launch_expf(x, y, n, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_router_exp_value(const float* x, float* y, int n, mr_stream_t stream)
+{
+    if (n < 0 || (n > 0 && (!x || !y))) return MR_EINVAL;
+    if (n == 0) return MR_OK;
+    const long long blocks = (static_cast<long long>(n) + 255) / 256;
+    const int grid = static_cast<int>(blocks < 4096 ? blocks : 4096);
+    return from_cuda(launch_kernel(k_exp_value, dim3(grid), dim3(256), 0, reinterpret_cast<cudaStream_t>(stream), 0,
+                                   x, y, n));
 }
 
 int moe_router_noop(mr_stream_t stream) { return from_cuda(launch_noop(reinterpret_cast<cudaStream_t>(stream))); }

@@ -96,27 +96,6 @@ __device__ __forceinline__ float2 exp_spec2(float2 x)
                        __fmul_rn(__fmul_rn(p.y, pow2_normal(hy)), pow2_normal(ny - hy)));
 }
 
-// exp for x <= 0 where only the value matters (softmax numerators): the same
-// reduction and polynomial, with x clamped at -87 so that 2^n stays a normal
-// scale applied by one exponent add. Below -87 it returns exp(-87) ~ 1.6e-38
-// instead of a smaller number, an absolute error under 2e-38.
-__device__ __forceinline__ float exp_nonpos(float x)
-{
-    x = fmaxf(x, -87.0f);
-    const float nf = rintf(__fmul_rn(x, kLog2e));
-    float r = __fmaf_rn(-nf, kLn2Hi, x);
-    r = __fmaf_rn(-nf, kLn2Lo, r);
-    const float p = exp_poly(r);
-    return __int_as_float(__float_as_int(p) + (__float2int_rn(nf) << 23));
-}
-
-// exp(x) for x <= 0 where only the value matters (softmax numerators), in
-// about eight instructions: e^x = 2^n * 2^f with n = rint(x*log2 e) and
-// f = x*log2 e - n computed from a two-part log2 e (f = fma(x, L2E_HI, -n),
-// then + x*L2E_LO), so f in [-1/2, 1/2] carries no error from rounding
-// x*log2 e; 2^f comes from the hardware base-2 exponential (relative error
-// about 2^-22), 2^n is an exponent add. x is clamped at -87 (2^n stays normal;
-// below that the result is exp(-87) ~ 1.6e-38 instead of smaller).
 constexpr float kLog2eHi = kLog2e;
 constexpr float kLog2eLo = static_cast<float>(1.0 / kLn2 - static_cast<double>(kLog2e));
 
@@ -127,18 +106,16 @@ __device__ __forceinline__ float exp2_hw(float f)
     return y;
 }
 
+// exp(x) for x <= 0 where only the value matters (softmax numerators), in
+// three instructions: the hardware base-2 exponential of x log2 e, formed as
+// fma(x, L2E_HI, x * L2E_LO) from a two-part log2 e with one rounding. Its
+// relative error is that rounding (at most |x log2 e| * 2^-24, ln 2 times that
+// in the result) plus the hardware exponential's; results below 2^-126 flush
+// to zero. Not the specification exp_spec: these values decide no selection
+// (softmax selects on the logits), they are compared within a tolerance.
 __device__ __forceinline__ float exp_value(float x)
 {
-    // n = rint(x*log2 e) by adding 1.5*2^23: the sum's low mantissa bits hold n
-    // (|n| < 2^22), and since the shifter's own bits vanish when shifted left
-    // by 23, (bits of t) << 23 is exactly n << 23, the exponent increment.
-    constexpr float kShifter = 12582912.0f;  // 1.5 * 2^23
-    x = fmaxf(x, -87.0f);
-    const float t = __fmaf_rn(x, kLog2eHi, kShifter);
-    const float n = __fsub_rn(t, kShifter);
-    float f = __fmaf_rn(x, kLog2eHi, -n);
-    f = __fmaf_rn(x, kLog2eLo, f);
-    return __int_as_float(__float_as_int(exp2_hw(f)) + (__float_as_int(t) << 23));
+    return exp2_hw(__fmaf_rn(x, kLog2eHi, __fmul_rn(x, kLog2eLo)));
 }
 
 // exp_value on two values at once: the same operations, with the floating-point
@@ -146,15 +123,9 @@ __device__ __forceinline__ float exp_value(float x)
 // exactly as the scalar op), so each result is bit-identical to exp_value's.
 __device__ __forceinline__ float2 exp_value2(float2 x)
 {
-    constexpr float kShifter = 12582912.0f;  // 1.5 * 2^23
-    x.x = fmaxf(x.x, -87.0f);
-    x.y = fmaxf(x.y, -87.0f);
-    const float2 t = __ffma2_rn(x, make_float2(kLog2eHi, kLog2eHi), make_float2(kShifter, kShifter));
-    const float2 n = __fadd2_rn(t, make_float2(-kShifter, -kShifter));
-    float2 f = __ffma2_rn(x, make_float2(kLog2eHi, kLog2eHi), make_float2(-n.x, -n.y));
-    f = __ffma2_rn(x, make_float2(kLog2eLo, kLog2eLo), f);
-    return make_float2(__int_as_float(__float_as_int(exp2_hw(f.x)) + (__float_as_int(t.x) << 23)),
-                       __int_as_float(__float_as_int(exp2_hw(f.y)) + (__float_as_int(t.y) << 23)));
+    const float2 y = __ffma2_rn(x, make_float2(kLog2eHi, kLog2eHi),
+                                __fmul2_rn(x, make_float2(kLog2eLo, kLog2eLo)));
+    return make_float2(exp2_hw(y.x), exp2_hw(y.y));
 }
 
 // Logistic function 1 / (1 + exp(-x)), IEEE add and correctly rounded
