@@ -9,15 +9,15 @@
 // than the instruction caches, so warps stalled on instruction fetch; here the
 // whole routine is a few hundred instructions.
 //
-// Scores never take shared memory when the intermediate output is requested:
-// the scores pass writes them (softmax: the unnormalised numerators) straight
-// into the caller's intermediate row, and the emit pass reads them back from
-// L2 and overwrites them with the final values. The row is rewritten in L2
-// before it is evicted, so DRAM sees one write, and each warp needs only its
-// 9 KB of keys (E = 2304), which keeps twice as many warps resident as a
-// second shared row would. Without the intermediate output, softmax recomputes
-// exp(x - max) from the key (the key map is invertible) and sigmoid keeps its
-// scores in a shared row.
+// Scores never take shared memory, so each warp needs only its 9 KB of keys
+// (E = 2304), which keeps twice as many warps resident as a second shared row
+// would. Softmax makes two exp passes over the keys (the key map is
+// invertible): the first sums the numerators exp(x - max) (and, once the
+// threshold is known, writes out the candidates), the second writes the final
+// scores into the intermediate row; a winner's score is recomputed from its
+// key. Sigmoid writes its scores into the intermediate row as it makes the
+// keys (or, without that output, keeps them in a shared row) and reads the
+// winners' back.
 #pragma once
 
 #include "route.cuh"
@@ -85,7 +85,7 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
     // every pass below touches only the lane's own chunks (v*128 + 4*lane .. +3)
     auto k4 = [&](int v) -> uint4& { return *reinterpret_cast<uint4*>(kbuf + v * 128 + lane4); };
 
-    float* irow0 = a.inter ? a.inter + static_cast<size_t>(t) * E : nullptr;  // score scratch + output
+    float* irow0 = a.inter ? a.inter + static_cast<size_t>(t) * E : nullptr;  // intermediate output row
     // The previous row's threshold key, when there is one, is tested while the
     // keys are made: cw = this lane's count of keys >= warm (0 is never a key
     // of a real element, so warm = 0 means none).
@@ -250,10 +250,18 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
         m = float_of(kmax);
         uint32_t cpos = fused_pick ? warp_exclusive_scan(static_cast<uint32_t>(lane_lo), lane) : 0u;
         const uint32_t ppiv = lo;  // fused_pick: candidates are the keys >= lo
+        unsigned long long cm = 0ull;  // fused_pick: bit v set when chunk v holds a candidate
         float2 sum01 = make_float2(0.0f, 0.0f), sum23 = make_float2(0.0f, 0.0f);
         const float2 negm = make_float2(-m, -m);
-        // batches of kExpBatch chunks, keys loaded first: with generic pointers
-        // the compiler cannot move a later shared load above an earlier global store
+        // exp(x - m) of a chunk's keys, x - m computed as x + (-m) (the same
+        // IEEE result); padding keys (0) give 0
+        auto chunk_exp = [&](const uint4& q) {
+            const float2 e01 = exp_value2(__fadd2_rn(make_float2(float_of(q.x), float_of(q.y)), negm));
+            const float2 e23 = exp_value2(__fadd2_rn(make_float2(float_of(q.z), float_of(q.w)), negm));
+            return FULL ? make_float4(e01.x, e01.y, e23.x, e23.y)
+                        : make_float4(q.x ? e01.x : 0.0f, q.y ? e01.y : 0.0f, q.z ? e23.x : 0.0f, q.w ? e23.y : 0.0f);
+        };
+        // first pass: the sum (batches of kExpBatch chunks, keys loaded first)
         constexpr int kExpBatch = 2;
         for (int v0 = 0; v0 < nv; v0 += kExpBatch) {
             uint4 qb[kExpBatch];
@@ -265,39 +273,60 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
                 const int v = v0 + u;
                 if (v >= nv) break;
                 const uint4 q = qb[u];
-                // padding keys are 0: their numerator is dropped (computed, then selected away);
-                // x - m is computed as x + (-m), the same IEEE result
-                const float2 e01 = exp_value2(__fadd2_rn(make_float2(float_of(q.x), float_of(q.y)), negm));
-                const float2 e23 = exp_value2(__fadd2_rn(make_float2(float_of(q.z), float_of(q.w)), negm));
-                const float4 e = FULL ? make_float4(e01.x, e01.y, e23.x, e23.y)
-                                      : make_float4(q.x ? e01.x : 0.0f, q.y ? e01.y : 0.0f, q.z ? e23.x : 0.0f,
-                                                    q.w ? e23.y : 0.0f);
+                const float4 e = chunk_exp(q);
                 sum01 = __fadd2_rn(sum01, make_float2(e.x, e.y));
                 sum23 = __fadd2_rn(sum23, make_float2(e.z, e.w));
-                if (SELECT && fused_pick) {
-                    const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
-                    const uint32_t e0i = static_cast<uint32_t>(v * 128 + lane4);
+                if (SELECT && fused_pick)
+                    cm |= static_cast<unsigned long long>(max(max(q.x, q.y), max(q.z, q.w)) >= ppiv) << v;
+            }
+        }
+        // the candidates, from the marked chunks only (a few per lane)
+        if (SELECT && fused_pick) {
+            while (cm) {
+                const int v = __ffsll(static_cast<long long>(cm)) - 1;
+                cm &= cm - 1ull;
+                const uint4 q = k4(v);
+                const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+                const uint32_t e0i = static_cast<uint32_t>(v * 128 + lane4);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const bool in = kq[c] >= ppiv;
-                        if (in) cand[cpos] = comp(kq[c], e0i + c);
-                        cpos += in ? 1u : 0u;
-                    }
-                }
-                if (irow0) {
-                    const int o = v * 128 + lane4;
-                    if (vec && whole(v)) {
-                        *reinterpret_cast<float4*>(irow0 + o) = e;
-                    } else {
-                        const float ev[4] = {e.x, e.y, e.z, e.w};
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            if (o + c < E) irow0[o + c] = ev[c];
-                    }
+                for (int c = 0; c < 4; ++c) {
+                    // positions come from exact counts of these same keys, so
+                    // cpos stays below cnt_lo <= cap
+                    const bool in = kq[c] >= ppiv;
+                    if (in) cand[cpos] = comp(kq[c], e0i + c);
+                    cpos += in ? 1u : 0u;
                 }
             }
         }
         vmul = __frcp_rn(warp_sum(__fadd_rn(__fadd_rn(sum01.x, sum01.y), __fadd_rn(sum23.x, sum23.y))));
+        // second pass: the final scores s = exp(x - m) * (1 / sum), the values a
+        // winner's score_of gives too
+        if (irow0) {
+            const float2 vm = make_float2(vmul, vmul);
+            for (int v0 = 0; v0 < nv; v0 += kExpBatch) {
+                uint4 qb[kExpBatch];
+#pragma unroll
+                for (int u = 0; u < kExpBatch; ++u)
+                    qb[u] = (v0 + u < nv) ? k4(v0 + u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int u = 0; u < kExpBatch; ++u) {
+                    const int v = v0 + u;
+                    if (v >= nv) break;
+                    const float4 e = chunk_exp(qb[u]);
+                    const float2 s01 = __fmul2_rn(make_float2(e.x, e.y), vm);
+                    const float2 s23 = __fmul2_rn(make_float2(e.z, e.w), vm);
+                    const int o = v * 128 + lane4;
+                    if (vec && whole(v)) {
+                        *reinterpret_cast<float4*>(irow0 + o) = make_float4(s01.x, s01.y, s23.x, s23.y);
+                    } else {
+                        const float sv[4] = {s01.x, s01.y, s23.x, s23.y};
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            if (o + c < E) irow0[o + c] = sv[c];
+                    }
+                }
+            }
+        }
     }
     __syncwarp();  // scores written by one lane are read by another below
     // a winner's score: softmax recomputes it from the key; sigmoid reads it back
@@ -440,64 +469,27 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
     wsum = warp_sum(wsum);
     const float scale = a.renorm ? (wsum > 0.0f ? __fdiv_rn(a.scaling, wsum) : 0.0f) : a.scaling;
 
-    // 5. dense rows: intermediate = s; probs and routing_map are written as zero
-    //    vectors and the k_r winners are patched in afterwards, so no per-element
-    //    membership test is needed
-    if (a.probs || a.map || a.inter) {
+    // 5. dense rows (the intermediate row holds its final scores already):
+    //    probs and routing_map are written as zero vectors and the k_r winners
+    //    are patched in afterwards, so no per-element membership test is needed
+    if (a.probs || a.map) {
         InT* prow = a.probs ? static_cast<InT*>(a.probs) + static_cast<size_t>(t) * E : nullptr;
         uint8_t* mrow = a.map ? a.map + static_cast<size_t>(t) * E : nullptr;
-        float* irow = a.inter ? a.inter + static_cast<size_t>(t) * E : nullptr;
-        // sigmoid scores in the intermediate row are final already
-        const bool fix_inter = irow && SCORE == kSoftmax;
-        if (FULL) {
-            // batches of 4 chunks: all loads first (the output rows might alias
-            // for the compiler, so it would not hoist them past the stores)
-            for (int v0 = 0; v0 < nv; v0 += 4) {
-                float4 q[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (fix_inter && v0 + u < nv)
-                        q[u] = __ldcg(reinterpret_cast<const float4*>(irow + (v0 + u) * 128 + lane4));
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    if (v0 + u >= nv) break;
-                    const int e0 = (v0 + u) * 128 + lane4;
-                    if (fix_inter) {
-                        const float2 xy = __fmul2_rn(make_float2(q[u].x, q[u].y), make_float2(vmul, vmul));
-                        const float2 zw = __fmul2_rn(make_float2(q[u].z, q[u].w), make_float2(vmul, vmul));
-                        *reinterpret_cast<float4*>(irow + e0) = make_float4(xy.x, xy.y, zw.x, zw.y);
-                    }
-                    if (prow) {
-                        const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                        store4<InT>(prow + e0, z);
-                    }
-                    if (mrow) *reinterpret_cast<uint32_t*>(mrow + e0) = 0u;
+        for (int v = 0; v < nv; ++v) {
+            const int e0 = v * 128 + lane4;
+            if (!FULL && e0 >= E) continue;
+            if (vec && whole(v)) {
+                if (prow) {
+                    const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    store4<InT>(prow + e0, z);
                 }
-            }
-        } else {
-            for (int v = 0; v < nv; ++v) {
-                const int e0 = v * 128 + lane4;
-                if (e0 >= E) continue;
-                if (vec && whole(v)) {
-                    if (fix_inter) {
-                        float4 q = __ldcg(reinterpret_cast<const float4*>(irow + e0));
-                        q.x = __fmul_rn(q.x, vmul); q.y = __fmul_rn(q.y, vmul);
-                        q.z = __fmul_rn(q.z, vmul); q.w = __fmul_rn(q.w, vmul);
-                        *reinterpret_cast<float4*>(irow + e0) = q;
-                    }
-                    if (prow) {
-                        const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                        store4<InT>(prow + e0, z);
-                    }
-                    if (mrow) *reinterpret_cast<uint32_t*>(mrow + e0) = 0u;
-                } else {
+                if (mrow) *reinterpret_cast<uint32_t*>(mrow + e0) = 0u;
+            } else {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (e0 + c >= E) break;
-                        if (fix_inter) irow[e0 + c] = __fmul_rn(__ldcg(irow + e0 + c), vmul);
-                        if (prow) store_scalar<InT>(prow + e0 + c, 0.0f);
-                        if (mrow) mrow[e0 + c] = 0;
-                    }
+                for (int c = 0; c < 4; ++c) {
+                    if (e0 + c >= E) break;
+                    if (prow) store_scalar<InT>(prow + e0 + c, 0.0f);
+                    if (mrow) mrow[e0 + c] = 0;
                 }
             }
         }
