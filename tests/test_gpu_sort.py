@@ -97,6 +97,16 @@ FUSED = [synth.decode(T) for T in synth.DECODE_TS] + [synth.decode_gpt_oss(T) fo
     synth.Workload("decode_T16_grouped_shared", 16, 384, 9, synth.SIGMOID, synth.BF16, renorm=1, scaling=2.827,
                    n_group=8, topk_group=4, n_shared=1, bias_range=0.05, zipf_s=1.1, block_m=64),
     synth.Workload("decode_T5_e128_k4", 5, 128, 4, synth.SOFTMAX, synth.BF16, renorm=1, block_m=16),
+    # at most 32 pairs: a warp per token, one warp sorts (edges of that form)
+    synth.Workload("tiny_T1_e1024_k32", 1, 1024, 32, synth.SOFTMAX, synth.F32, renorm=1, block_m=16),
+    synth.Workload("tiny_T2_grouped_shared_bm24", 2, 384, 9, synth.SIGMOID, synth.BF16, renorm=1, scaling=2.827,
+                   n_group=8, topk_group=4, n_shared=1, bias_range=0.05, block_m=24),
+    synth.Workload("tiny_T16_e64_k2_bm1", 16, 64, 2, synth.SOFTMAX, synth.F32, renorm=1, block_m=1),
+    synth.Workload("tiny_T7_e256_k4_bm3", 7, 256, 4, synth.SOFTMAX, synth.BF16, renorm=1, block_m=3),
+    synth.Workload("tiny_T3_e37_k10_sigmoid", 3, 37, 10, synth.SIGMOID, synth.F32, renorm=1, scaling=1.5,
+                   bias_range=0.1, block_m=8),
+    synth.Workload("above_tiny_T3_e100_k11", 3, 100, 11, synth.SIGMOID, synth.F32, renorm=1, scaling=1.5,
+                   bias_range=0.1, block_m=8),
     synth.Workload("fused32_T17", 17, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
     synth.Workload("fused32_T32_e256_k8", 32, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
     synth.Workload("fused32_T24_e128_k4", 24, 128, 4, synth.SOFTMAX, synth.BF16, renorm=1, block_m=16),

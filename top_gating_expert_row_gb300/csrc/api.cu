@@ -151,6 +151,10 @@ int launch_fused_s0_d0(const RouteArgs&, const SortArgs&, int, bool, cudaStream_
 int launch_fused_s0_d1(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
 int launch_fused_s1_d0(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
 int launch_fused_s1_d1(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
+int launch_fused_tiny_s0_d0(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
+int launch_fused_tiny_s0_d1(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
+int launch_fused_tiny_s1_d0(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
+int launch_fused_tiny_s1_d1(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
 
 int launch_fwd(int score_fn, int in_dtype, const RouteArgs& a, int nv_idx, bool select, cudaStream_t st)
 {
@@ -173,6 +177,15 @@ int launch_fused_decode(int score_fn, int in_dtype, const RouteArgs& a, const So
     if (score_fn == kSoftmax)
         return in_dtype ? launch_fused_s0_d1(a, s, nv_idx, select, st) : launch_fused_s0_d0(a, s, nv_idx, select, st);
     return in_dtype ? launch_fused_s1_d1(a, s, nv_idx, select, st) : launch_fused_s1_d0(a, s, nv_idx, select, st);
+}
+
+int launch_fused_tiny(int score_fn, int in_dtype, const RouteArgs& a, const SortArgs& s, int nv_idx, bool select,
+                      cudaStream_t st)
+{
+    if (score_fn == kSoftmax)
+        return in_dtype ? launch_fused_tiny_s0_d1(a, s, nv_idx, select, st)
+                        : launch_fused_tiny_s0_d0(a, s, nv_idx, select, st);
+    return in_dtype ? launch_fused_tiny_s1_d1(a, s, nv_idx, select, st) : launch_fused_tiny_s1_d0(a, s, nv_idx, select, st);
 }
 
 // ---- launch overlap ---------------------------------------------------------------------------
@@ -729,6 +742,13 @@ int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int
     // k_r = 32
     const int force = g_path.forced();
     const bool decode_select = force == 2 || (force == 0 && k_r > 32);
+    // at most 32 pairs: a warp per token, one warp sorts (16 warps at most)
+    if (p->T >= 1 && p->T <= 16 && p->T * p->topk <= kFusedTinyPairs && kNvBuckets[nv] <= kRegisterMaxNv) {
+        RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, topk_idx, topk_w, status);
+        SortArgs s{sorted_token_ids, sorted_weights, expert_ids, num_tokens_post_pad, E_tot, block_m,
+                   log2_if_pow2(block_m)};
+        return from_cuda(launch_fused_tiny(p->score_fn, p->in_dtype, a, s, nv, decode_select, st));
+    }
     if (p->T > 16 && p->T <= kFusedClusterMaxTokens && kNvBuckets[nv] <= kRegisterMaxNv) {
         RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, topk_idx, topk_w, status);
         SortArgs s{sorted_token_ids, sorted_weights, expert_ids, num_tokens_post_pad, E_tot, block_m,

@@ -290,6 +290,84 @@ __global__ void __launch_bounds__(THREADS, 1) k_fused_decode(RouteArgs a, SortAr
     }
 }
 
+// Fused route + sort for at most 32 pairs (T * topk <= 32): T warps, a warp per
+// token, then warp 0 sorts with a pair per lane. A match on the expert ids gives
+// each pair its stable rank within its expert (lanes in pair order) and its
+// expert's count; an expert's offset is the sum of the padded counts of the
+// smaller expert ids present, read from the other lanes by shuffles. No pass
+// over all E_tot experts and at most one block barrier (none for one token):
+// a decode call waits on this chain alone.
+template <int NV, bool SELECT, bool FULL>
+__global__ void __launch_bounds__(kFusedThreads, 1) k_fused_tiny(RouteArgs a, SortArgs s)
+{
+    pdl_trigger_small();
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, SELECT, a.n_group > 0);
+    int32_t* s_idx = reinterpret_cast<int32_t*>(smem + static_cast<size_t>(a.T) * L.bytes);
+    float* s_w = reinterpret_cast<float*>(s_idx + kFusedTinyPairs);
+    const int N = a.T * a.topk;
+    pdl_wait();
+    {
+        unsigned char* wsm = smem + static_cast<size_t>(warp) * L.bytes;
+        uint32_t warm = 0u;
+        const int tok = warp;
+        const float scale = route_row<kScore, InT, NV, SELECT, FULL>(a, tok, wsm, L, lane, warm);
+        const size_t o = static_cast<size_t>(tok) * a.topk;
+        const uint32_t* win_idx = reinterpret_cast<const uint32_t*>(wsm + L.win_idx);
+        const float* win_val = reinterpret_cast<const float*>(wsm + L.win_val);
+        if (lane < a.topk) {  // compact outputs, to shared and global
+            const bool routed = lane < a.k_r;
+            const int32_t id = routed ? static_cast<int32_t>(win_idx[lane]) : a.E + (lane - a.k_r);
+            const float wv = routed ? __fmul_rn(win_val[lane], scale) : a.shared_weight;
+            s_idx[o + lane] = id;
+            s_w[o + lane] = wv;
+            if (a.topk_idx) a.topk_idx[o + lane] = id;
+            if (a.topk_w) a.topk_w[o + lane] = wv;
+        }
+    }
+    if (a.T > 1) {
+        __syncthreads();
+    } else {
+        __syncwarp();
+    }
+    if (warp != 0) return;
+    // lane p: pair p (token p / topk, slot p % topk); ids outside [0, E_tot)
+    // (NaN rows) are left out
+    const int e = lane < N ? s_idx[lane] : -1;
+    const bool valid = e >= 0 && e < s.E_tot;
+    const uint32_t key = valid ? static_cast<uint32_t>(e) : 0xffffffffu;
+    const uint32_t same = __match_any_sync(kFull, key);
+    const uint32_t rank = static_cast<uint32_t>(__popc(same & ((1u << lane) - 1u)));
+    const uint32_t c = static_cast<uint32_t>(__popc(same));
+    const uint32_t bm = static_cast<uint32_t>(s.block_m);
+    const uint32_t pad = s.bm_shift >= 0 ? ((c + bm - 1u) >> s.bm_shift) << s.bm_shift : (c + bm - 1u) / bm * bm;
+    const uint32_t lead = (valid && rank == 0u) ? pad : 0u;  // each expert's padded count, once
+    uint32_t off = 0u;
+#pragma unroll 8
+    for (int q = 0; q < 32; ++q) {
+        const uint32_t kq = __shfl_sync(kFull, key, q);
+        const uint32_t pq = __shfl_sync(kFull, lead, q);
+        off += kq < key ? pq : 0u;
+    }
+    const uint32_t npp = __reduce_add_sync(kFull, lead);
+    // every position a sentinel first, then the pairs over them (__syncwarp
+    // orders the two sets of stores)
+    for (uint32_t q = lane; q < npp; q += 32) {
+        s.ids[q] = N;
+        if (s.w) s.w[q] = 0.0f;
+    }
+    __syncwarp();
+    if (valid) {
+        s.ids[off + rank] = lane;
+        if (s.w) s.w[off + rank] = s_w[lane];
+        if (rank == 0u)
+            for (uint32_t q = off; q < off + pad; q += bm)
+                s.expert_ids[s.bm_shift >= 0 ? q >> s.bm_shift : q / bm] = e;
+    }
+    if (lane == 0) *s.num_post_pad = static_cast<int32_t>(npp);
+}
+
 // Fused route + sort in one launch of one thread-block cluster (cs CTAs of 32
 // warps): CTA r routes tokens [r*TP, min(T, (r+1)*TP)), a warp per token,
 // writes the compact outputs and keeps the pairs in shared memory, then the
@@ -368,6 +446,20 @@ ClusterFn cluster_kernel(int nv_idx)
         case 4: return k_fused_cluster<4, SELECT, FULL>;
         case 6: return k_fused_cluster<6, SELECT, FULL>;
         case 8: return k_fused_cluster<8, SELECT, FULL>;
+    }
+    return nullptr;
+}
+
+template <bool SELECT, bool FULL>
+FusedFn tiny_kernel(int nv_idx)
+{
+    switch (kNvBuckets[nv_idx]) {
+        case 1: return k_fused_tiny<1, SELECT, FULL>;
+        case 2: return k_fused_tiny<2, SELECT, FULL>;
+        case 3: return k_fused_tiny<3, SELECT, FULL>;
+        case 4: return k_fused_tiny<4, SELECT, FULL>;
+        case 6: return k_fused_tiny<6, SELECT, FULL>;
+        case 8: return k_fused_tiny<8, SELECT, FULL>;
     }
     return nullptr;
 }
@@ -477,6 +569,20 @@ int MR_CAT(launch_fused, MR_SUFFIX)(const RouteArgs& a, const SortArgs& s, int n
     int err = ensure_smem(reinterpret_cast<const void*>(f), smem);
     if (err != cudaSuccess) return err;
     return launch_kernel(f, dim3(1), dim3(threads), smem, st, 0, a, s);
+}
+
+int MR_CAT(launch_fused_tiny, MR_SUFFIX)(const RouteArgs& a, const SortArgs& s, int nv_idx, bool select,
+                                         cudaStream_t st)
+{
+    const bool full = a.vec && a.E == 128 * kNvBuckets[nv_idx];
+    const FusedFn f = select ? (full ? tiny_kernel<true, true>(nv_idx) : tiny_kernel<true, false>(nv_idx))
+                             : (full ? tiny_kernel<false, true>(nv_idx) : tiny_kernel<false, false>(nv_idx));
+    if (!f) return cudaErrorInvalidValue;
+    const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, select, a.n_group > 0);
+    const size_t smem = static_cast<size_t>(L.bytes) * a.T + 2 * kFusedTinyPairs * 4;
+    int err = ensure_smem(reinterpret_cast<const void*>(f), smem);
+    if (err != cudaSuccess) return err;
+    return launch_kernel(f, dim3(1), dim3(32 * a.T), smem, st, 0, a, s);
 }
 
 }  // namespace mr

@@ -44,6 +44,8 @@ constexpr int kFusedMaxNv = 8;
 constexpr int kFusedWideThreads = 1024;
 constexpr int kFusedWideMaxNv = 2;
 constexpr int kFusedWideMaxTokens = 64;
+// T * topk <= 32 pairs (rows of E <= 1024): T warps route, one warp sorts
+constexpr int kFusedTinyPairs = 32;
 // whether moe_router_fused_fwd_sort runs as one launch for T tokens of row bucket nv
 inline bool fused_one_launch(int T, int nv_bucket)
 {
@@ -112,6 +114,8 @@ int launch_fwd(int score_fn, int in_dtype, const RouteArgs& a, int nv_idx, bool 
                cudaStream_t st);
 int launch_fused_decode(int score_fn, int in_dtype, const RouteArgs& a, const SortArgs& s,
                         int nv_idx, bool select, cudaStream_t st);
+int launch_fused_tiny(int score_fn, int in_dtype, const RouteArgs& a, const SortArgs& s, int nv_idx,
+                      bool select, cudaStream_t st);
 // The fused call as one launch of one thread-block cluster (a warp per token);
 // cudaErrorNotSupported, with nothing launched, when no cluster fits.
 int launch_fused_cluster(int score_fn, int in_dtype, const RouteArgs& a, const SortArgs& s, int nv_idx,
