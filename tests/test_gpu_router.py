@@ -45,6 +45,9 @@ CASES = [
     W("e192_g4_k8_m4", 70, 192, 8, SG, renorm=1, n_group=4, topk_group=2, n_shared=2, shared_weight=0.5),
     W("e48_g3_k6_m2", 70, 48, 6, SG, n_group=3, topk_group=3),
     W("bf16_e2304_k36", 64, 2304, 36, SM, BF16),
+    W("e64_k4_bf16", 200, 64, 4, SM, BF16),
+    W("e100_k37_bf16_ragged", 80, 100, 37, SM, BF16, renorm=1),
+    W("e768_k40_bf16", 60, 768, 40, SM, BF16, sigma=0.5),
     # rows wider than the register-resident buckets, up to the library's limit
     W("e4096_k36", 64, 4096, 36),
     W("e5000_k20_sigmoid_ragged", 30, 5000, 20, SG, renorm=1),
@@ -127,13 +130,17 @@ def _tie_logits(kind, T, E):
 @pytest.mark.parametrize("compact", [True, False], ids=["compact", "dense_only"])
 @pytest.mark.parametrize("path", [ARGMAX, SELECT], ids=["argmax", "select"])
 @pytest.mark.parametrize("kind", ["integers", "all_equal", "signed_zeros", "saturated_sigmoid", "two_values"])
-@pytest.mark.parametrize("E,k,fn,T", [(512, 36, SM, 96), (256, 8, SG, 96), (2304, 36, SG, 96), (64, 3, SM, 96),
-                                       (2304, 36, SM, 3500)])
-def test_ties_go_to_lower_index(mr, orc, kind, E, k, fn, T, path, compact):
+@pytest.mark.parametrize("E,k,fn,T,dt", [(512, 36, SM, 96, F32), (256, 8, SG, 96, F32), (2304, 36, SG, 96, F32),
+                                          (64, 3, SM, 96, F32), (2304, 36, SM, 3500, F32), (256, 8, SM, 96, BF16),
+                                          (512, 36, SM, 96, BF16), (100, 37, SM, 50, BF16)])
+def test_ties_go_to_lower_index(mr, orc, kind, E, k, fn, T, dt, path, compact):
     # T=3500 gives every CTA of the persistent softmax wide-row grid several rows;
-    # dense_only takes the set-only selection (no candidate rank)
-    w = W(f"ties_{kind}", T, E, k, fn, renorm=1)
+    # dense_only takes the set-only selection (no candidate rank); bf16 softmax
+    # rows take the packed arg-max rounds
+    w = W(f"ties_{kind}", T, E, k, fn, dt, renorm=1)
     x = _tie_logits(kind, w.T, E)
+    if dt == BF16:
+        x = x.to(torch.bfloat16)
     xg = x.cuda()
     out = gpu_route(mr, w, xg, None, path, compact=compact)
     torch.cuda.synchronize()

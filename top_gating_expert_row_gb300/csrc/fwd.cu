@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_fused_tiny(RouteArgs a, So
     const uint32_t lead = (valid && rank == 0u) ? pad : 0u;  // each expert's padded count, once
     uint32_t off = 0u;
 #pragma unroll 8
-    for (int q = 0; q < 32; ++q) {
+    for (int q = 0; q < N; ++q) {  // lanes N.. hold no pair
         const uint32_t kq = __shfl_sync(kFull, key, q);
         const uint32_t pq = __shfl_sync(kFull, lead, q);
         off += kq < key ? pq : 0u;

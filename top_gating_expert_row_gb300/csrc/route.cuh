@@ -433,7 +433,51 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
     };
 
     // 3. selection
-    if (!SELECT) {
+    // bf16 softmax rows select on bf16 logits, whose keys carry a constant low
+    // half (0 or 0xffff, by sign): key & 0xffff0000 | ~index & 0xffff then
+    // orders exactly like (key, then lower index), so an arg-max round is one
+    // warp reduction that yields the winner and its index at once
+    constexpr bool kPacked = SCORE == kSoftmax && sizeof(InT) == 2;
+    if (!SELECT && kPacked) {
+        uint32_t b1 = 0u, b2 = 0u;    // the lane's best two composites after lc
+        uint32_t lc = 0xffffffffu;    // the lane's last winner (none yet)
+        auto rescan = [&]() {
+            b1 = 0u;
+            b2 = 0u;
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t q = (key[v][c] & 0xffff0000u) |
+                                       (~static_cast<uint32_t>(v * 128 + lane4 + c) & 0xffffu);
+                    const bool after = q < lc;
+                    const bool gt1 = after && q > b1;
+                    const bool gt2 = after && !gt1 && q > b2;
+                    b2 = gt1 ? b1 : (gt2 ? q : b2);
+                    b1 = gt1 ? q : b1;
+                }
+        };
+        rescan();
+        bool has2 = true;
+        for (int j = 0; j < k_r; ++j) {
+            const uint32_t w = __reduce_max_sync(kFull, b1);
+            const uint32_t widx = ~w & 0xffffu;
+            if (lane == 0) {
+                win_idx[j] = widx;
+                win_val[j] = __fmul_rn(vbuf[min(widx, static_cast<uint32_t>(E - 1))], vmul);
+            }
+            if (b1 == w) {  // this lane supplied the winner (composites are distinct)
+                lc = b1;
+                if (has2) {
+                    b1 = b2;
+                    has2 = false;
+                } else if (j + 1 < k_r) {
+                    rescan();
+                    has2 = true;
+                }
+            }
+        }
+    } else if (!SELECT) {
         // k_r rounds of arg-max over the lanes' best keys. Each lane keeps its two
         // best (key, index) pairs in selection order (larger key, then lower
         // index; the lane's elements are scanned in index order with strict
