@@ -626,14 +626,18 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
                 }
             }
             warm = lo;  // the next row's first pivot: this row's threshold
-            float ws = 0.0f;
+            float scale = a.scaling;
+            if (a.renorm) {
+                float ws = 0.0f;
 #pragma unroll
-            for (int v = 0; v < NV; ++v)
+                for (int v = 0; v < NV; ++v)
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    if (winmask & (1u << (v * 4 + c))) ws = __fadd_rn(ws, __fmul_rn(vbuf[v * 128 + lane4 + c], vmul));
-            const float wsum = warp_sum(ws);
-            const float scale = a.renorm ? (wsum > 0.0f ? __fdiv_rn(a.scaling, wsum) : 0.0f) : a.scaling;
+                    for (int c = 0; c < 4; ++c)
+                        if (winmask & (1u << (v * 4 + c)))
+                            ws = __fadd_rn(ws, __fmul_rn(vbuf[v * 128 + lane4 + c], vmul));
+                const float wsum = warp_sum(ws);
+                scale = wsum > 0.0f ? __fdiv_rn(a.scaling, wsum) : 0.0f;
+            }
             dense_rows();
             __syncwarp();  // the winners' writes below land after every lane's zeros
 #pragma unroll
@@ -716,11 +720,14 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
     }
     __syncwarp();
 
-    // 4. weights
-    float wsum = 0.0f;
-    for (int j = lane; j < k_r; j += 32) wsum = __fadd_rn(wsum, win_val[j]);
-    wsum = warp_sum(wsum);
-    const float scale = a.renorm ? (wsum > 0.0f ? __fdiv_rn(a.scaling, wsum) : 0.0f) : a.scaling;
+    // 4. weights (the sum of the winners' scores only matters with renorm)
+    float scale = a.scaling;
+    if (a.renorm) {
+        float wsum = 0.0f;
+        for (int j = lane; j < k_r; j += 32) wsum = __fadd_rn(wsum, win_val[j]);
+        wsum = warp_sum(wsum);
+        scale = wsum > 0.0f ? __fdiv_rn(a.scaling, wsum) : 0.0f;
+    }
 
     // 5. dense rows: intermediate = s; probs and routing_map are written as zero
     //    vectors and the k_r winners are patched in afterwards (compact outputs:

@@ -463,11 +463,14 @@ __device__ __forceinline__ float route_row_wide(const RouteArgs& a, int t, unsig
     __syncwarp();
     if (!SELECT && FULL && st.next && lane == 0) bulk_load_row(wsm + L.kbuf + st.off, st.next, st.bytes, st.bar, st.drop);
 
-    // 4. weights
-    float wsum = 0.0f;
-    for (int j = lane; j < k_r; j += 32) wsum = __fadd_rn(wsum, win_val[j]);
-    wsum = warp_sum(wsum);
-    const float scale = a.renorm ? (wsum > 0.0f ? __fdiv_rn(a.scaling, wsum) : 0.0f) : a.scaling;
+    // 4. weights (the sum of the winners' scores only matters with renorm)
+    float scale = a.scaling;
+    if (a.renorm) {
+        float wsum = 0.0f;
+        for (int j = lane; j < k_r; j += 32) wsum = __fadd_rn(wsum, win_val[j]);
+        wsum = warp_sum(wsum);
+        scale = wsum > 0.0f ? __fdiv_rn(a.scaling, wsum) : 0.0f;
+    }
 
     // 5. dense rows (the intermediate row holds its final scores already):
     //    probs and routing_map are written as zero vectors and the k_r winners
