@@ -86,49 +86,37 @@ __host__ __device__ inline WarpLayout warp_layout(int k_r, int stop, int E, bool
 // ---------------------------------------------------------------------------
 // group_kept: the same selection, returned as a mask of the kept groups (bit g
 // set: group g is kept) without touching the keys.
+// Insert k into the descending list top[0..MAXM).
 template <int MAXM>
-__device__ uint32_t group_kept(const uint32_t* skeys, int E, int G, int gk, int m, int lane)
+__device__ __forceinline__ void top_insert(uint32_t (&top)[MAXM], uint32_t k)
 {
-    const int gs = E / G;
-    int lpg = 32 / G;                      // lanes per group, rounded down to a power of 2
-    lpg = 1 << (31 - __clz(lpg));
-    const int g = lane / lpg, j = lane % lpg;
-    uint32_t top[MAXM];
 #pragma unroll
-    for (int i = 0; i < MAXM; ++i) top[i] = 0u;
-    if (g < G) {
-#pragma unroll 4
-        for (int i = j; i < gs; i += lpg) {
-            uint32_t k = skeys[g * gs + i];
-#pragma unroll
-            for (int q = 0; q < MAXM; ++q) {
-                const uint32_t hi = max(k, top[q]);
-                k = min(k, top[q]);
-                top[q] = hi;
-            }
-        }
+    for (int q = 0; q < MAXM; ++q) {
+        const uint32_t hi = max(k, top[q]);
+        k = min(k, top[q]);
+        top[q] = hi;
     }
+}
+
+// The group selection from each lane's partial list (lanes g*lpg .. g*lpg+lpg-1
+// hold group g's): merge the lists across the group's lanes, score the group
+// (fp32 sum of its m largest keys, largest first), rank the G scores (ties to
+// the lower group index) and return the mask of the gk best.
+template <int MAXM>
+__device__ __forceinline__ uint32_t group_finish(uint32_t (&top)[MAXM], int G, int lpg, int gk, int m, int lane)
+{
     for (int o = 1; o < lpg; o <<= 1) {
         uint32_t other[MAXM];
 #pragma unroll
         for (int i = 0; i < MAXM; ++i) other[i] = __shfl_xor_sync(kFull, top[i], o);
 #pragma unroll
-        for (int i = 0; i < MAXM; ++i) {
-            uint32_t k = other[i];
-#pragma unroll
-            for (int q = 0; q < MAXM; ++q) {
-                const uint32_t hi = max(k, top[q]);
-                k = min(k, top[q]);
-                top[q] = hi;
-            }
-        }
+        for (int i = 0; i < MAXM; ++i) top_insert(top, other[i]);
     }
     float acc = float_of(top[0]);
 #pragma unroll
     for (int i = 1; i < MAXM; ++i)
         if (i < m) acc = __fadd_rn(acc, float_of(top[i]));
     const uint32_t sk = key_of(acc);
-    // rank the G group scores: ties go to the lower group index
     const uint32_t mine = __shfl_sync(kFull, sk, (lane < G ? lane : 0) * lpg);
     uint32_t rank = 0;
     for (int q = 0; q < G; ++q) {
@@ -136,6 +124,48 @@ __device__ uint32_t group_kept(const uint32_t* skeys, int E, int G, int gk, int 
         rank += (o > mine) || (o == mine && q < lane);
     }
     return __ballot_sync(kFull, lane < G && rank < (uint32_t)gk);
+}
+
+// lanes per group: 32 / G rounded down to a power of 2
+__device__ __forceinline__ int group_lanes(int G)
+{
+    const int lpg = 32 / G;
+    return 1 << (31 - __clz(lpg));
+}
+
+template <int MAXM>
+__device__ uint32_t group_kept(const uint32_t* skeys, int E, int G, int gk, int m, int lane)
+{
+    const int gs = E / G;
+    const int lpg = group_lanes(G);
+    const int g = lane / lpg, j = lane % lpg;
+    uint32_t top[MAXM];
+#pragma unroll
+    for (int i = 0; i < MAXM; ++i) top[i] = 0u;
+    if (g < G) {
+#pragma unroll 4
+        for (int i = j; i < gs; i += lpg) top_insert(top, skeys[g * gs + i]);
+    }
+    return group_finish(top, G, lpg, gk, m, lane);
+}
+
+// group_kept over per-chunk lists: for rows whose groups are whole chunks of 4
+// keys (gs % 4 == 0), entry n = the MAXM largest of keys 4n .. 4n+3, sorted;
+// group g is entries [g * gs/4, (g+1) * gs/4).
+template <int MAXM>
+__device__ uint32_t group_kept_entries(const uint32_t* ent, int G, int epg, int gk, int m, int lane)
+{
+    const int lpg = group_lanes(G);
+    const int g = lane / lpg, j = lane % lpg;
+    uint32_t top[MAXM];
+#pragma unroll
+    for (int i = 0; i < MAXM; ++i) top[i] = 0u;
+    if (g < G) {
+        for (int i = j; i < epg; i += lpg)
+#pragma unroll
+            for (int q = 0; q < MAXM; ++q) top_insert(top, ent[(g * epg + i) * MAXM + q]);
+    }
+    return group_finish(top, G, lpg, gk, m, lane);
 }
 
 template <int MAXM>
@@ -359,40 +389,79 @@ __device__ __forceinline__ float route_row(const RouteArgs& a, int t, unsigned c
     // 2. group limit (keys staged through shared memory)
     if (a.n_group > 0) {
         uint32_t* sk = reinterpret_cast<uint32_t*>(wsm + L.keys);
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            const int e0 = v * 128 + lane4;
-            if (whole(v)) {
-                *reinterpret_cast<uint4*>(sk + e0) = make_uint4(key[v][0], key[v][1], key[v][2], key[v][3]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    if (inside(v, c)) sk[e0 + c] = key[v][c];
-            }
-        }
-        __syncwarp();
         const int m = k_r / a.topk_group;
-        uint32_t kept;
-        if (m <= 1) kept = group_kept<1>(sk, E, a.n_group, a.topk_group, m, lane);
-        else if (m <= 2) kept = group_kept<2>(sk, E, a.n_group, a.topk_group, m, lane);
-        else if (m <= 4) kept = group_kept<4>(sk, E, a.n_group, a.topk_group, m, lane);
-        else kept = group_kept<8>(sk, E, a.n_group, a.topk_group, m, lane);
-        // the keys are still in registers: drop those of the groups not kept.
-        // An element's group e / gs is taken as umulhi(e, ceil(2^32 / gs)), exact
-        // for e and gs below 2^12 (gs = 1: the group is e itself).
         const uint32_t gs = static_cast<uint32_t>(E / a.n_group);
-        const uint32_t inv_gs = gs > 1u ? 0xffffffffu / gs + 1u : 0u;
-        uint32_t lmax = 0u;
+        uint32_t kept;
+        // An index's group n / d is taken as umulhi(n, ceil(2^32 / d)), exact for
+        // n and d below 2^12 (d = 1: the group is n itself).
+        auto group_of = [](uint32_t n, uint32_t d, uint32_t inv) { return d > 1u ? __umulhi(n, inv) : n; };
+        if (FULL && (gs & 3u) == 0u && m <= 4) {
+            // groups of whole chunks: each lane's chunk v lies in one group, so
+            // the lane stages the m largest of its 4 keys (entry 32 v + lane) and
+            // the group pass merges gs / 4 short lists instead of gs keys
+            auto stage = [&](auto mc) {
+                constexpr int M = decltype(mc)::value;
 #pragma unroll
-        for (int v = 0; v < NV; ++v)
+                for (int v = 0; v < NV; ++v) {
+                    uint32_t top[M];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint32_t e = static_cast<uint32_t>(v * 128 + lane4 + c);
-                const uint32_t g = gs > 1u ? __umulhi(e, inv_gs) : e;
-                const bool keep = e < static_cast<uint32_t>(E) && ((kept >> g) & 1u);
-                key[v][c] = keep ? key[v][c] : 0u;
-                lmax = max(lmax, key[v][c]);
+                    for (int i = 0; i < M; ++i) top[i] = 0u;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) top_insert(top, key[v][c]);
+#pragma unroll
+                    for (int i = 0; i < M; ++i) sk[(v * 32 + lane) * M + i] = top[i];
+                }
+                __syncwarp();
+                return group_kept_entries<M>(sk, a.n_group, static_cast<int>(gs >> 2), a.topk_group, m, lane);
+            };
+            if (m <= 1) kept = stage(std::integral_constant<int, 1>{});
+            else if (m <= 2) kept = stage(std::integral_constant<int, 2>{});
+            else kept = stage(std::integral_constant<int, 4>{});
+        } else {
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const int e0 = v * 128 + lane4;
+                if (whole(v)) {
+                    *reinterpret_cast<uint4*>(sk + e0) = make_uint4(key[v][0], key[v][1], key[v][2], key[v][3]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        if (inside(v, c)) sk[e0 + c] = key[v][c];
+                }
             }
+            __syncwarp();
+            if (m <= 1) kept = group_kept<1>(sk, E, a.n_group, a.topk_group, m, lane);
+            else if (m <= 2) kept = group_kept<2>(sk, E, a.n_group, a.topk_group, m, lane);
+            else if (m <= 4) kept = group_kept<4>(sk, E, a.n_group, a.topk_group, m, lane);
+            else kept = group_kept<8>(sk, E, a.n_group, a.topk_group, m, lane);
+        }
+        // the keys are still in registers: drop those of the groups not kept
+        uint32_t lmax = 0u;
+        if (FULL && (gs & 3u) == 0u) {
+            // a chunk's 4 keys share one group: one division per chunk
+            const uint32_t epg = gs >> 2;
+            const uint32_t inv = epg > 1u ? 0xffffffffu / epg + 1u : 0u;
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const bool keep = (kept >> group_of(static_cast<uint32_t>(v * 32 + lane), epg, inv)) & 1u;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    key[v][c] = keep ? key[v][c] : 0u;
+                    lmax = max(lmax, key[v][c]);
+                }
+            }
+        } else {
+            const uint32_t inv_gs = gs > 1u ? 0xffffffffu / gs + 1u : 0u;
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t e = static_cast<uint32_t>(v * 128 + lane4 + c);
+                    const bool keep = e < static_cast<uint32_t>(E) && ((kept >> group_of(e, gs, inv_gs)) & 1u);
+                    key[v][c] = keep ? key[v][c] : 0u;
+                    lmax = max(lmax, key[v][c]);
+                }
+        }
         lane_max = lmax;
         kmax = __reduce_max_sync(kFull, lmax);
         __syncwarp();  // the staged keys are read no more; the region may be reused
