@@ -30,6 +30,7 @@ import ctypes
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -87,12 +88,20 @@ def peaks() -> dict:
 FWD_SOURCES = ("common.cuh", "route.cuh", "route_wide.cuh", "internal.h", "fwd.cu")
 
 
+def _code_only(text: str) -> str:
+    """The source with its comments and blank lines taken out, so that the hash
+    follows the code a profile was taken on, not its commentary."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "top_gating_expert_row_gb300", "csrc")
     for f in FWD_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

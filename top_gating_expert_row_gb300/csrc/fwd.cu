@@ -5,6 +5,8 @@
 //   k_router_fwd     persistent grid, 8 warps per CTA, one token row per warp
 //                    at a time (TransformerEngine PR 3012, fused_topk_with_
 //                    score_function; also serves fused_score_for_moe_aux_loss)
+//   k_fused_tiny     T*topk <= 32 pairs: a warp per token, then one warp sorts
+//                    the pairs (a pair per lane) with no pass over all experts
 //   k_fused_decode   ONE CTA for T <= 16 tokens (T <= 64 for E <= 256, with 32
 //                    warps): warp t routes token t (and t + 32), then
 //                    the whole CTA histograms, scans and scatters the T*topk
