@@ -107,6 +107,15 @@ FUSED = [synth.decode(T) for T in synth.DECODE_TS] + [synth.decode_gpt_oss(T) fo
                    bias_range=0.1, block_m=8),
     synth.Workload("above_tiny_T3_e100_k11", 3, 100, 11, synth.SIGMOID, synth.F32, renorm=1, scaling=1.5,
                    bias_range=0.1, block_m=8),
+    # at most 128 pairs and 16 tokens: a warp per token, one warp ranks in four slots
+    synth.Workload("small_T1_e1024_k100", 1, 1024, 100, synth.SOFTMAX, synth.F32, renorm=1, block_m=16),
+    synth.Workload("small_T9_e256_k8_bm24", 9, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=24),
+    synth.Workload("small_T7_grouped_shared_bm48", 7, 384, 9, synth.SIGMOID, synth.BF16, renorm=1, scaling=2.827,
+                   n_group=8, topk_group=4, n_shared=1, bias_range=0.05, zipf_s=1.1, block_m=48),
+    synth.Workload("small_T16_e64_k8_bm1", 16, 64, 8, synth.SOFTMAX, synth.F32, renorm=1, block_m=1),
+    synth.Workload("small_T11_e100_k6_sigmoid", 11, 100, 6, synth.SIGMOID, synth.F32, renorm=1, scaling=1.5,
+                   bias_range=0.1, block_m=8),
+    synth.Workload("above_small_T16_e128_k9", 16, 128, 9, synth.SOFTMAX, synth.BF16, renorm=1, block_m=16),
     synth.Workload("fused32_T17", 17, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
     synth.Workload("fused32_T32_e256_k8", 32, 256, 8, synth.SOFTMAX, synth.BF16, renorm=1, block_m=32),
     synth.Workload("fused32_T24_e128_k4", 24, 128, 4, synth.SOFTMAX, synth.BF16, renorm=1, block_m=16),

@@ -155,6 +155,10 @@ int launch_fused_tiny_s0_d0(const RouteArgs&, const SortArgs&, int, bool, cudaSt
 int launch_fused_tiny_s0_d1(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
 int launch_fused_tiny_s1_d0(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
 int launch_fused_tiny_s1_d1(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
+int launch_fused_small_s0_d0(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
+int launch_fused_small_s0_d1(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
+int launch_fused_small_s1_d0(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
+int launch_fused_small_s1_d1(const RouteArgs&, const SortArgs&, int, bool, cudaStream_t);
 
 int launch_fwd(int score_fn, int in_dtype, const RouteArgs& a, int nv_idx, bool select, cudaStream_t st)
 {
@@ -186,6 +190,16 @@ int launch_fused_tiny(int score_fn, int in_dtype, const RouteArgs& a, const Sort
         return in_dtype ? launch_fused_tiny_s0_d1(a, s, nv_idx, select, st)
                         : launch_fused_tiny_s0_d0(a, s, nv_idx, select, st);
     return in_dtype ? launch_fused_tiny_s1_d1(a, s, nv_idx, select, st) : launch_fused_tiny_s1_d0(a, s, nv_idx, select, st);
+}
+
+int launch_fused_small(int score_fn, int in_dtype, const RouteArgs& a, const SortArgs& s, int nv_idx, bool select,
+                       cudaStream_t st)
+{
+    if (score_fn == kSoftmax)
+        return in_dtype ? launch_fused_small_s0_d1(a, s, nv_idx, select, st)
+                        : launch_fused_small_s0_d0(a, s, nv_idx, select, st);
+    return in_dtype ? launch_fused_small_s1_d1(a, s, nv_idx, select, st)
+                    : launch_fused_small_s1_d0(a, s, nv_idx, select, st);
 }
 
 // ---- launch overlap ---------------------------------------------------------------------------
@@ -748,6 +762,20 @@ int moe_router_fused_fwd_sort(const mr_router_params* p, const void* logits, int
         SortArgs s{sorted_token_ids, sorted_weights, expert_ids, num_tokens_post_pad, E_tot, block_m,
                    log2_if_pow2(block_m)};
         return from_cuda(launch_fused_tiny(p->score_fn, p->in_dtype, a, s, nv, decode_select, st));
+    }
+    // at most 128 pairs and 16 tokens: a warp per token, one warp ranks and scans
+    if (p->T >= 1 && p->T <= 16 && p->T * p->topk <= kFusedSmallPairs && kNvBuckets[nv] <= kRegisterMaxNv) {
+        RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, topk_idx, topk_w, status);
+        SortArgs s{sorted_token_ids, sorted_weights, expert_ids, num_tokens_post_pad, E_tot, block_m,
+                   log2_if_pow2(block_m)};
+        const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, decode_select, a.n_group > 0);
+        const size_t smem = static_cast<size_t>(L.bytes) * p->T + small_sort_layout(E_tot).bytes;
+        int dev = 0, maxsm = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return MR_ECUDA;
+        if (smem <= static_cast<size_t>(maxsm))
+            return from_cuda(launch_fused_small(p->score_fn, p->in_dtype, a, s, nv, decode_select, st));
     }
     if (p->T > 16 && p->T <= kFusedClusterMaxTokens && kNvBuckets[nv] <= kRegisterMaxNv) {
         RouteArgs a = route_args(p, logits, nullptr, nullptr, nullptr, topk_idx, topk_w, status);

@@ -7,6 +7,9 @@
 //                    score_function; also serves fused_score_for_moe_aux_loss)
 //   k_fused_tiny     T*topk <= 32 pairs: a warp per token, then one warp sorts
 //                    the pairs (a pair per lane) with no pass over all experts
+//   k_fused_small    T*topk <= 128 pairs, T <= 16: a warp per token, warp 0
+//                    ranks the pairs and scans the padded counts, the CTA
+//                    writes the sentinels
 //   k_fused_decode   ONE CTA for T <= 16 tokens (T <= 64 for E <= 256, with 32
 //                    warps): warp t routes token t (and t + 32), then
 //                    the whole CTA histograms, scans and scatters the T*topk
@@ -370,6 +373,114 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_fused_tiny(RouteArgs a, So
     if (lane == 0) *s.num_post_pad = static_cast<int32_t>(npp);
 }
 
+// Fused route + sort for 32 < T * topk <= 128 pairs, T <= 16: T warps route a
+// token each; warp 0 takes the pairs in four slots of 32 (pair 32 s + lane),
+// gives each its stable rank from a match on the expert ids within the slot
+// plus the count of its expert in the earlier slots (shared per-expert
+// counters the slot's leaders advance), and scans the experts' padded counts;
+// the CTA writes the sentinels, then warp 0 the pairs over them. Three block
+// barriers.
+template <int NV, bool SELECT, bool FULL>
+__global__ void __launch_bounds__(kFusedThreads, 1) k_fused_small(RouteArgs a, SortArgs s)
+{
+    pdl_trigger_small();
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nt = blockDim.x;
+    const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, SELECT, a.n_group > 0);
+    const int E_tot = s.E_tot;
+    const SmallSortLayout F = small_sort_layout(E_tot);
+    unsigned char* base = smem + static_cast<size_t>(a.T) * L.bytes;
+    int32_t* s_idx = reinterpret_cast<int32_t*>(base + F.idx);
+    float* s_w = reinterpret_cast<float*>(base + F.w);
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(base + F.cnt);
+    uint32_t* off = reinterpret_cast<uint32_t*>(base + F.off);
+    uint32_t* s_npp = reinterpret_cast<uint32_t*>(base + F.npp);
+    const int N = a.T * a.topk;
+    const uint32_t bm = static_cast<uint32_t>(s.block_m);
+    auto padded = [&](uint32_t c) {
+        return s.bm_shift >= 0 ? ((c + bm - 1u) >> s.bm_shift) << s.bm_shift : (c + bm - 1u) / bm * bm;
+    };
+    for (int e = tid; e < E_tot; e += nt) cnt[e] = 0u;
+    pdl_wait();
+    {
+        unsigned char* wsm = smem + static_cast<size_t>(warp) * L.bytes;
+        uint32_t warm = 0u;
+        const int tok = warp;
+        const float scale = route_row<kScore, InT, NV, SELECT, FULL>(a, tok, wsm, L, lane, warm);
+        const size_t o = static_cast<size_t>(tok) * a.topk;
+        const uint32_t* win_idx = reinterpret_cast<const uint32_t*>(wsm + L.win_idx);
+        const float* win_val = reinterpret_cast<const float*>(wsm + L.win_val);
+        for (int j = lane; j < a.topk; j += 32) {  // compact outputs, to shared and global
+            const bool routed = j < a.k_r;
+            const int32_t id = routed ? static_cast<int32_t>(win_idx[j]) : a.E + (j - a.k_r);
+            const float wv = routed ? __fmul_rn(win_val[j], scale) : a.shared_weight;
+            s_idx[o + j] = id;
+            s_w[o + j] = wv;
+            if (a.topk_idx) a.topk_idx[o + j] = id;
+            if (a.topk_w) a.topk_w[o + j] = wv;
+        }
+    }
+    __syncthreads();  // pairs in shared memory, counters zeroed
+    constexpr int kSlots = kFusedSmallPairs / 32;
+    int e_s[kSlots];
+    uint32_t rank_s[kSlots];
+    if (warp == 0) {
+        const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+        for (int sl = 0; sl < kSlots; ++sl) {
+            const int p = sl * 32 + lane;
+            const int e = p < N ? s_idx[p] : -1;
+            // ids outside [0, E_tot) (NaN rows) are left out
+            const bool valid = e >= 0 && e < E_tot;
+            const uint32_t key = valid ? static_cast<uint32_t>(e) : 0xffffffffu;
+            const uint32_t same = __match_any_sync(kFull, key);
+            const int leader = __ffs(same) - 1;
+            uint32_t b = 0u;
+            if (valid && lane == leader) {  // the expert's count in the earlier slots, advanced by this one's
+                b = cnt[e];
+                cnt[e] = b + static_cast<uint32_t>(__popc(same));
+            }
+            b = __shfl_sync(kFull, b, leader);
+            e_s[sl] = valid ? e : -1;
+            rank_s[sl] = b + static_cast<uint32_t>(__popc(same & lt));
+            __syncwarp();  // this slot's counts before the next slot reads them
+        }
+        // exclusive scan of the padded counts: lane l takes experts l*per ..
+        const int per = (E_tot + 31) >> 5;
+        const int e0 = lane * per, e1 = min(E_tot, e0 + per);
+        uint32_t local = 0u;
+        for (int e = e0; e < e1; ++e) local += padded(cnt[e]);
+        uint32_t run = warp_exclusive_scan(local, lane);
+        for (int e = e0; e < e1; ++e) {
+            off[e] = run;
+            run += padded(cnt[e]);
+        }
+        if (lane == 31) *s_npp = run;
+    }
+    __syncthreads();  // offsets and the padded total
+    const uint32_t npp = *s_npp;
+    for (uint32_t q = static_cast<uint32_t>(tid); q < npp; q += static_cast<uint32_t>(nt)) {
+        s.ids[q] = N;
+        if (s.w) s.w[q] = 0.0f;
+    }
+    __syncthreads();  // the sentinels before the pairs over them
+    if (warp == 0) {
+#pragma unroll
+        for (int sl = 0; sl < kSlots; ++sl) {
+            const int e = e_s[sl];
+            if (e < 0) continue;
+            const int p = sl * 32 + lane;
+            const uint32_t oe = off[e];
+            s.ids[oe + rank_s[sl]] = p;
+            if (s.w) s.w[oe + rank_s[sl]] = s_w[p];
+            if (rank_s[sl] == 0u)  // the expert's first pair writes its block ids
+                for (uint32_t q = oe; q < oe + padded(cnt[e]); q += bm)
+                    s.expert_ids[s.bm_shift >= 0 ? q >> s.bm_shift : q / bm] = e;
+        }
+        if (lane == 0) *s.num_post_pad = static_cast<int32_t>(npp);
+    }
+}
+
 // Fused route + sort in one launch of one thread-block cluster (cs CTAs of 32
 // warps): CTA r routes tokens [r*TP, min(T, (r+1)*TP)), a warp per token,
 // writes the compact outputs and keeps the pairs in shared memory, then the
@@ -448,6 +559,20 @@ ClusterFn cluster_kernel(int nv_idx)
         case 4: return k_fused_cluster<4, SELECT, FULL>;
         case 6: return k_fused_cluster<6, SELECT, FULL>;
         case 8: return k_fused_cluster<8, SELECT, FULL>;
+    }
+    return nullptr;
+}
+
+template <bool SELECT, bool FULL>
+FusedFn small_kernel(int nv_idx)
+{
+    switch (kNvBuckets[nv_idx]) {
+        case 1: return k_fused_small<1, SELECT, FULL>;
+        case 2: return k_fused_small<2, SELECT, FULL>;
+        case 3: return k_fused_small<3, SELECT, FULL>;
+        case 4: return k_fused_small<4, SELECT, FULL>;
+        case 6: return k_fused_small<6, SELECT, FULL>;
+        case 8: return k_fused_small<8, SELECT, FULL>;
     }
     return nullptr;
 }
@@ -582,6 +707,20 @@ int MR_CAT(launch_fused_tiny, MR_SUFFIX)(const RouteArgs& a, const SortArgs& s, 
     if (!f) return cudaErrorInvalidValue;
     const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, select, a.n_group > 0);
     const size_t smem = static_cast<size_t>(L.bytes) * a.T + 2 * kFusedTinyPairs * 4;
+    int err = ensure_smem(reinterpret_cast<const void*>(f), smem);
+    if (err != cudaSuccess) return err;
+    return launch_kernel(f, dim3(1), dim3(32 * a.T), smem, st, 0, a, s);
+}
+
+int MR_CAT(launch_fused_small, MR_SUFFIX)(const RouteArgs& a, const SortArgs& s, int nv_idx, bool select,
+                                          cudaStream_t st)
+{
+    const bool full = a.vec && a.E == 128 * kNvBuckets[nv_idx];
+    const FusedFn f = select ? (full ? small_kernel<true, true>(nv_idx) : small_kernel<true, false>(nv_idx))
+                             : (full ? small_kernel<false, true>(nv_idx) : small_kernel<false, false>(nv_idx));
+    if (!f) return cudaErrorInvalidValue;
+    const WarpLayout L = warp_layout(a.k_r, a.stop, a.E, select, a.n_group > 0);
+    const size_t smem = static_cast<size_t>(L.bytes) * a.T + small_sort_layout(s.E_tot).bytes;
     int err = ensure_smem(reinterpret_cast<const void*>(f), smem);
     if (err != cudaSuccess) return err;
     return launch_kernel(f, dim3(1), dim3(32 * a.T), smem, st, 0, a, s);

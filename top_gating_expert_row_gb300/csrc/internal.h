@@ -46,6 +46,27 @@ constexpr int kFusedWideMaxNv = 2;
 constexpr int kFusedWideMaxTokens = 64;
 // T * topk <= 32 pairs (rows of E <= 1024): T warps route, one warp sorts
 constexpr int kFusedTinyPairs = 32;
+// T * topk <= 128 pairs, T <= 16: T warps route, one warp ranks the pairs (up
+// to four per lane) and scans the experts' padded counts, the CTA writes the
+// sentinels
+constexpr int kFusedSmallPairs = 128;
+// shared memory of that kernel after the warp regions: pairs (ids, weights),
+// per-expert counts and offsets, the padded total
+struct SmallSortLayout {
+    int idx, w, cnt, off, npp, bytes;
+};
+__host__ __device__ inline SmallSortLayout small_sort_layout(int E_tot)
+{
+    SmallSortLayout F;
+    int o = 0;
+    F.idx = o; o += kFusedSmallPairs * 4;
+    F.w = o; o += kFusedSmallPairs * 4;
+    F.cnt = o; o += (E_tot * 4 + 15) / 16 * 16;
+    F.off = o; o += (E_tot * 4 + 15) / 16 * 16;
+    F.npp = o; o += 16;
+    F.bytes = o;
+    return F;
+}
 // whether moe_router_fused_fwd_sort runs as one launch for T tokens of row bucket nv
 inline bool fused_one_launch(int T, int nv_bucket)
 {
@@ -116,6 +137,8 @@ int launch_fused_decode(int score_fn, int in_dtype, const RouteArgs& a, const So
                         int nv_idx, bool select, cudaStream_t st);
 int launch_fused_tiny(int score_fn, int in_dtype, const RouteArgs& a, const SortArgs& s, int nv_idx,
                       bool select, cudaStream_t st);
+int launch_fused_small(int score_fn, int in_dtype, const RouteArgs& a, const SortArgs& s, int nv_idx,
+                       bool select, cudaStream_t st);
 // The fused call as one launch of one thread-block cluster (a warp per token);
 // cudaErrorNotSupported, with nothing launched, when no cluster fits.
 int launch_fused_cluster(int score_fn, int in_dtype, const RouteArgs& a, const SortArgs& s, int nv_idx,
