@@ -264,11 +264,13 @@ int moe_sort_noalloc(const int32_t* topk_idx, const float* topk_w, int T, int to
 
 /*
  * moe_router_fused_fwd_sort -- moe_router_fwd (compact outputs) followed by moe_sort
- * over E_tot = E + n_shared experts ([FLY] fused top-k + sorting). For
- * T <= MR_MAX_FUSED_TOKENS and E <= MR_MAX_FUSED_EXPERTS, and for
- * T <= MR_MAX_FUSED_TOKENS_SMALL_E and E <= MR_MAX_FUSED_EXPERTS_SMALL, it is ONE
- * launch of one CTA; above that (the pages report no gain from fusing beyond T = 16
- * and leave larger T open) it runs as the separate forward and sort launches.
+ * over E_tot = E + n_shared experts ([FLY] fused top-k + sorting). With rows of
+ * E <= MR_MAX_FUSED_EXPERTS it is ONE launch: of one CTA for T <= MR_MAX_FUSED_TOKENS
+ * (a warp per token; up to 128 pairs one warp sorts them), and of one thread-block
+ * cluster for MR_MAX_FUSED_TOKENS < T <= 512 where the device schedules such a cluster
+ * (else one CTA up to T <= MR_MAX_FUSED_TOKENS_SMALL_E when E <= MR_MAX_FUSED_EXPERTS_SMALL).
+ * Otherwise (the pages report no gain from fusing beyond T = 16 and leave larger T open)
+ * it runs as the separate forward and sort launches. Results are the same in every form.
  * topk_idx / topk_w are nullable (compact outputs written only when given). The
  * workspace (moe_router_fused_workspace_bytes, 0 for the one-launch sizes) holds
  * the compact outputs when those are NULL and the sort's scratch (0 bytes for the
