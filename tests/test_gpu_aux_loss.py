@@ -53,6 +53,20 @@ def test_aux_loss_and_counts_match_oracle(mr, orc, T, E, k, coeff):
     assert_close(grad, orc.aux_loss_bwd(T, ref_counts, k, coeff, N, 1.7), f"grad_probs T={T} E={E}")
 
 
+@pytest.mark.parametrize("T,E", [(70001, 16), (5000, 80), (3, 2304), (1030, 4096)], ids=lambda v: str(v))
+def test_counts_of_any_nonzero_byte(mr, orc, T, E):
+    """Token counts count every nonzero map byte once (values 1..255), over 64-column
+    slabs with a partial last slab, chunks of rows whose counts need more than 16
+    bits in all (T above 65535), and a handful of rows."""
+    g = torch.Generator().manual_seed(13)
+    vals = torch.randint(1, 256, (T, E), generator=g, dtype=torch.int32).to(torch.uint8)
+    keep = torch.rand(T, E, generator=g) < 0.3
+    rmap = torch.where(keep, vals, torch.zeros_like(vals)).contiguous()
+    counts = mr.tokens_per_expert(rmap.cuda())
+    torch.cuda.synchronize()
+    assert_equal(counts, orc.tokens_per_expert(rmap.numpy()), f"tokens_per_expert T={T} E={E}")
+
+
 def test_misaligned_rows_take_the_scalar_path(mr, orc):
     T, E, k = 500, 64, 4
     base = _probs(T * E + 1, 1).reshape(-1)

@@ -270,6 +270,96 @@ __global__ void __launch_bounds__(kAuxThreads) k_tokens_per_expert(const uint8_t
     }
 }
 
+// Counts of rows with 16-byte aligned map rows: a CTA covers a 64-column slab of
+// a chunk of rows; lane (r, c) of a warp (r = lane / 4, c = lane % 4) loads the
+// 16 bytes of columns 16c .. 16c+15 of row 8i + r, so one warp load covers 8
+// rows and every row's slab is one 64-byte segment. The lanes' byte-wise counts
+// are added across the 8 row lanes by shuffles (two counts per 32-bit word),
+// across the warps in shared memory, and once per column into `out`: a chunk of
+// 1024 rows or more per CTA, so a column takes few atomics.
+__global__ void __launch_bounds__(kAuxThreads) k_tokens_per_expert_slab(const uint8_t* map, int T, int E,
+                                                                        int rows_per_chunk, int32_t* out)
+{
+    pdl_trigger_small();
+    pdl_wait();
+    __shared__ uint32_t red[kAuxWarps][64];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = lane >> 2, c = lane & 3;
+    const int col0 = blockIdx.x * 64 + c * 16;
+    const bool live = col0 < E;  // E is a multiple of 16: a lane's 16 columns are all in or all out
+    const int t0 = blockIdx.y * rows_per_chunk;
+    const int t1 = min(T, t0 + rows_per_chunk);
+    uint32_t cnt[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) cnt[i] = 0u;
+    uint32_t packed[4] = {0u, 0u, 0u, 0u};  // byte-wide counters, flushed before any reaches 256
+    int held = 0;
+    auto flush = [&]() {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) cnt[4 * i + b] += (packed[i] >> (8 * b)) & 0xffu;
+            packed[i] = 0u;
+        }
+        held = 0;
+    };
+    auto add = [&](const uint4& q) {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t f = w[i] | (w[i] >> 4);
+            f |= f >> 2;
+            f |= f >> 1;
+            packed[i] += f & 0x01010101u;
+        }
+    };
+    const uint8_t* base = map + col0;
+    // rows t0 + 8 (warp + 8 j) + r: four loads in flight per lane
+    constexpr int kStep = 8 * kAuxWarps;  // rows per CTA-wide load
+    int t = t0 + 8 * warp + r;
+    if (live) {
+        for (; t + 3 * kStep < t1; t += 4 * kStep) {
+            uint4 q[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                q[u] = __ldcs(reinterpret_cast<const uint4*>(base + static_cast<size_t>(t + u * kStep) * E));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) add(q[u]);
+            held += 4;
+            if (held > 248) flush();
+        }
+        for (; t < t1; t += kStep) {
+            add(__ldcs(reinterpret_cast<const uint4*>(base + static_cast<size_t>(t) * E)));
+            if (++held > 248) flush();
+        }
+    }
+    flush();
+    // the 8 row lanes of each column group: counts of one chunk stay below 2^16,
+    // so two travel in one word
+    uint32_t two[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) two[i] = cnt[2 * i] | (cnt[2 * i + 1] << 16);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) two[i] += __shfl_xor_sync(kFull, two[i], o);
+    if (r == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            red[warp][c * 16 + 2 * i] = two[i] & 0xffffu;
+            red[warp][c * 16 + 2 * i + 1] = two[i] >> 16;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < 64) {
+        const int col = blockIdx.x * 64 + threadIdx.x;
+        uint32_t sum = 0u;
+#pragma unroll
+        for (int w = 0; w < kAuxWarps; ++w) sum += red[w][threadIdx.x];
+        if (col < E && sum) atomicAdd(reinterpret_cast<unsigned int*>(out + col), sum);
+    }
+}
+
 }  // namespace
 
 int aux_chunks(long long T)
@@ -321,11 +411,25 @@ int launch_tokens_per_expert(const uint8_t* map, int T, int E, int32_t* out, cud
 {
     cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(E) * sizeof(int32_t), st);
     if (e != cudaSuccess || T <= 0) return e;
+    const int vec = (E % 16 == 0) && (reinterpret_cast<uintptr_t>(map) % 16 == 0);
+    if (vec) {
+        // 64-column slabs, chunks of at least 1024 rows and at most 65535 (a
+        // chunk's counts stay below 2^16), about four CTAs per SM in all
+        const int S = (E + 63) / 64;
+        int dev = 0, sms = 152;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const long long want = std::max<long long>(1, (4LL * sms + S - 1) / S);
+        const long long by_rows = std::max<long long>(1, (static_cast<long long>(T) + 1023) / 1024);
+        const long long need = (static_cast<long long>(T) + 65534) / 65535;
+        const int R = static_cast<int>(std::max(need, std::min(want, by_rows)));
+        const int rows = static_cast<int>((static_cast<long long>(T) + R - 1) / R);
+        return launch_kernel(k_tokens_per_expert_slab, dim3(S, R), dim3(kAuxThreads), 0, st, 0, map, T, E, rows,
+                             out);
+    }
     constexpr int kRows = 128;
     const int R = std::min((T + kRows - 1) / kRows, 8192);
     const int rows = (T + R - 1) / R;
     const int S = (E + 511) / 512;
-    const int vec = (E % 16 == 0) && (reinterpret_cast<uintptr_t>(map) % 16 == 0);
     return launch_kernel(k_tokens_per_expert, dim3(S, R), dim3(kAuxThreads), 0, st, 0, map, T, E, rows, vec, out);
 }
 
