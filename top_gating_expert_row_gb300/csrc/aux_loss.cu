@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kAuxThreads) k_tokens_per_expert(const uint8_t
 // rows and every row's slab is one 64-byte segment. The lanes' byte-wise counts
 // are added across the 8 row lanes by shuffles (two counts per 32-bit word),
 // across the warps in shared memory, and once per column into `out`: a chunk of
-// 1024 rows or more per CTA, so a column takes few atomics.
+// 512 rows or more per CTA, so a column takes few atomics.
 __global__ void __launch_bounds__(kAuxThreads) k_tokens_per_expert_slab(const uint8_t* map, int T, int E,
                                                                         int rows_per_chunk, int32_t* out)
 {
@@ -314,18 +314,18 @@ __global__ void __launch_bounds__(kAuxThreads) k_tokens_per_expert_slab(const ui
         }
     };
     const uint8_t* base = map + col0;
-    // rows t0 + 8 (warp + 8 j) + r: four loads in flight per lane
+    // rows t0 + 8 (warp + 8 j) + r: eight loads in flight per lane
     constexpr int kStep = 8 * kAuxWarps;  // rows per CTA-wide load
     int t = t0 + 8 * warp + r;
     if (live) {
-        for (; t + 3 * kStep < t1; t += 4 * kStep) {
-            uint4 q[4];
+        for (; t + 7 * kStep < t1; t += 8 * kStep) {
+            uint4 q[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < 8; ++u)
                 q[u] = __ldcs(reinterpret_cast<const uint4*>(base + static_cast<size_t>(t + u * kStep) * E));
 #pragma unroll
-            for (int u = 0; u < 4; ++u) add(q[u]);
-            held += 4;
+            for (int u = 0; u < 8; ++u) add(q[u]);
+            held += 8;
             if (held > 248) flush();
         }
         for (; t < t1; t += kStep) {
@@ -413,13 +413,13 @@ int launch_tokens_per_expert(const uint8_t* map, int T, int E, int32_t* out, cud
     if (e != cudaSuccess || T <= 0) return e;
     const int vec = (E % 16 == 0) && (reinterpret_cast<uintptr_t>(map) % 16 == 0);
     if (vec) {
-        // 64-column slabs, chunks of at least 1024 rows and at most 65535 (a
+        // 64-column slabs, chunks of at least 512 rows and at most 65535 (a
         // chunk's counts stay below 2^16), about four CTAs per SM in all
         const int S = (E + 63) / 64;
         int dev = 0, sms = 152;
         if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         const long long want = std::max<long long>(1, (4LL * sms + S - 1) / S);
-        const long long by_rows = std::max<long long>(1, (static_cast<long long>(T) + 1023) / 1024);
+        const long long by_rows = std::max<long long>(1, (static_cast<long long>(T) + 511) / 512);
         const long long need = (static_cast<long long>(T) + 65534) / 65535;
         const int R = static_cast<int>(std::max(need, std::min(want, by_rows)));
         const int rows = static_cast<int>((static_cast<long long>(T) + R - 1) / R);
